@@ -1,0 +1,175 @@
+"""Seeded synthetic inputs for the QSA indexer step.
+
+This module only draws inputs (numpy PCG64 streams, platform independent); it
+holds none of the indexer's arithmetic.  Both the CUDA path and the CPU oracle
+are fed the very same bytes from here.
+
+Shapes follow the workloads the pages describe: a key cache of one FP16 index
+key (dim 128) per compressed position, compress ratio 4, 64-token pages of 16
+positions, an int32 block table per request, and query rows that each see the
+compressed positions completed before them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+COMPRESS_RATIO = 4
+PAGE_POSITIONS = 16          # 64-token pages at compress ratio 4
+HEAD_DIM = 128
+
+
+@dataclass
+class Workload:
+    name: str
+    q: np.ndarray             # float16 [R, H, D]
+    w: np.ndarray             # float32 [R, H]
+    k_cache: np.ndarray       # float16 [num_pages, PAGE_POSITIONS, D]
+    block_table: np.ndarray   # int32 [num_reqs, max_pages]
+    row_req: np.ndarray       # int32 [R]
+    row_visible: np.ndarray   # int32 [R]
+    row_token: np.ndarray     # int64 [R] 0-based token position of each query row
+    req_positions: np.ndarray  # int32 [num_reqs] compressed positions stored per request
+    k: int
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def ld(self) -> int:
+        """Longest row a request's block table can address (logit row stride)."""
+        return int(self.block_table.shape[1]) * int(self.k_cache.shape[1])
+
+    @property
+    def visible_pairs(self) -> int:
+        return int(np.sum(self.row_visible.astype(np.int64)))
+
+
+def _values(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
+    if dist == "int4":
+        return rng.integers(-4, 5, size=shape).astype(np.float16)
+    if dist == "tern":
+        return rng.integers(-1, 2, size=shape).astype(np.float16)
+    if dist == "gauss":
+        return (rng.standard_normal(size=shape, dtype=np.float32)
+                / np.float32(np.sqrt(128.0))).astype(np.float16)
+    if dist == "zero":
+        return np.zeros(shape, dtype=np.float16)
+    raise ValueError(dist)
+
+
+def _weights(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
+    if dist == "int4":
+        return rng.choice(np.array([0.25, 0.5, 1.0, 2.0], dtype=np.float32), size=shape)
+    if dist in ("tern", "ones"):
+        return np.ones(shape, dtype=np.float32)
+    if dist == "gauss":
+        return rng.random(size=shape, dtype=np.float32)
+    if dist == "zero":
+        return np.zeros(shape, dtype=np.float32)
+    raise ValueError(dist)
+
+
+def make_workload(name: str, *, seed: int, ctx_tokens, rows_per_req, k: int, heads: int = 4,
+                  head_dim: int = HEAD_DIM, page_positions: int = PAGE_POSITIONS,
+                  dist: str = "gauss", wdist: str | None = None, shuffle_pages: bool = True,
+                  visibility: str = "pages", extra_pages: int = 0) -> Workload:
+    """Build one batch.
+
+    ctx_tokens[b]: tokens in request b's context; the request stores
+    ctx // 4 compressed positions.  rows_per_req[b]: query rows of request b,
+    the last rows of its context (prefill chunk / decode token).
+    visibility: "pages" -> V = (t+1) // 4 (a position is stored once its fourth
+    token exists); "plus_one" -> V = t // 4 + 1 (the alternative reading).
+    """
+    rng = np.random.default_rng(seed)
+    ctx_tokens = [int(c) for c in ctx_tokens]
+    rows_per_req = [int(n) for n in rows_per_req]
+    B = len(ctx_tokens)
+    assert len(rows_per_req) == B
+    P = [c // COMPRESS_RATIO for c in ctx_tokens]
+    pages = [-(-p // page_positions) for p in P]
+    max_pages = max(1, max(pages) + extra_pages)
+    num_pages = max(1, sum(pages))
+    phys = rng.permutation(num_pages).astype(np.int32) if shuffle_pages else \
+        np.arange(num_pages, dtype=np.int32)
+    bt = np.full((B, max_pages), -1, dtype=np.int32)
+    off = 0
+    for b in range(B):
+        bt[b, :pages[b]] = phys[off:off + pages[b]]
+        off += pages[b]
+    k_cache = _values(rng, (num_pages, page_positions, head_dim), dist)
+    row_req, row_tok = [], []
+    for b in range(B):
+        n = rows_per_req[b]
+        row_req += [b] * n
+        row_tok += list(range(ctx_tokens[b] - n, ctx_tokens[b]))
+    R = len(row_req)
+    q = _values(rng, (R, heads, head_dim), dist)
+    w = _weights(rng, (R, heads), wdist or dist)
+    row_tok = np.asarray(row_tok, dtype=np.int64)
+    if visibility == "pages":
+        vis = (row_tok + 1) // COMPRESS_RATIO
+    elif visibility == "plus_one":
+        vis = row_tok // COMPRESS_RATIO + 1
+    else:
+        raise ValueError(visibility)
+    req_arr = np.asarray(row_req, dtype=np.int32)
+    vis = np.minimum(vis, np.asarray(P, dtype=np.int64)[req_arr]).astype(np.int32)
+    return Workload(name=name, q=q, w=w, k_cache=k_cache, block_table=bt, row_req=req_arr,
+                    row_visible=vis, row_token=row_tok, req_positions=np.asarray(P, np.int32),
+                    k=int(k), meta=dict(seed=seed, dist=dist, shuffle=shuffle_pages,
+                                        visibility=visibility))
+
+
+# The five synthetic batches (sizes as in the kernel-bench description of the
+# pages plus the decode, tie-stress and long-prefill shapes built around it).
+
+def tiny(seed: int = 0) -> Workload:
+    """1 request, 64 rows at the end of a 1,024-token context, k 64, integer data."""
+    return make_workload("tiny_1x64rows_ctx1024_k64_int", seed=seed, ctx_tokens=[1024],
+                         rows_per_req=[64], k=64, dist="int4", shuffle_pages=False)
+
+
+def bench(seed: int = 1, k: int = 2048, ctx: int = 184_320, visibility: str = "pages") -> Workload:
+    """Last 1,616-row chunk of a 184,320-token context (46,080 positions), k 2,048."""
+    return make_workload(f"prefill_1x1616rows_ctx{ctx}_k{k}", seed=seed, ctx_tokens=[ctx],
+                         rows_per_req=[1616], k=k, dist="gauss", shuffle_pages=False,
+                         visibility=visibility)
+
+
+def decode(seed: int = 2, num_reqs: int = 64) -> Workload:
+    """64 requests x 1 row, contexts uniform in [8,192, 131,072] tokens, k 2,048."""
+    rng = np.random.default_rng(10_000 + seed)
+    ctx = rng.integers(8192, 131072, size=num_reqs, endpoint=True)
+    return make_workload(f"decode_{num_reqs}x1row_ctx8k-128k_k2048", seed=seed, ctx_tokens=ctx,
+                         rows_per_req=[1] * num_reqs, k=2048, dist="gauss", shuffle_pages=True)
+
+
+def tie_stress(seed: int = 3) -> Workload:
+    """8 requests x 256 rows at the end of 32,768 tokens, ternary data, w = 1, k 512."""
+    return make_workload("ties_8x256rows_ctx32768_k512_tern", seed=seed, ctx_tokens=[32768] * 8,
+                         rows_per_req=[256] * 8, k=512, dist="tern", shuffle_pages=True)
+
+
+def long_prefill(seed: int = 4) -> Workload:
+    """4 requests x 4,096 rows at the end of 131,072 tokens (32,768 positions), k 2,048."""
+    return make_workload("prefill_4x4096rows_ctx131072_k2048", seed=seed,
+                         ctx_tokens=[131072] * 4, rows_per_req=[4096] * 4, k=2048,
+                         dist="gauss", shuffle_pages=True)
+
+
+CONFIGS = {
+    "tiny": tiny,
+    "bench": bench,
+    "decode": decode,
+    "ties": tie_stress,
+    "long": long_prefill,
+}
