@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the QSA indexer step (score + exact top-k) on GB300.
+
+One step = one qsa_select_paged_tokens call over one batch, inputs resident
+in HBM.  Default workload: the last 1,616-row prefill chunk of a
+184,320-token context (46,080 compressed positions, 4 heads x 128, top-2,048,
+64-token pages).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (the only reference implementation of
+this step) on the host cores, on a bounded sample of rows per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_attention_select_gb300 import workloads as W  # noqa: E402
+
+METRIC = "indexer rows/s (score + exact top-k) and % of roofline on 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(key)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if v is not None:
+                    out[key] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                out["source"] = "measured"
+                return out
+        except Exception:
+            pass
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def algorithmic(wl):
+    """Scoring FLOPs and compulsory bytes of one step (per the step's definition)."""
+    pairs = wl.visible_pairs
+    H, D = wl.heads, 128
+    flops = 2.0 * H * D * pairs
+    P = wl.k_cache.shape[1]
+    pages = int(np.sum((wl.req_positions.astype(np.int64) + P - 1) // P))
+    key_bytes = pages * P * D * 2
+    q_bytes = wl.q.nbytes + wl.w.nbytes + wl.row_req.nbytes + wl.row_visible.nbytes
+    logit_bytes = 4 * pairs
+    idx_bytes = wl.rows * wl.k * 4
+    return dict(flops=flops, key_bytes=key_bytes, q_bytes=q_bytes, logit_bytes=logit_bytes,
+                idx_bytes=idx_bytes, bytes=key_bytes + q_bytes + logit_bytes + idx_bytes,
+                pairs=pairs)
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_rows_per_s(wl, nrows: int, threads: int = 0):
+    """Time the oracle (as it stands) on the first nrows rows of the workload."""
+    import oracle
+    rows = np.linspace(0, wl.rows - 1, num=min(nrows, wl.rows)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.select_paged_tokens(wl.q[rows], wl.w[rows], wl.k_cache, wl.block_table,
+                               wl.row_req[rows], wl.row_visible[rows], wl.k, ld=wl.ld,
+                               nthreads=threads)
+    dt = time.perf_counter() - t0
+    return len(rows) / dt, len(rows), dt
+
+
+def cpu_baseline(wl, budget_s: float = 12.0):
+    import oracle
+    cores = oracle.max_threads()
+    # calibrate on a handful of rows, then size the sample to the budget
+    rps, n, dt = oracle_rows_per_s(wl, max(cores, 4))
+    n2 = int(min(wl.rows, max(n, rps * budget_s * 0.8)))
+    if n2 > n:
+        rps, n, dt = oracle_rows_per_s(wl, n2)
+    return {"value": rps, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {wl.rows} rows of {wl.name} (evenly spaced), all visible "
+                      f"positions each, {dt:.1f} s on {cores} threads"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    wl = W.CONFIGS[args.workload]()
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    per_step = max(4, 2 * cores)
+    rps0, _, dt0 = oracle_rows_per_s(wl, per_step)
+    # keep the whole --steps/--warmup run within a few minutes
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    if dt0 > budget:
+        per_step = max(1, int(per_step * budget / dt0))
+    for _ in range(args.warmup):
+        oracle_rows_per_s(wl, per_step)
+    times, rows = [], 0
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        _, n, dt = oracle_rows_per_s(wl, per_step)
+        times.append(dt)
+        rows += n
+    total = time.perf_counter() - t_all
+    value = rows / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "k": wl.k, "heads": wl.heads,
+                   "sample_rows_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} evenly spaced rows of {wl.rows} per step"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    from block_sparse_attention_select_gb300 import qsa
+
+    qsa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = W.CONFIGS[args.workload]()
+    alg = algorithmic(wl)
+    peaks = load_peaks()
+
+    q = torch.from_numpy(wl.q).to(dev)
+    w = torch.from_numpy(wl.w).to(dev)
+    rr = torch.from_numpy(wl.row_req).to(dev)
+    rv = torch.from_numpy(wl.row_visible).to(dev)
+    keys = qsa.PagedKeys(torch.from_numpy(wl.k_cache).to(dev), torch.from_numpy(wl.block_table).to(dev))
+    out_idx = torch.empty((wl.rows, wl.k), dtype=torch.int32, device=dev)
+    out_val = torch.empty((wl.rows, wl.k), dtype=torch.float32, device=dev)
+    wsb = qsa.alloc_workspace(wl.rows, keys.max_len, wl.k, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    qsa.set_config(qsa.QSA_CFG_PATH, {"auto": 0, "dense": 1, "filter": 2}[args.path])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qsa.select_paged_tokens(q, w, keys, rr, rv, wl.k, out_idx, out_val, wsb, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert qsa.get_device_status() == qsa.QSA_OK
+    launches_per_step = qsa.last_launch_count()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    qsa.set_config(qsa.QSA_CFG_KERNEL_TIMING, 1)
+    qsa.kernel_times()                                   # drop anything pending
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()                                     # L2 flushed between steps
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    kt = qsa.kernel_times()
+    qsa.set_config(qsa.QSA_CFG_KERNEL_TIMING, 0)
+    clk = clocks.stop()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, ws)
+    value = wl.rows * ws / (ms / 1e3)
+
+    # dominant kernel: the scorer launch with the largest total time
+    dom = max(kt.items(), key=lambda kv: kv[1][0])
+    dom_name, (dom_ms_total, dom_n) = dom
+    dom_ms = dom_ms_total / max(1, dom_n)
+    if dom_name.startswith("score"):
+        bound, unit = "tensor", "TFLOP/s"
+        work = alg["flops"] * (1.0 / 16 if dom_name == "score_sample" else 1.0)
+        achieved = work / (dom_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]          # burst figure: the kernel runs for microseconds
+    else:
+        bound, unit = "hbm", "GB/s"
+        work = alg["logit_bytes"] + alg["idx_bytes"]
+        achieved = work / (dom_ms / 1e3) / 1e9
+        peak = peaks["hbm_gbs"]
+    t_flop = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_mem = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_flop, t_mem)
+    roof_traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            tr = json.load(open(tr_path))
+            ent = tr.get(wl.name, {}).get(dom_name)
+            if ent and ent.get("kernel_rev") == kernel_revision():
+                roof_traffic = ent["bytes_per_launch"]
+        except Exception:
+            roof_traffic = None
+
+    # end to end through the public API: host inputs in, host result out
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, wl, qsa, keys, stream, dev)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_baseline(wl)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "positions_max": int(wl.row_visible.max()),
+                   "visible_pairs": alg["pairs"], "k": wl.k, "heads": wl.heads, "head_dim": 128,
+                   "page_positions": int(wl.k_cache.shape[1]), "path": args.path,
+                   "l2": "flushed between steps (512 MiB write)",
+                   "accumulate": "f32", "median_ms": statistics.median(step_ms)},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": roof_traffic, "kernel": dom_name,
+                     "kernel_ms": dom_ms, "peak_source": peaks["source"]},
+        "step_roofline": {"t_roof_us": t_roof * 1e6, "t_flop_us": t_flop * 1e6,
+                          "t_mem_us": t_mem * 1e6, "frac": t_roof / (ms / 1e3),
+                          "gflop": alg["flops"] / 1e9, "mbytes": alg["bytes"] / 1e6,
+                          "peak_source": peaks["source"]},
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kt.items()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def kernel_revision():
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "block_sparse_attention_select_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def measure_e2e(args, wl, qsa, keys_dev, stream, dev):
+    import torch
+    host = {n: torch.from_numpy(getattr(wl, n)).pin_memory()
+            for n in ("q", "w", "row_req", "row_visible", "k_cache", "block_table")}
+    d = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_idx = torch.empty((wl.rows, wl.k), dtype=torch.int32, device=dev)
+    out_host = torch.empty((wl.rows, wl.k), dtype=torch.int32).pin_memory()
+    wsb = qsa.alloc_workspace(wl.rows, keys_dev.max_len, wl.k, dev)
+    keys = qsa.PagedKeys(d["k_cache"], d["block_table"])
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for n in host:
+            d[n].copy_(host[n], non_blocking=True)
+        qsa.select_paged_tokens(d["q"], d["w"], keys, d["row_req"], d["row_visible"], wl.k,
+                                out_idx, None, wsb, stream, with_values=False)
+        out_host.copy_(out_idx, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        one()
+    n = max(5, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t0) / n
+    return {"value": wl.rows / dt, "unit": "rows/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(W.CONFIGS), default="bench")
+    ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,540 @@
+// C ABI of the QSA indexer library: argument checks, workspace layout, tensor
+// maps, path choice and the launch sequence.  Declarations: include/qsa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/qsa.h"
+#include "qsa_internal.h"
+
+namespace {
+
+using namespace qsa;
+
+__device__ uint32_t g_device_status;   // one per device: error bits recorded by the kernels
+
+constexpr int MAX_DEVICES = 64;
+constexpr float OVERSAMPLE = 1.5f;     // expected candidates per row / k on the filter path
+
+struct DeviceInfo {
+    bool probed = false;
+    bool usable = false;
+    int sms = 0;
+    uint32_t *status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[MAX_DEVICES];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int64_t g_cfg_path = 0;
+uint64_t g_wait_ns = 2000000000ull;
+thread_local int32_t g_launches = 0;
+
+// Optional per-launch CUDA-event timing (test / benchmark instrument).
+enum Kind { K_PLAN = 0, K_SCORE_LOGITS, K_SCORE_SAMPLE, K_SCORE_FILTER, K_SCORE_FALLBACK,
+            K_SEL_DENSE, K_SEL_THRESH, K_SEL_CAND, K_SEL_FLAGGED, K_PAD, K_KINDS };
+struct Pending { cudaEvent_t a, b; int kind; };
+bool g_timing = false;
+std::vector<Pending> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Runs `launch` (returns cudaError_t as int), bracketed by events when timing.
+template <typename F>
+int timed(int kind, void *stream, F &&launch)
+{
+    if (!g_timing) return launch();
+    std::lock_guard<std::mutex> lk(g_mu);
+    Pending p{take_event(), take_event(), kind};
+    cudaEventRecord(p.a, static_cast<cudaStream_t>(stream));
+    int rc = launch();
+    cudaEventRecord(p.b, static_cast<cudaStream_t>(stream));
+    g_pending.push_back(p);
+    return rc;
+}
+
+qsa_status from_status_bits(uint32_t bits)
+{
+    if (bits & ST_TIMEOUT) return QSA_ERR_TIMEOUT;
+    if (bits & ST_BAD_PAGE) return QSA_ERR_BAD_PAGE;
+    if (bits & ST_BAD_ROW) return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
+qsa_status device_info(DeviceInfo **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return QSA_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.probed) {
+        d.probed = true;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        void *sym = nullptr;
+        // the kernels are built for sm_103a only
+        d.usable = (major == 10 && minor == 3) &&
+                   cudaGetSymbolAddress(&sym, g_device_status) == cudaSuccess && d.sms > 0;
+        d.status = static_cast<uint32_t *>(sym);
+        if (d.usable && !g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) == cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        if (!g_encode) d.usable = false;
+        cudaGetLastError();
+    }
+    if (!d.usable) return QSA_ERR_NO_DEVICE;
+    *out = &d;
+    return QSA_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int32_t pow2_floor(double x)
+{
+    int32_t p = 1;
+    while (p * 2 <= x) p *= 2;
+    return p;
+}
+
+int32_t pow2_ceil(int32_t x)
+{
+    int32_t p = 1;
+    while (p < x) p *= 2;
+    return p;
+}
+
+// Sampled-threshold filter parameters for a top-k of k over rows of up to max_len.
+struct FilterShape {
+    int32_t stride;     // sample every stride-th key tile
+    int32_t cap;        // candidate slots per row
+    int64_t sample_ld;  // columns of the sample matrix
+};
+
+FilterShape filter_shape(int64_t max_len, int32_t k)
+{
+    FilterShape f;
+    f.stride = std::max(1, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
+    f.cap = 2 * k + 2048;
+    const int64_t tiles = (max_len + TILE_M - 1) / TILE_M;
+    f.sample_ld = std::max<int64_t>(TILE_M, (tiles + f.stride - 1) / f.stride * TILE_M);
+    return f;
+}
+
+bool use_filter(int64_t max_len, int32_t k)
+{
+    if (g_cfg_path == 1) return false;
+    if (g_cfg_path == 2) return true;
+    const FilterShape f = filter_shape(max_len, k);
+    return f.stride >= 4 && max_len >= 8LL * k;
+}
+
+struct Layout {
+    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, cnt, flag, cand;
+    size_t total;
+};
+
+Layout layout(int32_t R, int64_t ld, int32_t k)
+{
+    Layout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = up(o + bytes, 256); return at; };
+    L.plan = take(sizeof(Plan));
+    L.row_vis = take(sizeof(int32_t) * R);
+    L.groups = take(sizeof(Group) * R);
+    L.item_prefix = take(sizeof(int32_t) * (static_cast<size_t>(R) + 1));
+    L.sample_prefix = take(sizeof(int32_t) * (static_cast<size_t>(R) + 1));
+    L.logits = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(ld));
+    const FilterShape f = filter_shape(ld, std::max(k, 1));
+    L.sample = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(f.sample_ld));
+    L.tau = take(sizeof(float) * R);
+    L.cnt = take(sizeof(int32_t) * R);
+    L.flag = take(sizeof(int32_t) * R);
+    L.cand = take(sizeof(uint2) * static_cast<size_t>(R) * static_cast<size_t>(f.cap));
+    L.total = o;
+    return L;
+}
+
+qsa_status launch_rc(int rc)
+{
+    if (rc == 0) { ++g_launches; return QSA_OK; }
+    return QSA_ERR_LAUNCH;
+}
+
+qsa_status make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(HEAD_DIM * 2)};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QSA_OK : QSA_ERR_INVALID_ARG;
+}
+
+bool supported_heads(int32_t H) { return H == 1 || H == 2 || H == 4 || H == 8; }
+
+qsa_status check_keys(const qsa_paged_keys *keys)
+{
+    if (!keys || !keys->k_cache || !keys->block_table) return QSA_ERR_INVALID_ARG;
+    if (keys->num_pages < 1 || keys->num_reqs < 1 || keys->max_pages_per_req < 1)
+        return QSA_ERR_INVALID_ARG;
+    if (keys->head_dim != HEAD_DIM) return QSA_ERR_UNSUPPORTED;
+    const int32_t P = keys->page_positions;
+    if (P < 8 || P > 256 || (P & (P - 1)) != 0) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(keys->num_pages) * P >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(keys->max_pages_per_req) * P >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    if (!aligned(keys->k_cache, 16)) return QSA_ERR_INVALID_ARG;
+    return QSA_OK;
+}
+
+// Shared prologue of the two scoring calls: plan + tensor maps.
+struct ScoreSetup {
+    Layout L;
+    uint8_t *ws;
+    CUtensorMap tq, tk;
+    ScoreParams sp;
+};
+
+qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
+                       const qsa_paged_keys *keys, const int32_t *row_req, const int32_t *row_visible,
+                       int64_t ld, int64_t max_len, int32_t k, int32_t sample_stride, void *ws,
+                       size_t ws_bytes, DeviceInfo *d, void *stream)
+{
+    s.L = layout(rows, ld, k);
+    if (!ws || ws_bytes < s.L.total) return QSA_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return QSA_ERR_INVALID_ARG;
+    s.ws = static_cast<uint8_t *>(ws);
+    qsa_status st = make_tmap(&s.tq, q, static_cast<uint64_t>(rows) * H, N_MAX);
+    if (st != QSA_OK) return st;
+    st = make_tmap(&s.tk, keys->k_cache,
+                   static_cast<uint64_t>(keys->num_pages) * keys->page_positions,
+                   static_cast<uint32_t>(std::min(keys->page_positions, TILE_M)));
+    if (st != QSA_OK) return st;
+    auto at = [&](size_t off) { return s.ws + off; };
+    st = launch_rc(timed(K_PLAN, stream, [&] {
+        return launch_plan(row_req, row_visible, rows, H, keys->num_reqs, max_len, sample_stride,
+                           reinterpret_cast<int32_t *>(at(s.L.row_vis)),
+                           reinterpret_cast<Group *>(at(s.L.groups)),
+                           reinterpret_cast<int32_t *>(at(s.L.item_prefix)),
+                           reinterpret_cast<int32_t *>(at(s.L.sample_prefix)),
+                           reinterpret_cast<Plan *>(at(s.L.plan)), d->status, stream);
+    }));
+    if (st != QSA_OK) return st;
+    ScoreParams &p = s.sp;
+    std::memset(&p, 0, sizeof(p));
+    p.w = w;
+    p.row_vis = reinterpret_cast<const int32_t *>(at(s.L.row_vis));
+    p.groups = reinterpret_cast<const Group *>(at(s.L.groups));
+    p.item_prefix = reinterpret_cast<const int32_t *>(at(s.L.item_prefix));
+    p.sample_prefix = reinterpret_cast<const int32_t *>(at(s.L.sample_prefix));
+    p.plan = reinterpret_cast<const Plan *>(at(s.L.plan));
+    p.block_table = keys->block_table;
+    p.max_pages = keys->max_pages_per_req;
+    p.num_pages = keys->num_pages;
+    p.page_pos = keys->page_positions;
+    p.page_box = std::min(keys->page_positions, TILE_M);
+    p.H = H;
+    p.R = rows;
+    p.sample_stride = sample_stride;
+    p.status = d->status;
+    p.wait_limit_ns = g_wait_ns;
+    return QSA_OK;
+}
+
+qsa_status check_common(const void *q, const float *w, int32_t rows, int32_t H,
+                        const qsa_paged_keys *keys, const int32_t *row_req,
+                        const int32_t *row_visible)
+{
+    if (rows < 0) return QSA_ERR_INVALID_ARG;
+    if (!q || !w || !row_req || !row_visible) return QSA_ERR_INVALID_ARG;
+    if (!supported_heads(H)) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(rows) * H >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    if (!aligned(q, 16)) return QSA_ERR_INVALID_ARG;
+    return check_keys(keys);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qsa_workspace_bytes(int32_t rows, int32_t max_visible, int32_t k, int32_t flags)
+{
+    (void)flags;
+    if (rows <= 0) return 256;
+    const int64_t ld = std::max<int64_t>(8, (static_cast<int64_t>(std::max(max_visible, 0)) + 7) / 8 * 8);
+    return layout(rows, ld, std::max(k, 1)).total;
+}
+
+const char *qsa_status_string(qsa_status s)
+{
+    switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case QSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case QSA_ERR_LAUNCH: return "kernel launch failed";
+    case QSA_ERR_BAD_PAGE: return "block table holds a page id outside the key cache";
+    case QSA_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case QSA_ERR_CUDA: return "CUDA runtime error";
+    case QSA_ERR_NO_DEVICE: return "no usable sm_103 device";
+    }
+    return "unknown status";
+}
+
+qsa_status qsa_set_config(int32_t key, int64_t value)
+{
+    if (key == QSA_CFG_PATH) {
+        if (value < 0 || value > 2) return QSA_ERR_INVALID_ARG;
+        g_cfg_path = value;
+        return QSA_OK;
+    }
+    if (key == QSA_CFG_KERNEL_TIMING) {
+        if (value < 0 || value > 1) return QSA_ERR_INVALID_ARG;
+        g_timing = value != 0;
+        return QSA_OK;
+    }
+    if (key == QSA_CFG_WAIT_LIMIT_NS) {
+        if (value <= 0) return QSA_ERR_INVALID_ARG;
+        g_wait_ns = static_cast<uint64_t>(value);
+        return QSA_OK;
+    }
+    return QSA_ERR_INVALID_ARG;
+}
+
+int32_t qsa_last_launch_count(void) { return g_launches; }
+
+qsa_status qsa_kernel_times(double *ms, int32_t *launches, int32_t n)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    qsa_status st = QSA_OK;
+    for (const Pending &p : g_pending) {
+        float t = 0.f;
+        if (cudaEventSynchronize(p.b) != cudaSuccess || cudaEventElapsedTime(&t, p.a, p.b) != cudaSuccess) {
+            cudaGetLastError();
+            st = QSA_ERR_CUDA;
+        } else if (p.kind < n) {
+            if (ms) ms[p.kind] += t;
+            if (launches) launches[p.kind] += 1;
+        }
+        g_event_pool.push_back(p.a);
+        g_event_pool.push_back(p.b);
+    }
+    g_pending.clear();
+    return st;
+}
+
+qsa_status qsa_get_device_status(void *stream)
+{
+    DeviceInfo *d = nullptr;
+    qsa_status st = device_info(&d);
+    if (st != QSA_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return QSA_ERR_CUDA;
+    }
+    uint32_t bits = 0;
+    const uint32_t zero = 0;
+    if (cudaMemcpy(&bits, d->status, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(d->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return QSA_ERR_CUDA;
+    }
+    return from_status_bits(bits);
+}
+
+qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t H,
+                           const qsa_paged_keys *keys, const int32_t *row_req,
+                           const int32_t *row_visible, float *logits, int64_t ld_logits,
+                           void *ws, size_t ws_bytes, void *stream)
+{
+    g_launches = 0;
+    qsa_status st = check_common(q, w, rows, H, keys, row_req, row_visible);
+    if (st != QSA_OK) return st;
+    if (!logits || ld_logits < 1) return QSA_ERR_INVALID_ARG;
+    if (rows == 0) return QSA_OK;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != QSA_OK) return st;
+    const int64_t max_len = std::min<int64_t>(ld_logits,
+        static_cast<int64_t>(keys->max_pages_per_req) * keys->page_positions);
+    ScoreSetup s;
+    // the score-only call needs no logits scratch: size the layout for one column
+    st = setup_score(s, q, w, rows, H, keys, row_req, row_visible, 1, max_len, 1, 1, ws,
+                     ws_bytes, d, stream);
+    if (st != QSA_OK) return st;
+    s.sp.mode = SCORE_LOGITS;
+    s.sp.out = logits;
+    s.sp.ld = ld_logits;
+    s.sp.pad_inf = 1;
+    st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }));
+    if (st != QSA_OK) return st;
+    return launch_rc(timed(K_PAD, stream, [&] {
+        return launch_pad(logits, ld_logits, rows,
+                          reinterpret_cast<const int32_t *>(s.ws + s.L.row_vis), stream);
+    }));
+}
+
+qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
+                          const int32_t *row_visible, int32_t k, int32_t *out_idx,
+                          float *out_val, void *ws, size_t ws_bytes, void *stream)
+{
+    (void)ws;
+    (void)ws_bytes;
+    g_launches = 0;
+    if (rows < 0 || k < 0 || ld_logits < 1) return QSA_ERR_INVALID_ARG;
+    if (k > QSA_MAX_K) return QSA_ERR_UNSUPPORTED;
+    if (rows == 0 || k == 0) return QSA_OK;
+    if (!logits || !row_visible || !out_idx) return QSA_ERR_INVALID_ARG;
+    if (ld_logits > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    DeviceInfo *d = nullptr;
+    qsa_status st = device_info(&d);
+    if (st != QSA_OK) return st;
+    SelectParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.mode = SEL_DENSE;
+    p.R = rows;
+    p.k = k;
+    p.logits = logits;
+    p.ld = ld_logits;
+    p.max_len = ld_logits;
+    p.row_vis = row_visible;
+    p.out_idx = out_idx;
+    p.out_val = out_val;
+    p.sort_cap = pow2_ceil(k);
+    p.smem_cap = std::max(8192, p.sort_cap);
+    p.status = d->status;
+    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, stream); }));
+}
+
+qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, int32_t H,
+                                   const qsa_paged_keys *keys, const int32_t *row_req,
+                                   const int32_t *row_visible, int32_t k, int32_t *out_idx,
+                                   float *out_val, void *ws, size_t ws_bytes, void *stream)
+{
+    g_launches = 0;
+    qsa_status st = check_common(q, w, rows, H, keys, row_req, row_visible);
+    if (st != QSA_OK) return st;
+    if (k < 0) return QSA_ERR_INVALID_ARG;
+    if (k > QSA_MAX_K) return QSA_ERR_UNSUPPORTED;
+    if (!out_idx) return QSA_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return QSA_OK;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != QSA_OK) return st;
+    const int64_t ld = static_cast<int64_t>(keys->max_pages_per_req) * keys->page_positions;
+    const bool filter = use_filter(ld, k);
+    const FilterShape f = filter_shape(ld, k);
+    ScoreSetup s;
+    st = setup_score(s, q, w, rows, H, keys, row_req, row_visible, ld, ld, k,
+                     filter ? f.stride : 1, ws, ws_bytes, d, stream);
+    if (st != QSA_OK) return st;
+    auto at = [&](size_t off) { return s.ws + off; };
+    float *logits = reinterpret_cast<float *>(at(s.L.logits));
+
+    SelectParams sel;
+    std::memset(&sel, 0, sizeof(sel));
+    sel.R = rows;
+    sel.k = k;
+    sel.max_len = ld;
+    sel.row_vis = reinterpret_cast<const int32_t *>(at(s.L.row_vis));
+    sel.plan = reinterpret_cast<Plan *>(at(s.L.plan));
+    sel.out_idx = out_idx;
+    sel.out_val = out_val;
+    sel.sort_cap = pow2_ceil(k);
+    sel.status = d->status;
+    sel.row_flag = reinterpret_cast<int32_t *>(at(s.L.flag));
+
+    if (!filter) {
+        s.sp.mode = SCORE_LOGITS;
+        s.sp.out = logits;
+        s.sp.ld = ld;
+        if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+        sel.mode = SEL_DENSE;
+        sel.logits = logits;
+        sel.ld = ld;
+        sel.smem_cap = std::max(8192, sel.sort_cap);
+        return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, stream); }));
+    }
+
+    float *sample = reinterpret_cast<float *>(at(s.L.sample));
+    float *tau = reinterpret_cast<float *>(at(s.L.tau));
+    int32_t *cnt = reinterpret_cast<int32_t *>(at(s.L.cnt));
+    uint2 *cand = reinterpret_cast<uint2 *>(at(s.L.cand));
+
+    // 1. scores of every stride-th key tile
+    s.sp.mode = SCORE_SAMPLE;
+    s.sp.out = sample;
+    s.sp.ld = f.sample_ld;
+    if ((st = launch_rc(timed(K_SCORE_SAMPLE, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+    // 2. per-row threshold tau_r: a sample quantile that keeps ~OVERSAMPLE * k positions
+    SelectParams th = sel;
+    th.mode = SEL_THRESH;
+    th.logits = sample;
+    th.ld = f.sample_ld;
+    th.cap = f.cap;
+    th.sample_stride = f.stride;
+    th.tau = tau;
+    th.cand_count_w = cnt;
+    th.oversample = OVERSAMPLE;
+    th.smem_cap = 0;
+    th.sort_cap = 0;
+    if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, stream); }))) != QSA_OK) return st;
+    // 3. full scoring pass keeping only scores >= tau_r
+    s.sp.mode = SCORE_FILTER;
+    s.sp.tau = tau;
+    s.sp.cand = cand;
+    s.sp.cand_count = cnt;
+    s.sp.cap = f.cap;
+    if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+    // 4. exact top-k of each candidate list; rows whose list cannot be trusted
+    //    (fewer than k candidates or overflow) are flagged
+    SelectParams cs = sel;
+    cs.mode = SEL_CAND;
+    cs.cand = cand;
+    cs.cand_count = cnt;
+    cs.cap = f.cap;
+    cs.smem_cap = f.cap;
+    if ((st = launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, stream); }))) != QSA_OK) return st;
+    // 5. flagged rows only: dense scores, then the dense selector
+    s.sp.mode = SCORE_FALLBACK;
+    s.sp.out = logits;
+    s.sp.ld = ld;
+    s.sp.row_flag = sel.row_flag;
+    if ((st = launch_rc(timed(K_SCORE_FALLBACK, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+    SelectParams ds = sel;
+    ds.mode = SEL_DENSE_FLAGGED;
+    ds.logits = logits;
+    ds.ld = ld;
+    ds.smem_cap = std::max(8192, sel.sort_cap);
+    return launch_rc(timed(K_SEL_FLAGGED, stream, [&] { return launch_select(ds, stream); }));
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Shared host/device definitions of the QSA library (not part of the ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace qsa {
+
+// Device status bits (the host maps the highest-priority one to qsa_status).
+enum : uint32_t {
+    ST_BAD_PAGE = 1u << 0,
+    ST_BAD_ROW = 1u << 1,       // row_req out of range or row longer than allowed
+    ST_TIMEOUT = 1u << 2,
+};
+
+constexpr int TILE_M = 128;      // positions per scorer tile (MMA M, TMEM lanes)
+constexpr int HEAD_DIM = 128;    // index-key dimension (MMA K per head)
+constexpr int N_MAX = 256;       // MMA N: (query rows of a group) x heads
+constexpr int KSTAGES = 4;       // key tiles in flight per CTA
+constexpr int SCORE_THREADS = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int EPI_WARPS = 8;
+
+// A group: consecutive query rows of one request that share every key tile.
+struct Group {
+    int32_t row0;      // first query row
+    int32_t nrows;     // rows in the group (<= N_MAX / H)
+    int32_t req;       // request index (row of the block table)
+    int32_t vmax;      // longest visible length in the group (positions)
+};
+
+// Plan written by the plan kernel into the workspace.
+struct Plan {
+    int32_t n_groups;
+    int32_t n_items;           // (group, tile) items over all groups
+    int32_t n_sample_items;    // items of the sampled tiles only
+    int32_t any_fallback;      // set by the candidate selector
+};
+
+enum ScoreMode : int32_t {
+    SCORE_LOGITS = 0,      // logits for j < V_r (and -inf up to the tile end when pad_inf)
+    SCORE_SAMPLE = 1,      // sampled tiles only, into the sample matrix
+    SCORE_FILTER = 2,      // append (score, j) with score >= tau_r to the candidate lists
+    SCORE_FALLBACK = 3,    // like LOGITS, only for groups holding a flagged row
+};
+
+struct ScoreParams {
+    const float *w;             // [R, H]
+    const int32_t *row_vis;     // sanitised V_r [R]
+    const Group *groups;
+    const int32_t *item_prefix;     // [n_groups + 1] items before group g
+    const int32_t *sample_prefix;   // [n_groups + 1]
+    const Plan *plan;
+    const int32_t *block_table;
+    int32_t max_pages;
+    int32_t num_pages;
+    int32_t page_pos;           // positions per page
+    int32_t page_box;           // rows per TMA box = min(page_pos, TILE_M)
+    int32_t H;
+    int32_t R;
+    int32_t mode;
+    int32_t sample_stride;      // tiles between sampled tiles
+    // outputs
+    float *out;                 // logits [R, ld] or sample matrix [R, ld]
+    int64_t ld;
+    int32_t pad_inf;            // LOGITS: write -inf for V_r <= j < tile end (j < ld)
+    const float *tau;           // FILTER: per-row threshold
+    uint2 *cand;                // FILTER: [R, cap] (score bits, position)
+    int32_t *cand_count;        // FILTER: [R]
+    int32_t cap;
+    const int32_t *row_flag;    // FALLBACK: rows to redo
+    uint32_t *status;
+    uint64_t wait_limit_ns;
+};
+
+enum SelectMode : int32_t {
+    SEL_DENSE = 0,      // row r = logits[r, 0:V_r]
+    SEL_CAND = 1,       // row r = candidate list; flags the row when it is unusable
+    SEL_THRESH = 2,     // row r = sample row; writes tau_r, clears cand_count[r]
+    SEL_DENSE_FLAGGED = 3,  // like DENSE, only rows whose flag is set
+};
+
+struct SelectParams {
+    int32_t mode;
+    int32_t R;
+    int32_t k;
+    const float *logits;        // DENSE: logits; THRESH: sample matrix
+    int64_t ld;
+    int64_t max_len;            // largest valid V_r (longer rows are clamped and flagged)
+    const int32_t *row_vis;     // V_r
+    const uint2 *cand;          // CAND
+    const int32_t *cand_count;
+    int32_t cap;
+    int32_t *row_flag;          // CAND: set for rows that need the dense path
+    Plan *plan;
+    // THRESH
+    int32_t sample_stride;
+    float *tau;
+    int32_t *cand_count_w;
+    float oversample;           // expected candidates / k
+    // outputs
+    int32_t *out_idx;
+    float *out_val;
+    int32_t smem_cap;           // C: elements the CTA can hold
+    int32_t sort_cap;           // K_pad: power of two >= min(k, C)
+    uint32_t *status;
+};
+
+// Launchers (one translation unit each); return cudaError_t as int.
+int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t H,
+                int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
+                Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
+                uint32_t *status, void *stream);
+int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid,
+                 void *stream);
+int launch_select(const SelectParams &p, void *stream);
+size_t select_smem_bytes(int32_t smem_cap, int32_t sort_cap);
+uint32_t score_smem_bytes();
+int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream);
+
+}  // namespace qsa

@@ -1,0 +1,181 @@
+// Plan kernel: sanitises the per-row metadata and splits the query rows into
+// groups (consecutive rows of one request, at most 256 / H rows, so that one
+// group is the N side of one tensor-core tile), then lays the (group, key tile)
+// work items out for the persistent scorer.
+#include <cuda_runtime.h>
+
+#include "qsa_device.cuh"
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr int PLAN_THREADS = 1024;
+
+template <typename Op>
+__device__ int32_t block_incl_scan(int32_t v, int32_t *wbuf, Op op, int32_t ident)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = op(x, y);
+    }
+    if (lane == 31) wbuf[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int32_t t = wbuf[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t = op(t, y);
+        }
+        wbuf[lane] = t;
+    }
+    __syncthreads();
+    int32_t r = wid > 0 ? op(wbuf[wid - 1], x) : x;
+    __syncthreads();
+    (void)ident;
+    return r;
+}
+
+struct OpMax { __device__ int32_t operator()(int32_t a, int32_t b) const { return a > b ? a : b; } };
+struct OpAdd { __device__ int32_t operator()(int32_t a, int32_t b) const { return a + b; } };
+
+__global__ void __launch_bounds__(PLAN_THREADS)
+plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row_visible,
+            int32_t R, int32_t G, int32_t num_reqs, int64_t max_len, int32_t sample_stride,
+            int32_t *__restrict__ row_vis, Group *__restrict__ groups,
+            int32_t *__restrict__ item_prefix, int32_t *__restrict__ sample_prefix,
+            Plan *__restrict__ plan, uint32_t *status)
+{
+    __shared__ int32_t wbuf[32];
+    __shared__ int32_t s_req[PLAN_THREADS];
+    __shared__ int32_t carry_req, carry_run, carry_gid, carry_items, carry_samples;
+    const int tid = threadIdx.x;
+    if (tid == 0) { carry_req = -2; carry_run = 0; carry_gid = 0; }
+    __syncthreads();
+
+    // Phase 1: sanitise rows, find group starts.
+    for (int32_t base = 0; base < R; base += PLAN_THREADS) {
+        const int32_t r = base + tid;
+        int32_t req = -1;
+        if (r < R) {
+            int32_t b = row_req[r];
+            int64_t v = row_visible[r];
+            bool bad = false;
+            if (b < 0 || b >= num_reqs) { b = -1; v = 0; bad = true; }
+            if (v < 0) { v = 0; bad = true; }
+            if (v > max_len) { v = max_len; bad = true; }
+            if (bad) record_error(status, ST_BAD_ROW);
+            row_vis[r] = static_cast<int32_t>(v);
+            req = b;
+        }
+        s_req[tid] = req;
+        __syncthreads();
+        const int32_t prev = tid > 0 ? s_req[tid - 1] : carry_req;
+        const bool begin = r < R && (r == 0 || req != prev);
+        int32_t rs = block_incl_scan(begin ? r : -1, wbuf, OpMax(), -1);
+        if (rs < 0) rs = carry_run;
+        const bool gbegin = r < R && ((r - rs) % G == 0);
+        const int32_t incl = block_incl_scan(gbegin ? 1 : 0, wbuf, OpAdd(), 0);
+        const int32_t gid = carry_gid + incl - 1;
+        if (gbegin) {
+            groups[gid].row0 = r;
+            groups[gid].req = req;
+        }
+        __syncthreads();
+        if (tid == min(PLAN_THREADS - 1, R - 1 - base)) {
+            carry_req = req;
+            carry_run = rs;
+            carry_gid = gid + 1;
+        }
+        __syncthreads();
+    }
+    const int32_t n_groups = carry_gid;
+
+    // Phase 2: rows and longest visible length of each group.
+    for (int32_t g = tid; g < n_groups; g += PLAN_THREADS) {
+        const int32_t r0 = groups[g].row0;
+        const int32_t r1 = g + 1 < n_groups ? groups[g + 1].row0 : R;
+        int32_t vmax = 0;
+        for (int32_t r = r0; r < r1; ++r) vmax = max(vmax, row_vis[r]);
+        groups[g].nrows = r1 - r0;
+        groups[g].vmax = vmax;
+    }
+    __syncthreads();
+
+    // Phase 3: item offsets (all key tiles, and the sampled tiles only).
+    if (tid == 0) { carry_items = 0; carry_samples = 0; }
+    __syncthreads();
+    for (int32_t base = 0; base < n_groups; base += PLAN_THREADS) {
+        const int32_t g = base + tid;
+        int32_t tiles = 0, stiles = 0;
+        if (g < n_groups) {
+            tiles = (groups[g].vmax + TILE_M - 1) / TILE_M;
+            stiles = (tiles + sample_stride - 1) / sample_stride;
+        }
+        const int32_t it = block_incl_scan(tiles, wbuf, OpAdd(), 0);
+        const int32_t st = block_incl_scan(stiles, wbuf, OpAdd(), 0);
+        if (g < n_groups) {
+            item_prefix[g] = carry_items + it - tiles;
+            sample_prefix[g] = carry_samples + st - stiles;
+        }
+        __syncthreads();
+        if (tid == PLAN_THREADS - 1) {
+            carry_items += it;
+            carry_samples += st;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) {
+        item_prefix[n_groups] = carry_items;
+        sample_prefix[n_groups] = carry_samples;
+        plan->n_groups = n_groups;
+        plan->n_items = carry_items;
+        plan->n_sample_items = carry_samples;
+        plan->any_fallback = 0;
+    }
+}
+
+}  // namespace
+
+int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t H,
+                int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
+                Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
+                uint32_t *status, void *stream)
+{
+    const int32_t G = N_MAX / H;
+    plan_kernel<<<1, PLAN_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
+        row_req, row_visible, R, G, num_reqs, max_len, sample_stride, row_vis, groups,
+        item_prefix, sample_prefix, plan, status);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace qsa
+
+namespace qsa {
+namespace {
+
+// -inf for every position from the end of a row's last scored tile to ld.
+__global__ void pad_kernel(float *__restrict__ logits, int64_t ld, int32_t R,
+                           const int32_t *__restrict__ row_vis)
+{
+    const int32_t r = blockIdx.x;
+    if (r >= R) return;
+    const int64_t from = (static_cast<int64_t>(row_vis[r]) + TILE_M - 1) / TILE_M * TILE_M;
+    float *row = logits + static_cast<int64_t>(r) * ld;
+    const float ninf = -__int_as_float(0x7f800000);
+    for (int64_t j = from + threadIdx.x; j < ld; j += blockDim.x) row[j] = ninf;
+}
+
+}  // namespace
+
+int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream)
+{
+    pad_kernel<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(logits, ld, R, row_vis);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace qsa

@@ -1,0 +1,383 @@
+// Index scorer: the per-head contraction q[r,h,:] . k_j on the 5th-generation
+// tensor cores (tcgen05.mma kind::f16, FP16 in, FP32 accumulate in TMEM), fed
+// by TMA gathers of key pages through the block table, with the head
+// reduction logit = sum_h w[r,h] * max(dot, 0) and the causal mask fused into
+// the TMEM read-out.
+//
+// Tile: M = 128 key positions (TMEM lanes) x N = (rows of a group) * H
+// (TMEM columns, <= 256) x K = 128.  Keys are the A operand because they
+// differ per tile, the group's queries are the B operand and stay resident in
+// shared memory while the CTA walks the group's key tiles.  One persistent CTA
+// per SM: warp 0 issues TMA, warp 1 issues MMAs, warps 2..9 drain TMEM
+// (double-buffered accumulators, 2 x 256 columns) and write the results.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "qsa_device.cuh"
+#include "qsa_internal.h"
+
+namespace qsa {
+namespace {
+
+constexpr uint32_t Q_HALF_BYTES = N_MAX * 128;          // 256 rows x 128 B
+constexpr uint32_t Q_BYTES = 2 * Q_HALF_BYTES;            // 64 KiB
+constexpr uint32_t K_HALF_BYTES = TILE_M * 128;           // 128 rows x 128 B
+constexpr uint32_t K_STAGE_BYTES = 2 * K_HALF_BYTES;      // 32 KiB
+constexpr uint32_t SMEM_TILES = Q_BYTES + KSTAGES * K_STAGE_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+
+struct __align__(8) Ctrl {
+    uint64_t full[KSTAGES];
+    uint64_t empty[KSTAGES];
+    uint64_t q_full;
+    uint64_t q_empty;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+// Group data of one epilogue warp (the rows of its column half), private to
+// that warp so that a group change needs no barrier across warps.
+struct EpiRows {
+    float w[N_MAX / 2];        // w[(lr - first row of the half) * H + h]
+    int32_t vis[N_MAX / 2];    // V of each row
+    float tau[N_MAX / 2];      // FILTER threshold of each row
+    int32_t flag[N_MAX / 2];   // FALLBACK: row needs the dense path
+};
+
+constexpr uint32_t SMEM_BYTES = SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows) + 1024;
+
+// Walks the same (group, tile) sequence in every role of a CTA.
+struct ItemCursor {
+    const int32_t *prefix;
+    int32_t g, it, it_end, stride;
+    __device__ void init(const int32_t *pre, int32_t n_groups, int32_t it0, int32_t it1, int32_t s)
+    {
+        prefix = pre;
+        it = it0;
+        it_end = it1;
+        stride = s;
+        // last group whose first item is <= it0 (prefix is non-decreasing)
+        int32_t lo = 0, hi = n_groups - 1;
+        while (lo < hi) {
+            int32_t mid = (lo + hi + 1) >> 1;
+            if (__ldg(prefix + mid) <= it0) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+    }
+    __device__ bool valid() const { return it < it_end; }
+    __device__ void settle()
+    {
+        while (it >= __ldg(prefix + g + 1)) ++g;
+    }
+    __device__ int32_t tile() const { return (it - __ldg(prefix + g)) * stride; }
+    __device__ void next() { ++it; }
+};
+
+__device__ __forceinline__ bool group_flagged(const ScoreParams &p, const Group &gr)
+{
+    for (int32_t r = 0; r < gr.nrows; ++r)
+        if (__ldg(p.row_flag + gr.row0 + r)) return true;
+    return false;
+}
+
+template <int H>
+__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
+                                              int32_t tile, uint32_t taddr_row, int half,
+                                              int lane, int32_t p_in_tile)
+{
+    constexpr int ROWS_PER_CHUNK = 32 / H;
+    constexpr int ROWS_PER_HALF = (N_MAX / 2) / H;
+    const int32_t ncols = gr.nrows * H;
+    const int32_t j = tile * TILE_M + p_in_tile;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        const int32_t col0 = half * 128 + ch * 32;
+        if (col0 >= ncols) break;                       // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr_row + static_cast<uint32_t>(col0), v);
+        tmem_ld_wait();
+        const int32_t lr0 = col0 / H;
+#pragma unroll
+        for (int i = 0; i < ROWS_PER_CHUNK; ++i) {
+            const int32_t lr = lr0 + i;
+            if (lr >= gr.nrows) break;                  // warp-uniform
+            const int32_t el = lr - half * ROWS_PER_HALF;      // row within this warp's half
+            float s = 0.0f;
+#pragma unroll
+            for (int h = 0; h < H; ++h)
+                s = fmaf(e.w[el * H + h], fmaxf(__uint_as_float(v[i * H + h]), 0.0f), s);
+            const int32_t r = gr.row0 + lr;
+            const int32_t V = e.vis[el];
+            const bool ok = j < V;
+            if (p.mode == SCORE_FILTER) {
+                const bool take = ok && s >= e.tau[el];
+                const uint32_t m = __ballot_sync(0xffffffffu, take);
+                if (m) {
+                    const int leader = __ffs(m) - 1;
+                    int32_t base = 0;
+                    if (lane == leader) base = atomicAdd(p.cand_count + r, __popc(m));
+                    base = __shfl_sync(0xffffffffu, base, leader);
+                    if (take) {
+                        const int32_t slot = base + __popc(m & ((1u << lane) - 1u));
+                        if (slot < p.cap)
+                            p.cand[static_cast<int64_t>(r) * p.cap + slot] =
+                                make_uint2(__float_as_uint(s), static_cast<uint32_t>(j));
+                    }
+                }
+            } else if (p.mode == SCORE_SAMPLE) {
+                if (ok) {
+                    const int64_t col = static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
+                    p.out[static_cast<int64_t>(r) * p.ld + col] = s;
+                }
+            } else {
+                if (p.mode == SCORE_FALLBACK && !e.flag[el]) continue;
+                float *dst = p.out + static_cast<int64_t>(r) * p.ld + j;
+                if (ok) *dst = s;
+                else if (p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
+            }
+        }
+    }
+}
+
+template <int H>
+__global__ void __launch_bounds__(SCORE_THREADS, 1)
+score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+             const ScoreParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t *q_s = smem;
+    uint8_t *k_s = smem + Q_BYTES;
+    Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_TILES);
+    EpiRows *epi_rows = reinterpret_cast<EpiRows *>(smem + SMEM_TILES + sizeof(Ctrl));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (p.mode == SCORE_FALLBACK && p.plan->any_fallback == 0) return;
+    const bool sampled = p.mode == SCORE_SAMPLE;
+    const int32_t n_items = sampled ? p.plan->n_sample_items : p.plan->n_items;
+    const int32_t it0 = static_cast<int32_t>((static_cast<int64_t>(n_items) * blockIdx.x) / gridDim.x);
+    const int32_t it1 = static_cast<int32_t>((static_cast<int64_t>(n_items) * (blockIdx.x + 1)) / gridDim.x);
+    if (it0 >= it1) return;
+    const int32_t n_groups = p.plan->n_groups;
+    const int32_t *prefix = sampled ? p.sample_prefix : p.item_prefix;
+    const int32_t stride = sampled ? p.sample_stride : 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < KSTAGES; ++s) {
+            mbar_init(&c.full[s], 1);
+            mbar_init(&c.empty[s], 1);
+        }
+        mbar_init(&c.q_full, 1);
+        mbar_init(&c.q_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.acc_full[b], 1);
+            mbar_init(&c.acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(&c.drain, 1);
+        c.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    volatile int *abort = &c.abort;
+    const uint64_t lim = p.wait_limit_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            ItemCursor cur;
+            cur.init(prefix, n_groups, it0, it1, stride);
+            int32_t cur_g = -1, q_loads = 0, stage = 0;
+            uint32_t phase = 0;
+            bool skip_group = false;
+            Group gr{};
+            for (; cur.valid(); cur.next()) {
+                cur.settle();
+                if (cur.g != cur_g) {
+                    cur_g = cur.g;
+                    gr = p.groups[cur_g];
+                    skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
+                    if (skip_group) continue;
+                    if (q_loads > 0 && !mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim)) break;
+                    mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                    tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
+                    tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
+                    ++q_loads;
+                }
+                if (skip_group) continue;
+                if (!mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim)) break;
+                const int32_t pos0 = cur.tile() * TILE_M;
+                const int32_t valid = min(TILE_M, gr.vmax - pos0);
+                const int32_t nbox = (valid + p.page_box - 1) / p.page_box;
+                mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
+                uint8_t *dst = k_s + stage * K_STAGE_BYTES;
+                const int32_t *bt = p.block_table + static_cast<int64_t>(gr.req) * p.max_pages;
+                for (int32_t i = 0; i < nbox; ++i) {
+                    const int32_t pos = pos0 + i * p.page_box;
+                    const int32_t pid = __ldg(bt + pos / p.page_pos);
+                    int32_t y;
+                    if (pid >= 0 && pid < p.num_pages) {
+                        y = pid * p.page_pos + (pos % p.page_pos);
+                    } else {
+                        record_error(p.status, ST_BAD_PAGE);
+                        y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+                    }
+                    tma_load_2d(dst + i * p.page_box * 128, &tmap_k, &c.full[stage], 0, y);
+                    tma_load_2d(dst + K_HALF_BYTES + i * p.page_box * 128, &tmap_k, &c.full[stage], 64, y);
+                }
+                if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            ItemCursor cur;
+            cur.init(prefix, n_groups, it0, it1, stride);
+            int32_t cur_g = -1, stage = 0, q_uses = 0;
+            uint32_t phase = 0, acc_cnt = 0, idesc = 0;
+            bool skip_group = false, have_q = false;
+            for (; cur.valid(); cur.next()) {
+                cur.settle();
+                if (cur.g != cur_g) {
+                    cur_g = cur.g;
+                    const Group gr = p.groups[cur_g];
+                    skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
+                    if (skip_group) continue;
+                    if (have_q) umma_commit(&c.q_empty);   // previous group's MMAs done -> q free
+                    if (!mbar_wait(&c.q_full, q_uses & 1, abort, lim)) break;
+                    ++q_uses;
+                    have_q = true;
+                    const int n = ((gr.nrows * H + 15) / 16) * 16;
+                    idesc = umma_idesc_f16_f32(TILE_M, n);
+                }
+                if (skip_group) continue;
+                if (!mbar_wait(&c.full[stage], phase, abort, lim)) break;
+                const uint32_t b = acc_cnt & 1u;
+                if (!mbar_wait(&c.acc_empty[b], ((acc_cnt >> 1) & 1u) ^ 1u, abort, lim)) break;
+                tc_fence_after();
+                const uint32_t a_base = smem_u32(k_s + stage * K_STAGE_BYTES);
+                const uint32_t b_base = smem_u32(q_s);
+                const uint32_t d = tmem + b * 256u;
+#pragma unroll
+                for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
+                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
+                    const uint64_t ad = sw128_kmajor_desc(a_base + (kk >> 2) * K_HALF_BYTES + off);
+                    const uint64_t bd = sw128_kmajor_desc(b_base + (kk >> 2) * Q_HALF_BYTES + off);
+                    umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&c.empty[stage]);
+                umma_commit(&c.acc_full[b]);
+                if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
+                ++acc_cnt;
+            }
+            // every MMA issued by this thread has finished before TMEM is freed
+            umma_commit(&c.drain);
+            mbar_wait(&c.drain, 0, abort, lim);
+        }
+    } else {
+        // --------------------------------------------------- epilogue --
+        const int ew = warp - 2;
+        const int quarter = warp & 3;
+        const int half = ew >> 2;
+        const int32_t p_in_tile = quarter * 32 + lane;
+        EpiRows &er = epi_rows[ew];
+        ItemCursor cur;
+        cur.init(prefix, n_groups, it0, it1, stride);
+        int32_t cur_g = -1;
+        uint32_t acc_cnt = 0;
+        bool skip_group = false;
+        Group gr{};
+        for (; cur.valid(); cur.next()) {
+            cur.settle();
+            if (cur.g != cur_g) {
+                cur_g = cur.g;
+                gr = p.groups[cur_g];
+                skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
+                if (skip_group) continue;
+                // this warp's rows: [half * rows_per_half, +rows_per_half) of the group
+                constexpr int32_t RPH = (N_MAX / 2) / H;
+                const int32_t first = half * RPH;
+                const int32_t nmine = max(0, min(RPH, gr.nrows - first));
+                __syncwarp();
+                for (int32_t i = lane; i < nmine * H; i += 32)
+                    er.w[i] = __ldg(p.w + static_cast<int64_t>(gr.row0 + first) * H + i);
+                for (int32_t i = lane; i < nmine; i += 32) {
+                    const int32_t r = gr.row0 + first + i;
+                    er.vis[i] = __ldg(p.row_vis + r);
+                    er.tau[i] = p.mode == SCORE_FILTER ? __ldg(p.tau + r) : 0.0f;
+                    er.flag[i] = p.mode == SCORE_FALLBACK ? __ldg(p.row_flag + r) : 1;
+                }
+                __syncwarp();
+            }
+            if (skip_group) continue;
+            const uint32_t b = acc_cnt & 1u;
+            if (!mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * 256u;
+            epilogue_tile<H>(p, er, gr, cur.tile(), taddr, half, lane, p_in_tile);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.acc_empty[b]);
+            ++acc_cnt;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (c.abort && threadIdx.x == 0) record_error(p.status, ST_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+template <int H>
+int launch_h(const ScoreParams &p, const void *tq, const void *tk, int grid, cudaStream_t s)
+{
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    if (!attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(score_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(SMEM_BYTES));
+        if (e != cudaSuccess) return static_cast<int>(e);
+        attr_done[dev] = true;
+    }
+    score_kernel<H><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(
+        *static_cast<const CUtensorMap *>(tq), *static_cast<const CUtensorMap *>(tk), p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+
+uint32_t score_smem_bytes() { return SMEM_BYTES; }
+
+int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid, void *stream)
+{
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (p.H) {
+    case 1: return launch_h<1>(p, tmap_q, tmap_k, grid, s);
+    case 2: return launch_h<2>(p, tmap_q, tmap_k, grid, s);
+    case 4: return launch_h<4>(p, tmap_q, tmap_k, grid, s);
+    case 8: return launch_h<8>(p, tmap_q, tmap_k, grid, s);
+    default: return static_cast<int>(cudaErrorInvalidValue);
+    }
+}
+
+}  // namespace qsa

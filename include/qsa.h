@@ -1,0 +1,139 @@
+/*
+ * qsa.h - C ABI of the GB300 (sm_103a) QSA indexer library, libqsa.so.
+ *
+ * The operation ("spec(MODEL-MM-QWEN4-EXP) ...", section "The component
+ * deep-dives", and "[Perf][Qwen4Exp] Admit the cuBLAS QSA indexer and exact
+ * top-k on Turing", section "Purpose"):
+ *
+ *   for every query row r of request b = row_req[r], with V_r = row_visible[r]
+ *   visible compressed positions (compress ratio 4, so a query at token t sees
+ *   (t+1) // 4 of them):
+ *     logit[r, j] = sum_{h<H} w[r,h] * max(q[r,h,:] . k_j, 0)          j < V_r
+ *     k_j         = k_cache[block_table[b, j / P], j % P, :]            (paged)
+ *   with FP16 q and k, FP32 accumulation; then the exact top-k of row r,
+ *   ordered by score descending and, on equal scores, by position ascending
+ *   (the "exact lexicographic top-k" with its deterministic tie rule).
+ *
+ * Conventions shared by every entry point:
+ *  - All array arguments are DEVICE pointers into memory the caller owns and
+ *    keeps alive until the work on `stream` has finished.  The library never
+ *    allocates device memory per call; scratch comes from the caller's
+ *    workspace, sized by qsa_workspace_bytes().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call is asynchronous on that stream.
+ *  - Host-side argument checks run before any launch and return a status;
+ *    nothing is launched when a check fails.  No C++ exception crosses the ABI.
+ *  - Errors found on the device (bad page id, row_req out of range, a row
+ *    longer than the block table or the logit row, a pipeline wait that ran
+ *    out of time) never trap: the kernels record them in a per-device status
+ *    word and carry on with safe values.  qsa_get_device_status() reads and
+ *    clears that word.
+ *  - Supported shapes: head_dim == 128, H in {1, 2, 4, 8}, page_positions a
+ *    power of two in [8, 256], 0 <= k <= QSA_MAX_K.  k may exceed V_r.  Others
+ *    return QSA_ERR_UNSUPPORTED.  q and k_cache must be 16-byte aligned.
+ *  - Output of the top-k: out_idx[r, 0:min(k, V_r)] holds positions in
+ *    (score desc, position asc) order and -1 after that; out_val (optional,
+ *    may be NULL) holds the matching logits and -inf after that.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_MAX_K 8192
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1,   /* a host-side argument check failed, or (device) row data out of range */
+    QSA_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
+    QSA_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than qsa_workspace_bytes() */
+    QSA_ERR_LAUNCH = 4,        /* a kernel launch was refused by the runtime */
+    QSA_ERR_BAD_PAGE = 5,      /* (device) a block-table entry outside [0, num_pages) */
+    QSA_ERR_TIMEOUT = 6,       /* (device) a pipeline wait ran past its time limit */
+    QSA_ERR_CUDA = 7,          /* another CUDA runtime error */
+    QSA_ERR_NO_DEVICE = 8      /* no usable sm_100-family device */
+} qsa_status;
+
+/* Paged index-key side cache: one FP16 key of head_dim values per compressed
+ * position ("a side cache of one index-key vector per token", key only). */
+typedef struct {
+    const void    *k_cache;            /* device FP16 [num_pages, page_positions, head_dim], contiguous */
+    int32_t        num_pages;          /* physical pages in k_cache */
+    int32_t        page_positions;     /* positions per page (16 = 64 tokens at ratio 4) */
+    int32_t        head_dim;           /* must be 128 */
+    const int32_t *block_table;        /* device int32 [num_reqs, max_pages_per_req]: physical page ids */
+    int32_t        num_reqs;
+    int32_t        max_pages_per_req;  /* row stride of block_table; V_r <= max_pages_per_req * page_positions */
+} qsa_paged_keys;
+
+/* Bytes of device workspace the calls below need for `rows` query rows whose
+ * visible lengths are at most `max_visible` and a top-k of `k`.  For
+ * qsa_select_paged_tokens pass max_visible = max_pages_per_req * page_positions.
+ * `flags` is reserved (pass 0).  Host only; no device is touched. */
+size_t qsa_workspace_bytes(int32_t rows, int32_t max_visible, int32_t k, int32_t flags);
+
+/* Index scores only: logits[r * ld_logits + j] for 0 <= j < ld_logits, FP32,
+ * row-major; -inf for j >= V_r.  q: FP16 [rows, H, 128]; w: FP32 [rows, H];
+ * row_req, row_visible: int32 [rows].  Needs ld_logits >= max V_r; a row with
+ * V_r > ld_logits is clamped and flagged.  ws/ws_bytes as for the other calls. */
+qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t H,
+                           const qsa_paged_keys *keys, const int32_t *row_req,
+                           const int32_t *row_visible, float *logits, int64_t ld_logits,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* Exact top-k of each row of a logit matrix (row r holds V_r = row_visible[r]
+ * valid entries; entries past V_r are never read).  out_idx: int32 [rows, k];
+ * out_val: FP32 [rows, k] or NULL.  Scores must be finite.  ws may be NULL. */
+qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
+                          const int32_t *row_visible, int32_t k, int32_t *out_idx,
+                          float *out_val, void *ws, size_t ws_bytes, void *stream);
+
+/* The whole step: score every visible position of every row, then its exact
+ * top-k, without the caller seeing the logits.  Same arguments as above. */
+qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, int32_t H,
+                                   const qsa_paged_keys *keys, const int32_t *row_req,
+                                   const int32_t *row_visible, int32_t k, int32_t *out_idx,
+                                   float *out_val, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device (QSA_OK when no kernel recorded an error). */
+qsa_status qsa_get_device_status(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *qsa_status_string(qsa_status status);
+
+/* Tuning / test switches, process-wide (not thread-safe against concurrent
+ * calls).  QSA_CFG_PATH: 0 = automatic, 1 = materialise logits then select,
+ * 2 = sampled-threshold filter path.  QSA_CFG_WAIT_LIMIT_NS: time after which
+ * a pipeline wait gives up and records QSA_ERR_TIMEOUT (default 2 s).
+ * Returns QSA_ERR_INVALID_ARG for an unknown key or value. */
+#define QSA_CFG_PATH 1
+#define QSA_CFG_WAIT_LIMIT_NS 2
+#define QSA_CFG_KERNEL_TIMING 3   /* 1: bracket every launch with CUDA events on its stream */
+qsa_status qsa_set_config(int32_t key, int64_t value);
+
+/* Kernel kinds reported by qsa_kernel_times(). */
+#define QSA_KERNEL_KINDS 10
+/* 0 plan, 1 score (logits), 2 score (sampled tiles), 3 score (threshold filter),
+ * 4 score (fallback rows), 5 select (dense rows), 6 select (threshold),
+ * 7 select (candidates), 8 select (fallback rows), 9 -inf padding. */
+
+/* With QSA_CFG_KERNEL_TIMING on: synchronises the pending events, adds each
+ * launch's elapsed time to ms[kind] and its count to launches[kind] for the
+ * first n kinds (either array may be NULL), then forgets the events.
+ * Returns QSA_ERR_CUDA if an event could not be read. */
+qsa_status qsa_kernel_times(double *ms, int32_t *launches, int32_t n);
+
+/* Launches made by the most recent qsa_* call on this host thread (kernels of
+ * this library only). */
+int32_t qsa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QSA_H */

@@ -1,0 +1,99 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports
+every entry point of include/qsa.h, and rejects bad arguments on the host
+before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_select_gb300 import build as qbuild
+from block_sparse_attention_select_gb300 import qsa
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qsa.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"qsa_index_score", "qsa_topk_exact", "qsa_select_paged_tokens",
+            "qsa_workspace_bytes", "qsa_get_device_status", "qsa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for s in range(0, 9):
+        assert qsa.status_string(s)
+    assert qsa.status_string(0) == "ok"
+
+
+def test_workspace_size_grows_with_shape(lib):
+    a = qsa.workspace_bytes(1616, 46080, 2048)
+    b = qsa.workspace_bytes(3232, 46080, 2048)
+    assert a > 1616 * 46080 * 4 and b > a
+    assert qsa.workspace_bytes(0, 0, 0) > 0
+
+
+def _call_select(lib, **over):
+    keys = qsa.PagedKeysC(16, 4, 16, 128, 16, 1, 4)
+    args = dict(q=16, w=16, rows=8, H=4, keys=ctypes.byref(keys), row_req=16, row_visible=16,
+                k=8, out_idx=16, out_val=None, ws=256, ws_bytes=1 << 40, stream=None)
+    args.update(over)
+    vp = ctypes.c_void_p
+    return lib.qsa_select_paged_tokens(vp(args["q"]), vp(args["w"]), args["rows"], args["H"],
+                                       args["keys"], vp(args["row_req"]), vp(args["row_visible"]),
+                                       args["k"], vp(args["out_idx"]), vp(args["out_val"]),
+                                       vp(args["ws"]), args["ws_bytes"], vp(args["stream"]))
+
+
+def test_host_side_argument_checks(lib):
+    assert _call_select(lib, rows=0) == qsa.QSA_OK              # nothing to do
+    assert _call_select(lib, k=0) == qsa.QSA_OK
+    assert _call_select(lib, rows=-1) == qsa.QSA_ERR_INVALID_ARG
+    assert _call_select(lib, q=None) == qsa.QSA_ERR_INVALID_ARG
+    assert _call_select(lib, q=18) == qsa.QSA_ERR_INVALID_ARG   # not 16-byte aligned
+    assert _call_select(lib, H=3) == qsa.QSA_ERR_UNSUPPORTED
+    assert _call_select(lib, k=qsa.QSA_MAX_K + 1) == qsa.QSA_ERR_UNSUPPORTED
+    assert _call_select(lib, k=-2) == qsa.QSA_ERR_INVALID_ARG
+    bad_dim = qsa.PagedKeysC(16, 4, 16, 64, 16, 1, 4)
+    assert _call_select(lib, keys=ctypes.byref(bad_dim)) == qsa.QSA_ERR_UNSUPPORTED
+    bad_page = qsa.PagedKeysC(16, 4, 12, 128, 16, 1, 4)
+    assert _call_select(lib, keys=ctypes.byref(bad_page)) == qsa.QSA_ERR_UNSUPPORTED
+    no_table = qsa.PagedKeysC(16, 4, 16, 128, 0, 1, 4)
+    assert _call_select(lib, keys=ctypes.byref(no_table)) == qsa.QSA_ERR_INVALID_ARG
+    # with every host check passed and no GPU here, the call reports no device
+    assert _call_select(lib) in (qsa.QSA_ERR_NO_DEVICE, qsa.QSA_ERR_WORKSPACE)
+
+
+def test_config_switches(lib):
+    assert lib.qsa_set_config(qsa.QSA_CFG_PATH, 1) == qsa.QSA_OK
+    assert lib.qsa_set_config(qsa.QSA_CFG_PATH, 0) == qsa.QSA_OK
+    assert lib.qsa_set_config(qsa.QSA_CFG_PATH, 5) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_set_config(99, 1) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_set_config(qsa.QSA_CFG_WAIT_LIMIT_NS, 0) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_set_config(qsa.QSA_CFG_WAIT_LIMIT_NS, 2_000_000_000) == qsa.QSA_OK
+
+
+def test_topk_host_checks(lib):
+    f = lib.qsa_topk_exact
+    vp = ctypes.c_void_p
+    assert f(vp(16), 10, 0, vp(16), 4, vp(16), None, None, 0, None) == qsa.QSA_OK
+    assert f(vp(16), 10, 4, vp(16), -1, vp(16), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert f(vp(16), 0, 4, vp(16), 4, vp(16), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert f(None, 10, 4, vp(16), 4, vp(16), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert f(vp(16), 10, 4, vp(16), qsa.QSA_MAX_K + 1, vp(16), None, None, 0,
+             None) == qsa.QSA_ERR_UNSUPPORTED

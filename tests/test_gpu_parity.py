@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Integer-valued inputs must match bit for bit (indices and values); Gaussian
+inputs must give logits within |g - o| <= 1e-3 |o| + 1e-6 and selections that
+differ from the oracle's only at near-ties of the cutoff (within the same
+tolerance), with the disagreement rate reported.  Selections are also
+compared bit-exactly with the oracle's selector run on the GPU's own logits.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_select_gb300 import qsa
+from block_sparse_attention_select_gb300 import workloads as W
+
+from gpu_util import (assert_logits_close, check_sorted_valid, gpu_logits, gpu_select,
+                      near_tie_disagreement, to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    qsa.load()
+    assert torch.cuda.is_available()
+    yield
+    assert qsa.get_device_status() == qsa.QSA_OK
+
+
+def _oracle_rows(wl, rows, ld=None):
+    rows = np.asarray(rows)
+    ld = wl.ld if ld is None else ld
+    lg = oracle.score(wl.q[rows], wl.w[rows], wl.k_cache, wl.block_table, wl.row_req[rows],
+                      wl.row_visible[rows], ld)
+    idx, val = oracle.select(lg, wl.row_visible[rows], wl.k)
+    return lg, idx, val
+
+
+# ------------------------------------------------------------ tiny, exact ----
+
+@pytest.mark.parametrize("path", [qsa.PATH_DENSE, qsa.PATH_FILTER])
+def test_tiny_config_bit_exact(path):
+    wl = W.tiny()
+    oi, ov, ol = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                            wl.row_visible, wl.k, ld=wl.ld)
+    gi, gv = gpu_select(wl, path=path)
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov)
+
+
+def test_tiny_config_logits_bit_exact():
+    wl = W.tiny()
+    ol = oracle.score(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req, wl.row_visible, wl.ld)
+    np.testing.assert_array_equal(gpu_logits(wl), ol)
+
+
+# ------------------------------------------------- ragged, multi-request ----
+
+CASES = [
+    # (ctx tokens per request, rows per request, k, dist, H, page positions)
+    ([3000, 777, 5], [70, 3, 1], 33, "int4", 4, 16),
+    ([1030, 2050], [130, 65], 100, "int4", 2, 16),
+    ([4100], [40], 64, "int4", 8, 16),
+    ([2600, 900], [300, 20], 17, "int4", 1, 16),
+    ([6000, 1000], [5, 9], 128, "int4", 4, 8),
+    ([6000], [9], 128, "int4", 4, 32),
+    ([9000], [11], 128, "int4", 4, 128),
+    ([9000], [11], 96, "int4", 4, 256),
+    ([20000, 9000], [90, 45], 256, "gauss", 4, 16),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+@pytest.mark.parametrize("path", [qsa.PATH_DENSE, qsa.PATH_FILTER])
+def test_ragged_cases_against_oracle(case, path):
+    ctx, rows, k, dist, H, P = case
+    wl = W.make_workload("ragged", seed=hash((tuple(ctx), k, H, P)) % 1000, ctx_tokens=ctx,
+                         rows_per_req=rows, k=k, dist=dist, heads=H, page_positions=P)
+    d = to_device(wl)
+    ol, oi, ov = _oracle_rows(wl, np.arange(wl.rows))
+    gl = gpu_logits(wl, d)
+    gi, gv = gpu_select(wl, d, path=path)
+    check_sorted_valid(gi, gv, wl.row_visible, k)
+    if dist == "int4":
+        np.testing.assert_array_equal(gl, ol)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+    else:
+        assert_logits_close(gl, ol, wl.row_visible)
+        # exact against the oracle's selector on the GPU's own logits
+        ei, ev = oracle.select(gl, wl.row_visible, k)
+        np.testing.assert_array_equal(gi, ei)
+        np.testing.assert_array_equal(gv, ev)
+        rate, same = near_tie_disagreement(gi, oi, ol, wl.row_visible, k)
+        print(f"disagreement rate {rate:.2e}, identical rows {same:.3f}")
+
+
+def test_filter_path_falls_back_when_sampling_misleads():
+    # Scores are high only in sampled key tiles (every 2nd tile for k=256), so
+    # the sample threshold keeps fewer than k candidates and rows must take the
+    # dense fallback.  Integer data: the result must still be exact.
+    k, H, npos = 256, 1, 6000
+    wl = W.make_workload("fb", seed=1, ctx_tokens=[4 * npos], rows_per_req=[7], k=k,
+                         dist="zero", wdist="ones", heads=H, shuffle_pages=False)
+    keys = wl.k_cache.reshape(-1, 128)
+    j = np.arange(keys.shape[0])
+    keys[:, 0] = ((j % 97) + np.where((j // 128) % 2 == 0, 100, 0)).astype(np.float16)
+    wl.q[:, 0, 0] = 1
+    oi, ov, _ = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                           wl.row_visible, k, ld=wl.ld)
+    for path in (qsa.PATH_FILTER, qsa.PATH_DENSE):
+        gi, gv = gpu_select(wl, path=path)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+
+
+def test_filter_path_falls_back_on_candidate_overflow():
+    # every score equal (w = 0): the threshold admits every position, more than
+    # the candidate capacity -> fallback; the answer is the pure tie order.
+    k = 300
+    wl = W.make_workload("of", seed=2, ctx_tokens=[40000], rows_per_req=[5], k=k,
+                         dist="int4", wdist="zero")
+    gi, gv = gpu_select(wl, path=qsa.PATH_FILTER)
+    for r in range(wl.rows):
+        n = min(k, wl.row_visible[r])
+        np.testing.assert_array_equal(gi[r, :n], np.arange(n))
+        assert np.all(gv[r, :n] == 0) and not np.any(np.signbit(gv[r, :n]))
+
+
+def test_zero_visible_rows_and_k_above_visible():
+    wl = W.make_workload("z", seed=3, ctx_tokens=[3, 20, 700], rows_per_req=[3, 4, 2], k=200,
+                         dist="int4")
+    assert (wl.row_visible == 0).any() and (wl.row_visible < 200).all()
+    oi, ov, _ = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                           wl.row_visible, wl.k, ld=wl.ld)
+    for path in (qsa.PATH_DENSE, qsa.PATH_FILTER):
+        gi, gv = gpu_select(wl, path=path)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+
+
+def test_k_equals_one_and_max_k():
+    wl = W.make_workload("k", seed=4, ctx_tokens=[40000], rows_per_req=[3], k=1, dist="int4")
+    d = to_device(wl)
+    ol = oracle.score(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req, wl.row_visible, wl.ld)
+    for k in (1, qsa.QSA_MAX_K):
+        oi, ov = oracle.select(ol, wl.row_visible, k)
+        gi, gv = gpu_select(wl, d, k=k)
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov)
+
+
+# ---------------------------------------------------- selector on its own ----
+
+@pytest.mark.parametrize("n,k,kind", [(5000, 700, "gauss"), (30000, 2048, "gauss"),
+                                      (60000, 2048, "ties"), (60000, 4000, "few"),
+                                      (9000, 8192, "ties"), (100, 64, "ties")])
+def test_topk_exact_on_oracle_style_logits(n, k, kind):
+    rng = np.random.default_rng(n + k)
+    R = 9
+    if kind == "gauss":
+        lg = rng.standard_normal((R, n)).astype(np.float32)
+    elif kind == "ties":
+        lg = rng.integers(-20, 21, size=(R, n)).astype(np.float32) * np.float32(0.25)
+    else:
+        lg = rng.integers(0, 3, size=(R, n)).astype(np.float32)
+    lg[0, :] = 0.0
+    lg[1, ::2] = -0.0                      # -0 ties with +0
+    vis = rng.integers(0, n + 1, size=R).astype(np.int32)
+    vis[:3] = n
+    oi, ov = oracle.select(lg, vis, k)
+    gi, gv = qsa.topk_exact(torch.from_numpy(lg).cuda(), torch.from_numpy(vis).cuda(), k)
+    gi, gv = gi.cpu().numpy(), gv.cpu().numpy()
+    np.testing.assert_array_equal(gi, oi)
+    # values: the canonical +0 for either zero
+    np.testing.assert_array_equal(gv, ov + np.float32(0.0))
+
+
+# -------------------------------------------------------- device checks ----
+
+def test_bad_page_id_is_reported_not_faulted():
+    wl = W.make_workload("bp", seed=5, ctx_tokens=[2000], rows_per_req=[4], k=16, dist="int4")
+    bt = wl.block_table.copy()
+    bt[0, 3] = wl.k_cache.shape[0] + 1000
+    d = to_device(wl)
+    d["keys"] = qsa.PagedKeys(d["keys"].k_cache, torch.from_numpy(bt).cuda())
+    qsa.select_paged_tokens(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"], wl.k)
+    assert qsa.get_device_status() == qsa.QSA_ERR_BAD_PAGE
+    assert qsa.get_device_status() == qsa.QSA_OK          # read-and-clear
+    gi, _ = gpu_select(wl, d=to_device(wl))                # the context is still usable
+    assert gi.shape == (wl.rows, wl.k)
+
+
+def test_row_request_out_of_range_is_reported():
+    wl = W.make_workload("rr", seed=6, ctx_tokens=[2000], rows_per_req=[4], k=16, dist="int4")
+    d = to_device(wl)
+    d["row_req"][1] = 7
+    idx, _ = qsa.select_paged_tokens(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"],
+                                     wl.k)
+    assert qsa.get_device_status() == qsa.QSA_ERR_INVALID_ARG
+    assert torch.all(idx[1] == -1)
+
+
+def test_deterministic_and_counts_launches():
+    wl = W.make_workload("det", seed=7, ctx_tokens=[30000], rows_per_req=[100], k=512)
+    d = to_device(wl)
+    a = gpu_select(wl, d)
+    n = qsa.last_launch_count()
+    b = gpu_select(wl, d)
+    assert n >= 3
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------------ full-size configs ----
+
+def _sample_rows(R, rng, n=6):
+    return np.unique(np.r_[0, R - 1, rng.choice(R, size=n, replace=False)])
+
+
+@pytest.mark.parametrize("name", ["bench", "decode", "ties", "long"])
+def test_full_size_config(name):
+    wl = W.CONFIGS[name]()
+    d = to_device(wl)
+    gi, gv = gpu_select(wl, d)
+    check_sorted_valid(gi[:: max(1, wl.rows // 256)], gv[:: max(1, wl.rows // 256)],
+                       wl.row_visible[:: max(1, wl.rows // 256)], wl.k)
+    rows = _sample_rows(wl.rows, np.random.default_rng(11))
+    ol, oi, ov = _oracle_rows(wl, rows)
+    if name == "ties":
+        np.testing.assert_array_equal(gi[rows], oi)
+        np.testing.assert_array_equal(gv[rows], ov)
+    else:
+        rate, same = near_tie_disagreement(gi[rows], oi, ol, wl.row_visible[rows], wl.k)
+        print(f"{name}: disagreement rate {rate:.2e}, identical rows {same:.3f}")
+    if name == "bench":
+        # both paths select exactly the same positions on the same logits
+        gi2, gv2 = gpu_select(wl, d, path=qsa.PATH_DENSE)
+        gi3, gv3 = gpu_select(wl, d, path=qsa.PATH_FILTER)
+        np.testing.assert_array_equal(gi2, gi3)
+        np.testing.assert_array_equal(gv2, gv3)
