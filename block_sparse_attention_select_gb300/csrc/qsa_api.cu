@@ -124,13 +124,6 @@ int32_t pow2_floor(double x)
     return p;
 }
 
-int32_t pow2_ceil(int32_t x)
-{
-    int32_t p = 1;
-    while (p < x) p *= 2;
-    return p;
-}
-
 // Sampled-threshold filter parameters for a top-k of k over rows of up to max_len.
 struct FilterShape {
     int32_t stride;     // sample every stride-th key tile
@@ -157,7 +150,7 @@ bool use_filter(int64_t max_len, int32_t k)
 }
 
 struct Layout {
-    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, cnt, flag, cand;
+    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_cnt, cand;
     size_t total;
 };
 
@@ -175,9 +168,10 @@ Layout layout(int32_t R, int64_t ld, int32_t k)
     const FilterShape f = filter_shape(ld, std::max(k, 1));
     L.sample = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(f.sample_ld));
     L.tau = take(sizeof(float) * R);
-    L.cnt = take(sizeof(int32_t) * R);
     L.flag = take(sizeof(int32_t) * R);
-    L.cand = take(sizeof(uint2) * static_cast<size_t>(R) * static_cast<size_t>(f.cap));
+    const size_t tiles = static_cast<size_t>((ld + TILE_M - 1) / TILE_M);
+    L.cand_cnt = take(static_cast<size_t>(R) * tiles * 4);
+    L.cand = take(sizeof(uint2) * static_cast<size_t>(R) * tiles * 4 * CAND_SLOTS);
     L.total = o;
     return L;
 }
@@ -429,8 +423,7 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
     p.row_vis = row_visible;
     p.out_idx = out_idx;
     p.out_val = out_val;
-    p.sort_cap = pow2_ceil(k);
-    p.smem_cap = std::max(8192, p.sort_cap);
+    p.smem_cap = std::max(8192, k);
     p.status = d->status;
     return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, stream); }));
 }
@@ -468,7 +461,6 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     sel.plan = reinterpret_cast<Plan *>(at(s.L.plan));
     sel.out_idx = out_idx;
     sel.out_val = out_val;
-    sel.sort_cap = pow2_ceil(k);
     sel.status = d->status;
     sel.row_flag = reinterpret_cast<int32_t *>(at(s.L.flag));
 
@@ -480,14 +472,15 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
         sel.mode = SEL_DENSE;
         sel.logits = logits;
         sel.ld = ld;
-        sel.smem_cap = std::max(8192, sel.sort_cap);
+        sel.smem_cap = std::max(8192, k);
         return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, stream); }));
     }
 
     float *sample = reinterpret_cast<float *>(at(s.L.sample));
     float *tau = reinterpret_cast<float *>(at(s.L.tau));
-    int32_t *cnt = reinterpret_cast<int32_t *>(at(s.L.cnt));
+    uint8_t *cand_cnt = reinterpret_cast<uint8_t *>(at(s.L.cand_cnt));
     uint2 *cand = reinterpret_cast<uint2 *>(at(s.L.cand));
+    const int32_t tiles_ld = static_cast<int32_t>((ld + TILE_M - 1) / TILE_M);
 
     // 1. scores of every stride-th key tile
     s.sp.mode = SCORE_SAMPLE;
@@ -502,25 +495,23 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     th.cap = f.cap;
     th.sample_stride = f.stride;
     th.tau = tau;
-    th.cand_count_w = cnt;
     th.oversample = OVERSAMPLE;
-    th.smem_cap = 0;
-    th.sort_cap = 0;
+    th.smem_cap = static_cast<int32_t>(f.sample_ld);
     if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, stream); }))) != QSA_OK) return st;
     // 3. full scoring pass keeping only scores >= tau_r
     s.sp.mode = SCORE_FILTER;
     s.sp.tau = tau;
     s.sp.cand = cand;
-    s.sp.cand_count = cnt;
-    s.sp.cap = f.cap;
+    s.sp.cand_cnt = cand_cnt;
+    s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
     // 4. exact top-k of each candidate list; rows whose list cannot be trusted
     //    (fewer than k candidates or overflow) are flagged
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
     cs.cand = cand;
-    cs.cand_count = cnt;
-    cs.cap = f.cap;
+    cs.cand_cnt = cand_cnt;
+    cs.tiles_ld = tiles_ld;
     cs.smem_cap = f.cap;
     if ((st = launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, stream); }))) != QSA_OK) return st;
     // 5. flagged rows only: dense scores, then the dense selector
@@ -533,7 +524,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     ds.mode = SEL_DENSE_FLAGGED;
     ds.logits = logits;
     ds.ld = ld;
-    ds.smem_cap = std::max(8192, sel.sort_cap);
+    ds.smem_cap = std::max(8192, k);
     return launch_rc(timed(K_SEL_FLAGGED, stream, [&] { return launch_select(ds, stream); }));
 }
 

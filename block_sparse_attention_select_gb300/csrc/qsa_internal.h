@@ -16,8 +16,9 @@ constexpr int TILE_M = 128;      // positions per scorer tile (MMA M, TMEM lanes
 constexpr int HEAD_DIM = 128;    // index-key dimension (MMA K per head)
 constexpr int N_MAX = 256;       // MMA N: (query rows of a group) x heads
 constexpr int KSTAGES = 4;       // key tiles in flight per CTA
-constexpr int SCORE_THREADS = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
-constexpr int EPI_WARPS = 8;
+constexpr int EPI_WARPS = 16;    // 4 per TMEM lane quarter, each owning 64 accumulator columns
+constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, then epilogue
+constexpr int CAND_SLOTS = 16;   // candidate slots per (row, key tile, 32-position quarter)
 
 // A group: consecutive query rows of one request that share every key tile.
 struct Group {
@@ -25,6 +26,7 @@ struct Group {
     int32_t nrows;     // rows in the group (<= N_MAX / H)
     int32_t req;       // request index (row of the block table)
     int32_t vmax;      // longest visible length in the group (positions)
+    int32_t vmin;      // shortest visible length in the group
 };
 
 // Plan written by the plan kernel into the workspace.
@@ -63,9 +65,9 @@ struct ScoreParams {
     int64_t ld;
     int32_t pad_inf;            // LOGITS: write -inf for V_r <= j < tile end (j < ld)
     const float *tau;           // FILTER: per-row threshold
-    uint2 *cand;                // FILTER: [R, cap] (score bits, position)
-    int32_t *cand_count;        // FILTER: [R]
-    int32_t cap;
+    uint2 *cand;                // FILTER: [R, tiles_ld, 4, CAND_SLOTS] (score bits, position)
+    uint8_t *cand_cnt;          // FILTER: [R, tiles_ld, 4] candidates found per quarter tile
+    int32_t tiles_ld;           // key tiles per row in the candidate arrays
     const int32_t *row_flag;    // FALLBACK: rows to redo
     uint32_t *status;
     uint64_t wait_limit_ns;
@@ -86,21 +88,20 @@ struct SelectParams {
     int64_t ld;
     int64_t max_len;            // largest valid V_r (longer rows are clamped and flagged)
     const int32_t *row_vis;     // V_r
-    const uint2 *cand;          // CAND
-    const int32_t *cand_count;
-    int32_t cap;
+    const uint2 *cand;          // CAND: slots written by the filter scorer
+    const uint8_t *cand_cnt;
+    int32_t tiles_ld;
+    int32_t cap;                // THRESH: rows up to this length keep every position
     int32_t *row_flag;          // CAND: set for rows that need the dense path
     Plan *plan;
     // THRESH
     int32_t sample_stride;
     float *tau;
-    int32_t *cand_count_w;
     float oversample;           // expected candidates / k
     // outputs
     int32_t *out_idx;
     float *out_val;
-    int32_t smem_cap;           // C: elements the CTA can hold
-    int32_t sort_cap;           // K_pad: power of two >= min(k, C)
+    int32_t smem_cap;           // elements the CTA can hold in shared memory
     uint32_t *status;
 };
 
@@ -112,7 +113,7 @@ int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, i
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid,
                  void *stream);
 int launch_select(const SelectParams &p, void *stream);
-size_t select_smem_bytes(int32_t smem_cap, int32_t sort_cap);
+size_t select_smem_bytes(int32_t smem_cap);
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream);
 

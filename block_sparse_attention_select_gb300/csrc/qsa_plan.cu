@@ -99,10 +99,14 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     for (int32_t g = tid; g < n_groups; g += PLAN_THREADS) {
         const int32_t r0 = groups[g].row0;
         const int32_t r1 = g + 1 < n_groups ? groups[g + 1].row0 : R;
-        int32_t vmax = 0;
-        for (int32_t r = r0; r < r1; ++r) vmax = max(vmax, row_vis[r]);
+        int32_t vmax = 0, vmin = INT32_MAX;
+        for (int32_t r = r0; r < r1; ++r) {
+            vmax = max(vmax, row_vis[r]);
+            vmin = min(vmin, row_vis[r]);
+        }
         groups[g].nrows = r1 - r0;
         groups[g].vmax = vmax;
+        groups[g].vmin = vmin;
     }
     __syncthreads();
 

@@ -8,8 +8,9 @@
 // (TMEM columns, <= 256) x K = 128.  Keys are the A operand because they
 // differ per tile, the group's queries are the B operand and stay resident in
 // shared memory while the CTA walks the group's key tiles.  One persistent CTA
-// per SM: warp 0 issues TMA, warp 1 issues MMAs, warps 2..9 drain TMEM
-// (double-buffered accumulators, 2 x 256 columns) and write the results.
+// per SM: warp 0 issues TMA, warp 1 issues MMAs, 16 epilogue warps drain TMEM
+// (double-buffered accumulators, 2 x 256 columns; each warp owns one lane
+// quarter x 64 columns) and write the results.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -38,16 +39,18 @@ struct __align__(8) Ctrl {
     int32_t abort;
 };
 
-// Group data of one epilogue warp (the rows of its column half), private to
-// that warp so that a group change needs no barrier across warps.
+// Group data of one epilogue warp: the rows of its 64 accumulator columns,
+// private to the warp so that a group change needs no barrier across warps.
 struct EpiRows {
-    float w[N_MAX / 2];        // w[(lr - first row of the half) * H + h]
-    int32_t vis[N_MAX / 2];    // V of each row
-    float tau[N_MAX / 2];      // FILTER threshold of each row
-    int32_t flag[N_MAX / 2];   // FALLBACK: row needs the dense path
+    __align__(16) float w[64];   // w[(row - first row of the warp) * H + h]
+    int32_t vis[64];             // V of each row
+    float tau[64];               // FILTER threshold of each row
+    int32_t flag[64];            // FALLBACK: row needs the dense path
 };
 
+static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
 constexpr uint32_t SMEM_BYTES = SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows) + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Walks the same (group, tile) sequence in every role of a CTA.
 struct ItemCursor {
@@ -84,56 +87,73 @@ __device__ __forceinline__ bool group_flagged(const ScoreParams &p, const Group 
 }
 
 template <int H>
-__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
-                                              int32_t tile, uint32_t taddr_row, int half,
-                                              int lane, int32_t p_in_tile)
+__device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
 {
-    constexpr int ROWS_PER_CHUNK = 32 / H;
-    constexpr int ROWS_PER_HALF = (N_MAX / 2) / H;
-    const int32_t ncols = gr.nrows * H;
-    const int32_t j = tile * TILE_M + p_in_tile;
-#pragma unroll 1
-    for (int ch = 0; ch < 4; ++ch) {
-        const int32_t col0 = half * 128 + ch * 32;
-        if (col0 >= ncols) break;                       // warp-uniform
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(taddr_row + static_cast<uint32_t>(col0), v);
-        tmem_ld_wait();
-        const int32_t lr0 = col0 / H;
+    if constexpr (H == 1) {
+        out[0] = w[el];
+    } else if constexpr (H == 2) {
+        const float2 a = reinterpret_cast<const float2 *>(w)[el];
+        out[0] = a.x; out[1] = a.y;
+    } else {
 #pragma unroll
-        for (int i = 0; i < ROWS_PER_CHUNK; ++i) {
-            const int32_t lr = lr0 + i;
-            if (lr >= gr.nrows) break;                  // warp-uniform
-            const int32_t el = lr - half * ROWS_PER_HALF;      // row within this warp's half
+        for (int q = 0; q < H / 4; ++q) {
+            const float4 a = reinterpret_cast<const float4 *>(w)[el * (H / 4) + q];
+            out[4 * q] = a.x; out[4 * q + 1] = a.y; out[4 * q + 2] = a.z; out[4 * q + 3] = a.w;
+        }
+    }
+}
+
+// Drains this warp's 64 accumulator columns (64 / H query rows) of one tile.
+// Lane i holds key position tile * 128 + quarter * 32 + i.
+template <int H, int MODE>
+__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
+                                              int32_t tile, uint32_t taddr, int cq, int quarter,
+                                              int lane, uint32_t lt_mask)
+{
+    constexpr int RPC = 32 / H;       // rows per 32-column chunk
+    constexpr int RPW = 64 / H;       // rows per warp
+    const int32_t first = cq * RPW;
+    const int32_t nmine = min(RPW, gr.nrows - first);
+    if (nmine <= 0) return;
+    const int32_t p_in_tile = quarter * 32 + lane;
+    const int32_t j = tile * TILE_M + p_in_tile;
+    const bool full = (tile + 1) * TILE_M <= gr.vmin;       // every row sees the whole tile
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        const int32_t c0 = ch * RPC;
+        if (c0 >= nmine) break;                              // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + ch * 32), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < RPC; ++i) {
+            const int32_t el = c0 + i;
+            if (el >= nmine) break;                          // warp-uniform
+            if (MODE == SCORE_FALLBACK && !e.flag[el]) continue;
+            float wv[H];
+            load_w<H>(e.w, el, wv);
             float s = 0.0f;
 #pragma unroll
-            for (int h = 0; h < H; ++h)
-                s = fmaf(e.w[el * H + h], fmaxf(__uint_as_float(v[i * H + h]), 0.0f), s);
-            const int32_t r = gr.row0 + lr;
-            const int32_t V = e.vis[el];
-            const bool ok = j < V;
-            if (p.mode == SCORE_FILTER) {
+            for (int h = 0; h < H; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(v[i * H + h]), 0.0f), s);
+            const int32_t r = gr.row0 + first + el;
+            const bool ok = full || j < e.vis[el];
+            if constexpr (MODE == SCORE_FILTER) {
                 const bool take = ok && s >= e.tau[el];
                 const uint32_t m = __ballot_sync(0xffffffffu, take);
-                if (m) {
-                    const int leader = __ffs(m) - 1;
-                    int32_t base = 0;
-                    if (lane == leader) base = atomicAdd(p.cand_count + r, __popc(m));
-                    base = __shfl_sync(0xffffffffu, base, leader);
-                    if (take) {
-                        const int32_t slot = base + __popc(m & ((1u << lane) - 1u));
-                        if (slot < p.cap)
-                            p.cand[static_cast<int64_t>(r) * p.cap + slot] =
-                                make_uint2(__float_as_uint(s), static_cast<uint32_t>(j));
-                    }
+                const int64_t q_slot = (static_cast<int64_t>(r) * p.tiles_ld + tile) * 4 + quarter;
+                if (lane == 0) p.cand_cnt[q_slot] = static_cast<uint8_t>(__popc(m));
+                if (take) {
+                    const int32_t slot = __popc(m & lt_mask);
+                    if (slot < CAND_SLOTS)
+                        p.cand[q_slot * CAND_SLOTS + slot] =
+                            make_uint2(__float_as_uint(s), static_cast<uint32_t>(j));
                 }
-            } else if (p.mode == SCORE_SAMPLE) {
+            } else if constexpr (MODE == SCORE_SAMPLE) {
                 if (ok) {
                     const int64_t col = static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
                     p.out[static_cast<int64_t>(r) * p.ld + col] = s;
                 }
             } else {
-                if (p.mode == SCORE_FALLBACK && !e.flag[el]) continue;
                 float *dst = p.out + static_cast<int64_t>(r) * p.ld + j;
                 if (ok) *dst = s;
                 else if (p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
@@ -294,9 +314,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     } else {
         // --------------------------------------------------- epilogue --
         const int ew = warp - 2;
-        const int quarter = warp & 3;
-        const int half = ew >> 2;
-        const int32_t p_in_tile = quarter * 32 + lane;
+        const int quarter = warp & 3;           // TMEM lanes this warp may read
+        const int cq = ew >> 2;                 // accumulator columns [cq * 64, +64)
+        uint32_t lt_mask;
+        asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt_mask));
         EpiRows &er = epi_rows[ew];
         ItemCursor cur;
         cur.init(prefix, n_groups, it0, it1, stride);
@@ -311,10 +332,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 gr = p.groups[cur_g];
                 skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
                 if (skip_group) continue;
-                // this warp's rows: [half * rows_per_half, +rows_per_half) of the group
-                constexpr int32_t RPH = (N_MAX / 2) / H;
-                const int32_t first = half * RPH;
-                const int32_t nmine = max(0, min(RPH, gr.nrows - first));
+                constexpr int32_t RPW = 64 / H;
+                const int32_t first = cq * RPW;
+                const int32_t nmine = max(0, min(RPW, gr.nrows - first));
                 __syncwarp();
                 for (int32_t i = lane; i < nmine * H; i += 32)
                     er.w[i] = __ldg(p.w + static_cast<int64_t>(gr.row0 + first) * H + i);
@@ -331,7 +351,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             if (!mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * 256u;
-            epilogue_tile<H>(p, er, gr, cur.tile(), taddr, half, lane, p_in_tile);
+            const int32_t t = cur.tile();
+            switch (p.mode) {
+            case SCORE_FILTER: epilogue_tile<H, SCORE_FILTER>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
+            case SCORE_SAMPLE: epilogue_tile<H, SCORE_SAMPLE>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
+            case SCORE_FALLBACK: epilogue_tile<H, SCORE_FALLBACK>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
+            default: epilogue_tile<H, SCORE_LOGITS>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.acc_empty[b]);
