@@ -505,27 +505,26 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.cand_cnt = cand_cnt;
     s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
-    // 4. exact top-k of each candidate list; rows whose list cannot be trusted
-    //    (fewer than k candidates or overflow) are flagged
+    // 4. exact top-k of each candidate list; a row whose list cannot be trusted
+    //    (fewer than k candidates, or a slot overflow) is re-scored in full by
+    //    the selector itself and selected densely
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
     cs.cand = cand;
     cs.cand_cnt = cand_cnt;
     cs.tiles_ld = tiles_ld;
     cs.smem_cap = f.cap;
-    if ((st = launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, stream); }))) != QSA_OK) return st;
-    // 5. flagged rows only: dense scores, then the dense selector
-    s.sp.mode = SCORE_FALLBACK;
-    s.sp.out = logits;
-    s.sp.ld = ld;
-    s.sp.row_flag = sel.row_flag;
-    if ((st = launch_rc(timed(K_SCORE_FALLBACK, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
-    SelectParams ds = sel;
-    ds.mode = SEL_DENSE_FLAGGED;
-    ds.logits = logits;
-    ds.ld = ld;
-    ds.smem_cap = std::max(8192, k);
-    return launch_rc(timed(K_SEL_FLAGGED, stream, [&] { return launch_select(ds, stream); }));
+    cs.q = static_cast<const uint16_t *>(q);
+    cs.w = w;
+    cs.k_cache = static_cast<const uint16_t *>(keys->k_cache);
+    cs.block_table = keys->block_table;
+    cs.row_req = row_req;
+    cs.H = H;
+    cs.max_pages = keys->max_pages_per_req;
+    cs.num_pages = keys->num_pages;
+    cs.page_pos = keys->page_positions;
+    cs.fb_logits = logits;
+    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, stream); }));
 }
 
 }  // extern "C"

@@ -41,7 +41,6 @@ enum ScoreMode : int32_t {
     SCORE_LOGITS = 0,      // logits for j < V_r (and -inf up to the tile end when pad_inf)
     SCORE_SAMPLE = 1,      // sampled tiles only, into the sample matrix
     SCORE_FILTER = 2,      // append (score, j) with score >= tau_r to the candidate lists
-    SCORE_FALLBACK = 3,    // like LOGITS, only for groups holding a flagged row
 };
 
 struct ScoreParams {
@@ -68,7 +67,6 @@ struct ScoreParams {
     uint2 *cand;                // FILTER: [R, tiles_ld, 4, CAND_SLOTS] (score bits, position)
     uint8_t *cand_cnt;          // FILTER: [R, tiles_ld, 4] candidates found per quarter tile
     int32_t tiles_ld;           // key tiles per row in the candidate arrays
-    const int32_t *row_flag;    // FALLBACK: rows to redo
     uint32_t *status;
     uint64_t wait_limit_ns;
 };
@@ -76,8 +74,7 @@ struct ScoreParams {
 enum SelectMode : int32_t {
     SEL_DENSE = 0,      // row r = logits[r, 0:V_r]
     SEL_CAND = 1,       // row r = candidate list; flags the row when it is unusable
-    SEL_THRESH = 2,     // row r = sample row; writes tau_r, clears cand_count[r]
-    SEL_DENSE_FLAGGED = 3,  // like DENSE, only rows whose flag is set
+    SEL_THRESH = 2,     // row r = sample row; writes tau_r
 };
 
 struct SelectParams {
@@ -92,8 +89,17 @@ struct SelectParams {
     const uint8_t *cand_cnt;
     int32_t tiles_ld;
     int32_t cap;                // THRESH: rows up to this length keep every position
-    int32_t *row_flag;          // CAND: set for rows that need the dense path
+    int32_t *row_flag;          // CAND: set for rows that took the dense fallback
     Plan *plan;
+    // CAND fallback: a row whose candidate list cannot be trusted is re-scored
+    // here (plain FP32 arithmetic) into fb_logits[r * max_len ...] and selected densely
+    const uint16_t *q;          // FP16 bits [R, H, 128]
+    const float *w;             // [R, H]
+    const uint16_t *k_cache;    // FP16 bits [num_pages, page_pos, 128]
+    const int32_t *block_table;
+    const int32_t *row_req;
+    int32_t H, max_pages, num_pages, page_pos;
+    float *fb_logits;
     // THRESH
     int32_t sample_stride;
     float *tau;

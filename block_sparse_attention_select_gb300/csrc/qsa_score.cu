@@ -45,7 +45,6 @@ struct EpiRows {
     __align__(16) float w[64];   // w[(row - first row of the warp) * H + h]
     int32_t vis[64];             // V of each row
     float tau[64];               // FILTER threshold of each row
-    int32_t flag[64];            // FALLBACK: row needs the dense path
 };
 
 static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
@@ -79,11 +78,35 @@ struct ItemCursor {
     __device__ void next() { ++it; }
 };
 
-__device__ __forceinline__ bool group_flagged(const ScoreParams &p, const Group &gr)
+// d = a * b + c on packed FP32 pairs (one instruction on sm_100-family SMs).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
 {
-    for (int32_t r = 0; r < gr.nrows; ++r)
-        if (__ldg(p.row_flag + gr.row0 + r)) return true;
-    return false;
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// sum_h w[h] * max(acc[h], 0) for one (row, position).  Heads are paired
+// into packed FMAs; the accumulation starts from +0 so the result is never -0.
+template <int H>
+__device__ __forceinline__ float weighted_relu_sum(const float *w, const uint32_t *acc)
+{
+    if constexpr (H == 1) {
+        return fmaf(w[0], fmaxf(__uint_as_float(acc[0]), 0.0f), 0.0f);
+    } else {
+        float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < H; h += 2) {
+            const float2 a = make_float2(fmaxf(__uint_as_float(acc[h]), 0.0f),
+                                         fmaxf(__uint_as_float(acc[h + 1]), 0.0f));
+            s = ffma2(make_float2(w[h], w[h + 1]), a, s);
+        }
+        return s.x + s.y;
+    }
 }
 
 template <int H>
@@ -104,20 +127,26 @@ __device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
 }
 
 // Drains this warp's 64 accumulator columns (64 / H query rows) of one tile.
-// Lane i holds key position tile * 128 + quarter * 32 + i.
-template <int H, int MODE>
-__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
+// Lane i holds key position tile * 128 + quarter * 32 + i.  FULL: every row
+// of the group sees the whole tile, so no per-element visibility test.
+template <int H, int MODE, bool FULL>
+__device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRows &e, const Group &gr,
                                               int32_t tile, uint32_t taddr, int cq, int quarter,
-                                              int lane, uint32_t lt_mask)
+                                              int lane, uint32_t lt_mask, int32_t nmine)
 {
     constexpr int RPC = 32 / H;       // rows per 32-column chunk
     constexpr int RPW = 64 / H;       // rows per warp
-    const int32_t first = cq * RPW;
-    const int32_t nmine = min(RPW, gr.nrows - first);
-    if (nmine <= 0) return;
     const int32_t p_in_tile = quarter * 32 + lane;
     const int32_t j = tile * TILE_M + p_in_tile;
-    const bool full = (tile + 1) * TILE_M <= gr.vmin;       // every row sees the whole tile
+    const int64_t r0 = static_cast<int64_t>(gr.row0) + cq * RPW;     // first row of this warp
+    // per-mode row-0 addresses and per-row strides
+    const int64_t slot0 = (r0 * p.tiles_ld + tile) * 4 + quarter;   // FILTER
+    const int64_t slot_stride = static_cast<int64_t>(p.tiles_ld) * 4;
+    float *out0 = nullptr;
+    if constexpr (MODE == SCORE_SAMPLE)
+        out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
+    else if constexpr (MODE != SCORE_FILTER)
+        out0 = p.out + r0 * p.ld + j;
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int32_t c0 = ch * RPC;
@@ -129,37 +158,44 @@ __device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRow
         for (int i = 0; i < RPC; ++i) {
             const int32_t el = c0 + i;
             if (el >= nmine) break;                          // warp-uniform
-            if (MODE == SCORE_FALLBACK && !e.flag[el]) continue;
             float wv[H];
             load_w<H>(e.w, el, wv);
-            float s = 0.0f;
-#pragma unroll
-            for (int h = 0; h < H; ++h) s = fmaf(wv[h], fmaxf(__uint_as_float(v[i * H + h]), 0.0f), s);
-            const int32_t r = gr.row0 + first + el;
-            const bool ok = full || j < e.vis[el];
+            const float s = weighted_relu_sum<H>(wv, v + i * H);
+            const bool ok = FULL || j < e.vis[el];
             if constexpr (MODE == SCORE_FILTER) {
                 const bool take = ok && s >= e.tau[el];
                 const uint32_t m = __ballot_sync(0xffffffffu, take);
-                const int64_t q_slot = (static_cast<int64_t>(r) * p.tiles_ld + tile) * 4 + quarter;
+                const int64_t q_slot = slot0 + el * slot_stride;
                 if (lane == 0) p.cand_cnt[q_slot] = static_cast<uint8_t>(__popc(m));
-                if (take) {
+                if (m) {
                     const int32_t slot = __popc(m & lt_mask);
-                    if (slot < CAND_SLOTS)
+                    if (take && slot < CAND_SLOTS)
                         p.cand[q_slot * CAND_SLOTS + slot] =
                             make_uint2(__float_as_uint(s), static_cast<uint32_t>(j));
                 }
             } else if constexpr (MODE == SCORE_SAMPLE) {
-                if (ok) {
-                    const int64_t col = static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
-                    p.out[static_cast<int64_t>(r) * p.ld + col] = s;
-                }
+                if (ok) out0[el * p.ld] = s;
             } else {
-                float *dst = p.out + static_cast<int64_t>(r) * p.ld + j;
+                float *dst = out0 + el * p.ld;
                 if (ok) *dst = s;
                 else if (p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
             }
         }
     }
+}
+
+template <int H, int MODE>
+__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
+                                              int32_t tile, uint32_t taddr, int cq, int quarter,
+                                              int lane, uint32_t lt_mask)
+{
+    constexpr int RPW = 64 / H;
+    const int32_t nmine = min(RPW, gr.nrows - cq * RPW);
+    if (nmine <= 0) return;
+    if ((tile + 1) * TILE_M <= gr.vmin)
+        epilogue_rows<H, MODE, true>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+    else
+        epilogue_rows<H, MODE, false>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
 }
 
 template <int H>
@@ -178,7 +214,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    if (p.mode == SCORE_FALLBACK && p.plan->any_fallback == 0) return;
     const bool sampled = p.mode == SCORE_SAMPLE;
     const int32_t n_items = sampled ? p.plan->n_sample_items : p.plan->n_items;
     const int32_t it0 = static_cast<int32_t>((static_cast<int64_t>(n_items) * blockIdx.x) / gridDim.x);
@@ -221,49 +256,74 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
-            ItemCursor cur;
-            cur.init(prefix, n_groups, it0, it1, stride);
-            int32_t cur_g = -1, q_loads = 0, stage = 0;
-            uint32_t phase = 0;
-            bool skip_group = false;
-            Group gr{};
-            for (; cur.valid(); cur.next()) {
-                cur.settle();
-                if (cur.g != cur_g) {
-                    cur_g = cur.g;
-                    gr = p.groups[cur_g];
-                    skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
-                    if (skip_group) continue;
-                    if (q_loads > 0 && !mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim)) break;
-                    mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
-                    tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
-                    tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
-                    ++q_loads;
-                }
-                if (skip_group) continue;
-                if (!mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim)) break;
-                const int32_t pos0 = cur.tile() * TILE_M;
-                const int32_t valid = min(TILE_M, gr.vmax - pos0);
-                const int32_t nbox = (valid + p.page_box - 1) / p.page_box;
-                mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
-                uint8_t *dst = k_s + stage * K_STAGE_BYTES;
-                const int32_t *bt = p.block_table + static_cast<int64_t>(gr.req) * p.max_pages;
-                for (int32_t i = 0; i < nbox; ++i) {
-                    const int32_t pos = pos0 + i * p.page_box;
-                    const int32_t pid = __ldg(bt + pos / p.page_pos);
-                    int32_t y;
-                    if (pid >= 0 && pid < p.num_pages) {
-                        y = pid * p.page_pos + (pos % p.page_pos);
-                    } else {
-                        record_error(p.status, ST_BAD_PAGE);
-                        y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+        // The whole warp walks the items; lane i owns key box i of a tile.
+        // Block-table entries are loaded PREFETCH items ahead so that the
+        // page-id round trip never sits in front of a TMA issue.
+        constexpr int PREFETCH = 4;
+        ItemCursor cur, ahead;
+        cur.init(prefix, n_groups, it0, it1, stride);
+        ahead = cur;
+        auto page_id = [&](ItemCursor &a) -> int32_t {
+            if (!a.valid()) return -1;
+            a.settle();
+            const Group ga = p.groups[a.g];
+            const int32_t pos0 = a.tile() * TILE_M;
+            const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) / p.page_box;
+            if (lane >= nbox || ga.req < 0) return -1;
+            const int32_t pos = pos0 + lane * p.page_box;
+            return __ldg(p.block_table + static_cast<int64_t>(ga.req) * p.max_pages + pos / p.page_pos);
+        };
+        int32_t ring[PREFETCH];
+#pragma unroll
+        for (int d = 0; d < PREFETCH; ++d) {
+            ring[d] = page_id(ahead);
+            ahead.next();
+        }
+        int32_t cur_g = -1, q_loads = 0, stage = 0;
+        uint32_t phase = 0;
+        Group gr{};
+        for (; cur.valid(); cur.next()) {
+            cur.settle();
+            const int32_t pid = ring[0];
+#pragma unroll
+            for (int d = 0; d + 1 < PREFETCH; ++d) ring[d] = ring[d + 1];
+            ring[PREFETCH - 1] = page_id(ahead);
+            ahead.next();
+            if (cur.g != cur_g) {
+                cur_g = cur.g;
+                gr = p.groups[cur_g];
+                bool ok = true;
+                if (lane == 0) {
+                    ok = q_loads == 0 || mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                        tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
+                        tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
                     }
-                    tma_load_2d(dst + i * p.page_box * 128, &tmap_k, &c.full[stage], 0, y);
-                    tma_load_2d(dst + K_HALF_BYTES + i * p.page_box * 128, &tmap_k, &c.full[stage], 64, y);
                 }
-                if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
+                if (__any_sync(0xffffffffu, !ok)) break;
+                ++q_loads;
             }
+            if (__any_sync(0xffffffffu, !mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim))) break;
+            const int32_t pos0 = cur.tile() * TILE_M;
+            const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) / p.page_box;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
+            __syncwarp();
+            if (lane < nbox) {
+                const int32_t pos = pos0 + lane * p.page_box;
+                int32_t y;
+                if (pid >= 0 && pid < p.num_pages) {
+                    y = pid * p.page_pos + (pos % p.page_pos);
+                } else {
+                    record_error(p.status, ST_BAD_PAGE);
+                    y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+                }
+                uint8_t *dst = k_s + stage * K_STAGE_BYTES + lane * p.page_box * 128;
+                tma_load_2d(dst, &tmap_k, &c.full[stage], 0, y);
+                tma_load_2d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, y);
+            }
+            if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
@@ -272,14 +332,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             cur.init(prefix, n_groups, it0, it1, stride);
             int32_t cur_g = -1, stage = 0, q_uses = 0;
             uint32_t phase = 0, acc_cnt = 0, idesc = 0;
-            bool skip_group = false, have_q = false;
+            bool have_q = false;
             for (; cur.valid(); cur.next()) {
                 cur.settle();
                 if (cur.g != cur_g) {
                     cur_g = cur.g;
                     const Group gr = p.groups[cur_g];
-                    skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
-                    if (skip_group) continue;
                     if (have_q) umma_commit(&c.q_empty);   // previous group's MMAs done -> q free
                     if (!mbar_wait(&c.q_full, q_uses & 1, abort, lim)) break;
                     ++q_uses;
@@ -287,7 +345,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                     const int n = ((gr.nrows * H + 15) / 16) * 16;
                     idesc = umma_idesc_f16_f32(TILE_M, n);
                 }
-                if (skip_group) continue;
                 if (!mbar_wait(&c.full[stage], phase, abort, lim)) break;
                 const uint32_t b = acc_cnt & 1u;
                 if (!mbar_wait(&c.acc_empty[b], ((acc_cnt >> 1) & 1u) ^ 1u, abort, lim)) break;
@@ -323,15 +380,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         cur.init(prefix, n_groups, it0, it1, stride);
         int32_t cur_g = -1;
         uint32_t acc_cnt = 0;
-        bool skip_group = false;
         Group gr{};
         for (; cur.valid(); cur.next()) {
             cur.settle();
             if (cur.g != cur_g) {
                 cur_g = cur.g;
                 gr = p.groups[cur_g];
-                skip_group = (p.mode == SCORE_FALLBACK) && !group_flagged(p, gr);
-                if (skip_group) continue;
                 constexpr int32_t RPW = 64 / H;
                 const int32_t first = cq * RPW;
                 const int32_t nmine = max(0, min(RPW, gr.nrows - first));
@@ -342,11 +396,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                     const int32_t r = gr.row0 + first + i;
                     er.vis[i] = __ldg(p.row_vis + r);
                     er.tau[i] = p.mode == SCORE_FILTER ? __ldg(p.tau + r) : 0.0f;
-                    er.flag[i] = p.mode == SCORE_FALLBACK ? __ldg(p.row_flag + r) : 1;
                 }
                 __syncwarp();
             }
-            if (skip_group) continue;
             const uint32_t b = acc_cnt & 1u;
             if (!mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim)) break;
             tc_fence_after();
@@ -355,7 +407,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             switch (p.mode) {
             case SCORE_FILTER: epilogue_tile<H, SCORE_FILTER>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
             case SCORE_SAMPLE: epilogue_tile<H, SCORE_SAMPLE>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
-            case SCORE_FALLBACK: epilogue_tile<H, SCORE_FALLBACK>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
             default: epilogue_tile<H, SCORE_LOGITS>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
             }
             tc_fence_before();

@@ -9,6 +9,7 @@
 // ties at the cut are settled on ~position, and the winners are ordered by a
 // counting sort on the top bits of (key32 - cut) followed by small in-bucket
 // sorts.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "qsa_device.cuh"
@@ -27,7 +28,7 @@ struct SelShared {
     uint32_t wtot[32];
     uint32_t red_min[32], red_max[32];
     uint32_t cut_digit, cut_above, count, total, taken, nbig, flag, pad_;
-    uint32_t big[NBINS];              // buckets needing a warp sort
+    uint32_t big[NBINS / 4];          // buckets needing a warp sort (at most k / 17 <= 482)
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -273,7 +274,7 @@ __device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, i
     for (int lv = 0; lv < 3; ++lv) {
         clear_hist(sh);
         for (int32_t i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = score_key(__ldg(row + i));
+            const uint32_t key = score_key(__ldcg(row + i));
             if ((key & pmask) == prefix) atomicAdd(&sh.hist[(key >> level_shift(lv)) & level_mask(lv)], 1u);
         }
         __syncthreads();
@@ -289,7 +290,7 @@ __device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, i
             if (threadIdx.x == 0) sh.count = 0;
             __syncthreads();
             for (int32_t i = threadIdx.x; i < n; i += NT) {
-                const uint32_t key = score_key(__ldg(row + i));
+                const uint32_t key = score_key(__ldcg(row + i));
                 if ((key & pmask) >= prefix) {
                     const uint32_t slot = atomicAdd(&sh.count, 1u);
                     keys[slot] = key;
@@ -314,7 +315,7 @@ __device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ 
     __syncthreads();
     for (int32_t base = 0; base < n; base += NT) {
         const int32_t i = base + threadIdx.x;
-        const uint32_t key = i < n ? score_key(__ldg(row + i)) : 0u;
+        const uint32_t key = i < n ? score_key(__ldcg(row + i)) : 0u;
         if (i < n && key > T) {
             const uint32_t slot = atomicAdd(&sh.count, 1u);
             keys[slot] = key;
@@ -333,7 +334,7 @@ __device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ 
         __syncthreads();
         if (sh.taken >= k_rem) {
             for (int32_t j = base + NT + threadIdx.x; j < n; j += NT) {
-                const uint32_t kj = score_key(__ldg(row + j));
+                const uint32_t kj = score_key(__ldcg(row + j));
                 if (kj > T) {
                     const uint32_t slot = atomicAdd(&sh.count, 1u);
                     keys[slot] = kj;
@@ -347,7 +348,43 @@ __device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ 
     return static_cast<int32_t>(sh.count);
 }
 
-__global__ void __launch_bounds__(NT)
+// Plain FP32 scores of row r, written to `row` (multiply then add, head by
+// head, in the order of the definition).  Used only for rows whose candidate
+// list the filter could not certify; qf is shared scratch for H * 128 floats.
+__device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, float *row, float *qf)
+{
+    const int32_t H = p.H;
+    for (int32_t i = threadIdx.x; i < H * HEAD_DIM; i += NT)
+        qf[i] = __half2float(__ushort_as_half(p.q[static_cast<int64_t>(r) * H * HEAD_DIM + i]));
+    __syncthreads();
+    const int32_t *bt = p.block_table + static_cast<int64_t>(p.row_req[r]) * p.max_pages;
+    for (int32_t j = threadIdx.x; j < V; j += NT) {
+        const int32_t pid = __ldg(bt + j / p.page_pos);
+        float s = 0.0f;
+        if (pid >= 0 && pid < p.num_pages) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(
+                p.k_cache + (static_cast<int64_t>(pid) * p.page_pos + j % p.page_pos) * HEAD_DIM);
+            for (int32_t h = 0; h < H; ++h) {
+                float dot = 0.0f;
+#pragma unroll 1
+                for (int t = 0; t < HEAD_DIM / 8; ++t) {
+                    const uint4 kv = __ldg(kr + t);
+                    const __half *kh = reinterpret_cast<const __half *>(&kv);
+                    const float *qv = qf + h * HEAD_DIM + t * 8;
+#pragma unroll
+                    for (int d = 0; d < 8; ++d) dot = __fadd_rn(dot, __fmul_rn(qv[d], __half2float(kh[d])));
+                }
+                s = __fadd_rn(s, __fmul_rn(__ldg(p.w + static_cast<int64_t>(r) * H + h), dot > 0.0f ? dot : 0.0f));
+            }
+        } else {
+            record_error(p.status, ST_BAD_PAGE);   // as on the tensor path: the page reads as zeros
+        }
+        row[j] = s + 0.0f;
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(NT, 2)
 select_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -382,7 +419,7 @@ select_kernel(const SelectParams p)
             if (n_s <= p.smem_cap) {
                 uint32_t lo = 0xffffffffu, hi = 0u;
                 for (int32_t i = threadIdx.x; i < n_s; i += NT) {
-                    const uint32_t kv = score_key(__ldg(row + i));
+                    const uint32_t kv = score_key(__ldcg(row + i));
                     keys[i] = kv;
                     lo = min(lo, kv);
                     hi = max(hi, kv);
@@ -401,10 +438,9 @@ select_kernel(const SelectParams p)
         return;
     }
 
-    if (p.mode == SEL_DENSE_FLAGGED && p.row_flag[r] == 0) return;
-
-    int32_t n;
+    int32_t n = -1;
     const int32_t kk_target = min(p.k, V);
+    const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
     if (p.mode == SEL_CAND) {
         // gather the candidate slots of the row's key tiles, in position order
         const int32_t ne = ((V + TILE_M - 1) / TILE_M) * 4;
@@ -423,29 +459,33 @@ select_kernel(const SelectParams p)
         const bool any_over = __syncthreads_or(over) != 0;
         const uint32_t total = sh.total;
         if (any_over || total < static_cast<uint32_t>(kk_target) || total > static_cast<uint32_t>(p.smem_cap)) {
+            // the sample misled the threshold for this row: score it in full here
             if (threadIdx.x == 0) {
                 p.row_flag[r] = 1;
                 atomicExch(&p.plan->any_fallback, 1);
             }
-            return;
-        }
-        if (threadIdx.x == 0) p.row_flag[r] = 0;
-        for (int32_t e = e0; e < e1; ++e) {
-            const uint32_t c = cnt[e];
-            for (uint32_t s = 0; s < c; ++s) {
-                const uint2 v = slots[static_cast<int64_t>(e) * CAND_SLOTS + s];
-                keys[base] = score_key(__uint_as_float(v.x));
-                inv[base] = ~v.y;
-                ++base;
+            float *fb = p.fb_logits + static_cast<int64_t>(r) * p.max_len;
+            simt_score_row(p, r, V, fb, reinterpret_cast<float *>(keys));
+            row = fb;
+        } else {
+            if (threadIdx.x == 0) p.row_flag[r] = 0;
+            for (int32_t e = e0; e < e1; ++e) {
+                const uint32_t c = cnt[e];
+                for (uint32_t s = 0; s < c; ++s) {
+                    const uint2 v = slots[static_cast<int64_t>(e) * CAND_SLOTS + s];
+                    keys[base] = score_key(__uint_as_float(v.x));
+                    inv[base] = ~v.y;
+                    ++base;
+                }
             }
+            __syncthreads();
+            n = static_cast<int32_t>(total);
         }
-        __syncthreads();
-        n = static_cast<int32_t>(total);
-    } else {
-        const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+    }
+    if (n < 0) {
         if (V <= p.smem_cap) {
             for (int32_t i = threadIdx.x; i < V; i += NT) {
-                keys[i] = score_key(__ldg(row + i));
+                keys[i] = score_key(__ldcg(row + i));
                 inv[i] = ~static_cast<uint32_t>(i);
             }
             __syncthreads();
