@@ -9,7 +9,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/qsa.h"
+#include "qsa.h"
 #include "qsa_internal.h"
 
 namespace {
@@ -32,6 +32,7 @@ std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int64_t g_cfg_path = 0;
+int64_t g_cfg_scorer = 0;
 uint64_t g_wait_ns = 2000000000ull;
 thread_local int32_t g_launches = 0;
 
@@ -217,7 +218,27 @@ struct ScoreSetup {
     uint8_t *ws;
     CUtensorMap tq, tk;
     ScoreParams sp;
+    bool rows_kernel;   // query rows on TMEM lanes (prefill-sized groups)
+    const void *q;
 };
+
+// Rows-on-lanes scorer for prefill-like batches (many rows per request, at
+// most 4 heads); the positions-on-lanes scorer otherwise (decode batches).
+bool want_rows_kernel(int32_t rows, int32_t H, int32_t num_reqs)
+{
+    // The rows-on-lanes scorer issues M=128 x N=32 MMAs, which measured at
+    // about a quarter of the tensor rate of the N=256 positions-on-lanes
+    // tiles, so it is only used when asked for.
+    (void)rows;
+    (void)num_reqs;
+    return H <= 4 && g_cfg_scorer == 2;
+}
+
+int launch_scorer(const ScoreSetup &s, int grid, void *stream)
+{
+    return s.rows_kernel ? launch_score_rows(s.sp, &s.tk, s.q, grid, stream)
+                         : launch_score(s.sp, &s.tq, &s.tk, grid, stream);
+}
 
 qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
                        const qsa_paged_keys *keys, const int32_t *row_req, const int32_t *row_visible,
@@ -235,8 +256,11 @@ qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t row
                    static_cast<uint32_t>(std::min(keys->page_positions, TILE_M)));
     if (st != QSA_OK) return st;
     auto at = [&](size_t off) { return s.ws + off; };
+    s.rows_kernel = want_rows_kernel(rows, H, keys->num_reqs);
+    s.q = q;
+    const int32_t group_rows = s.rows_kernel ? 128 : N_MAX / H;
     st = launch_rc(timed(K_PLAN, stream, [&] {
-        return launch_plan(row_req, row_visible, rows, H, keys->num_reqs, max_len, sample_stride,
+        return launch_plan(row_req, row_visible, rows, group_rows, keys->num_reqs, max_len, sample_stride,
                            reinterpret_cast<int32_t *>(at(s.L.row_vis)),
                            reinterpret_cast<Group *>(at(s.L.groups)),
                            reinterpret_cast<int32_t *>(at(s.L.item_prefix)),
@@ -310,6 +334,11 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
     if (key == QSA_CFG_PATH) {
         if (value < 0 || value > 2) return QSA_ERR_INVALID_ARG;
         g_cfg_path = value;
+        return QSA_OK;
+    }
+    if (key == QSA_CFG_SCORER) {
+        if (value < 0 || value > 2) return QSA_ERR_INVALID_ARG;
+        g_cfg_scorer = value;
         return QSA_OK;
     }
     if (key == QSA_CFG_KERNEL_TIMING) {
@@ -389,7 +418,7 @@ qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t 
     s.sp.out = logits;
     s.sp.ld = ld_logits;
     s.sp.pad_inf = 1;
-    st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }));
+    st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_scorer(s, d->sms, stream); }));
     if (st != QSA_OK) return st;
     return launch_rc(timed(K_PAD, stream, [&] {
         return launch_pad(logits, ld_logits, rows,
@@ -468,7 +497,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
         s.sp.mode = SCORE_LOGITS;
         s.sp.out = logits;
         s.sp.ld = ld;
-        if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+        if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
         sel.mode = SEL_DENSE;
         sel.logits = logits;
         sel.ld = ld;
@@ -486,7 +515,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.mode = SCORE_SAMPLE;
     s.sp.out = sample;
     s.sp.ld = f.sample_ld;
-    if ((st = launch_rc(timed(K_SCORE_SAMPLE, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+    if ((st = launch_rc(timed(K_SCORE_SAMPLE, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
     // 2. per-row threshold tau_r: a sample quantile that keeps ~OVERSAMPLE * k positions
     SelectParams th = sel;
     th.mode = SEL_THRESH;
@@ -504,7 +533,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.cand = cand;
     s.sp.cand_cnt = cand_cnt;
     s.sp.tiles_ld = tiles_ld;
-    if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_score(s.sp, &s.tq, &s.tk, d->sms, stream); }))) != QSA_OK) return st;
+    if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
     // 4. exact top-k of each candidate list; a row whose list cannot be trusted
     //    (fewer than k candidates, or a slot overflow) is re-scored in full by
     //    the selector itself and selected densely

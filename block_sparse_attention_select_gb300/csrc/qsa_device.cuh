@@ -15,13 +15,6 @@ __device__ __forceinline__ void record_error(uint32_t *status, uint32_t bit)
     if (status) atomicOr(status, bit);
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // ------------------------------------------------------- float <-> key32 --
 // Order-preserving map of a binary32 score to uint32: larger score -> larger
 // key.  -0 is folded onto +0 first so that the two zeros tie.
@@ -86,18 +79,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Bounded wait: returns false (and raises *abort) if the phase did not
-// complete within limit_ns, or if another role already aborted.
+// complete within about limit_ns, or if another role already aborted.  The
+// deadline is kept in SM clock cycles (cheap to read) assuming at most
+// 4 cycles per ns, so the real limit lies between limit_ns / 2 and 2 limit_ns
+// for any clock between 1 and 4 GHz.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = clock64();
+    const long long limit = static_cast<long long>(limit_ns) * 2;
     uint32_t spins = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((++spins & 63u) == 0) {
+        if ((++spins & 255u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > limit_ns) {
+            if (clock64() - t0 > limit) {
                 *abort = 1;
                 return false;
             }

@@ -18,7 +18,7 @@ constexpr int N_MAX = 256;       // MMA N: (query rows of a group) x heads
 constexpr int KSTAGES = 4;       // key tiles in flight per CTA
 constexpr int EPI_WARPS = 16;    // 4 per TMEM lane quarter, each owning 64 accumulator columns
 constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, then epilogue
-constexpr int CAND_SLOTS = 16;   // candidate slots per (row, key tile, 32-position quarter)
+constexpr int CAND_SLOTS = 32;   // candidate slots per (row, key tile, 32-position quarter): one per lane, so a quarter never overflows
 
 // A group: consecutive query rows of one request that share every key tile.
 struct Group {
@@ -112,12 +112,13 @@ struct SelectParams {
 };
 
 // Launchers (one translation unit each); return cudaError_t as int.
-int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t H,
+int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t group_rows,
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
                 uint32_t *status, void *stream);
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid,
                  void *stream);
+int launch_score_rows(const ScoreParams &p, const void *tmap_k, const void *q, int grid, void *stream);
 int launch_select(const SelectParams &p, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);
 uint32_t score_smem_bytes();

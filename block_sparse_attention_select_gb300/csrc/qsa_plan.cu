@@ -145,12 +145,12 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
 
 }  // namespace
 
-int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t H,
+int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t group_rows,
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
                 uint32_t *status, void *stream)
 {
-    const int32_t G = N_MAX / H;
+    const int32_t G = group_rows;
     plan_kernel<<<1, PLAN_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
         row_req, row_visible, R, G, num_reqs, max_len, sample_stride, row_vis, groups,
         item_prefix, sample_prefix, plan, status);

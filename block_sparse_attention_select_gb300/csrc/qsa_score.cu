@@ -43,8 +43,8 @@ struct __align__(8) Ctrl {
 // private to the warp so that a group change needs no barrier across warps.
 struct EpiRows {
     __align__(16) float w[64];   // w[(row - first row of the warp) * H + h]
-    int32_t vis[64];             // V of each row
-    float tau[64];               // FILTER threshold of each row
+    __align__(16) int32_t vis[64];   // V of each row
+    __align__(16) float tau[64];     // FILTER threshold of each row
 };
 
 static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
@@ -134,12 +134,12 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                                               int32_t tile, uint32_t taddr, int cq, int quarter,
                                               int lane, uint32_t lt_mask, int32_t nmine)
 {
-    constexpr int RPC = 32 / H;       // rows per 32-column chunk
-    constexpr int RPW = 64 / H;       // rows per warp
+    constexpr int RPC = 32 / H;          // rows per 32-column chunk
+    constexpr int RPW = 64 / H;          // rows per warp
+    constexpr int B = RPC < 8 ? RPC : 8; // rows scored together: independent chains, no branches
     const int32_t p_in_tile = quarter * 32 + lane;
     const int32_t j = tile * TILE_M + p_in_tile;
     const int64_t r0 = static_cast<int64_t>(gr.row0) + cq * RPW;     // first row of this warp
-    // per-mode row-0 addresses and per-row strides
     const int64_t slot0 = (r0 * p.tiles_ld + tile) * 4 + quarter;   // FILTER
     const int64_t slot_stride = static_cast<int64_t>(p.tiles_ld) * 4;
     float *out0 = nullptr;
@@ -155,30 +155,36 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + ch * 32), v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < RPC; ++i) {
-            const int32_t el = c0 + i;
-            if (el >= nmine) break;                          // warp-uniform
-            float wv[H];
-            load_w<H>(e.w, el, wv);
-            const float s = weighted_relu_sum<H>(wv, v + i * H);
-            const bool ok = FULL || j < e.vis[el];
-            if constexpr (MODE == SCORE_FILTER) {
-                const bool take = ok && s >= e.tau[el];
-                const uint32_t m = __ballot_sync(0xffffffffu, take);
-                const int64_t q_slot = slot0 + el * slot_stride;
-                if (lane == 0) p.cand_cnt[q_slot] = static_cast<uint8_t>(__popc(m));
-                if (m) {
-                    const int32_t slot = __popc(m & lt_mask);
-                    if (take && slot < CAND_SLOTS)
-                        p.cand[q_slot * CAND_SLOTS + slot] =
-                            make_uint2(__float_as_uint(s), static_cast<uint32_t>(j));
+        for (int b0 = 0; b0 < RPC; b0 += B) {
+            if (c0 + b0 >= nmine) break;                     // warp-uniform
+            float s[B];
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+                float wv[H];
+                load_w<H>(e.w, c0 + b0 + i, wv);
+                s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
+            }
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+                const int32_t el = c0 + b0 + i;
+                const bool live = el < nmine;                 // warp-uniform
+                const bool ok = live && (FULL || j < e.vis[el]);
+                if constexpr (MODE == SCORE_FILTER) {
+                    const bool take = ok && s[i] >= e.tau[el];
+                    const uint32_t m = __ballot_sync(0xffffffffu, take);
+                    const int64_t q_slot = slot0 + el * slot_stride;
+                    if (live && lane == 0) p.cand_cnt[q_slot] = static_cast<uint8_t>(__popc(m));
+                    static_assert(CAND_SLOTS >= 32, "one slot per lane");
+                    if (take)
+                        p.cand[q_slot * CAND_SLOTS + __popc(m & lt_mask)] =
+                            make_uint2(__float_as_uint(s[i]), static_cast<uint32_t>(j));
+                } else if constexpr (MODE == SCORE_SAMPLE) {
+                    if (ok) out0[el * p.ld] = s[i];
+                } else {
+                    float *dst = out0 + el * p.ld;
+                    if (ok) *dst = s[i];
+                    else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
                 }
-            } else if constexpr (MODE == SCORE_SAMPLE) {
-                if (ok) out0[el * p.ld] = s;
-            } else {
-                float *dst = out0 + el * p.ld;
-                if (ok) *dst = s;
-                else if (p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
             }
         }
     }
@@ -282,48 +288,57 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         int32_t cur_g = -1, q_loads = 0, stage = 0;
         uint32_t phase = 0;
         Group gr{};
-        for (; cur.valid(); cur.next()) {
-            cur.settle();
-            const int32_t pid = ring[0];
+        bool stop = false;
+        // the ring slot read in an iteration is refilled in the same iteration
+        // and read again PREFETCH iterations later (no move of a pending load)
+        while (cur.valid() && !stop) {
 #pragma unroll
-            for (int d = 0; d + 1 < PREFETCH; ++d) ring[d] = ring[d + 1];
-            ring[PREFETCH - 1] = page_id(ahead);
-            ahead.next();
-            if (cur.g != cur_g) {
-                cur_g = cur.g;
-                gr = p.groups[cur_g];
-                bool ok = true;
-                if (lane == 0) {
-                    ok = q_loads == 0 || mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
-                        tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
-                        tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
+            for (int u = 0; u < PREFETCH; ++u) {
+                if (!cur.valid()) break;
+                cur.settle();
+                const int32_t pid = ring[u];
+                ring[u] = page_id(ahead);
+                ahead.next();
+                if (cur.g != cur_g) {
+                    cur_g = cur.g;
+                    gr = p.groups[cur_g];
+                    bool ok = true;
+                    if (lane == 0) {
+                        ok = q_loads == 0 || mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+                            tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
+                            tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
+                        }
                     }
+                    if (__any_sync(0xffffffffu, !ok)) { stop = true; break; }
+                    ++q_loads;
                 }
-                if (__any_sync(0xffffffffu, !ok)) break;
-                ++q_loads;
-            }
-            if (__any_sync(0xffffffffu, !mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim))) break;
-            const int32_t pos0 = cur.tile() * TILE_M;
-            const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) / p.page_box;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
-            __syncwarp();
-            if (lane < nbox) {
-                const int32_t pos = pos0 + lane * p.page_box;
-                int32_t y;
-                if (pid >= 0 && pid < p.num_pages) {
-                    y = pid * p.page_pos + (pos % p.page_pos);
-                } else {
-                    record_error(p.status, ST_BAD_PAGE);
-                    y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+                if (__any_sync(0xffffffffu, !mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim))) {
+                    stop = true;
+                    break;
                 }
-                uint8_t *dst = k_s + stage * K_STAGE_BYTES + lane * p.page_box * 128;
-                tma_load_2d(dst, &tmap_k, &c.full[stage], 0, y);
-                tma_load_2d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, y);
+                const int32_t pos0 = cur.tile() * TILE_M;
+                const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) / p.page_box;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
+                __syncwarp();
+                if (lane < nbox) {
+                    const int32_t pos = pos0 + lane * p.page_box;
+                    int32_t y;
+                    if (pid >= 0 && pid < p.num_pages) {
+                        y = pid * p.page_pos + (pos % p.page_pos);
+                    } else {
+                        record_error(p.status, ST_BAD_PAGE);
+                        y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+                    }
+                    uint8_t *dst = k_s + stage * K_STAGE_BYTES + lane * p.page_box * 128;
+                    tma_load_2d(dst, &tmap_k, &c.full[stage], 0, y);
+                    tma_load_2d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, y);
+                }
+                if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
+                cur.next();
             }
-            if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
