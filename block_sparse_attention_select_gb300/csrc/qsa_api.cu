@@ -136,7 +136,7 @@ FilterShape filter_shape(int64_t max_len, int32_t k)
 {
     FilterShape f;
     f.stride = std::max(1, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
-    f.cap = 2 * k + 2048;
+    f.cap = std::max(2 * k + 256, k + 512);   // candidates the selector holds: ~1.5 k expected
     const int64_t tiles = (max_len + TILE_M - 1) / TILE_M;
     f.sample_ld = std::max<int64_t>(TILE_M, (tiles + f.stride - 1) / f.stride * TILE_M);
     return f;
@@ -170,7 +170,7 @@ Layout layout(int32_t R, int64_t ld, int32_t k)
     L.sample = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(f.sample_ld));
     L.tau = take(sizeof(float) * R);
     L.flag = take(sizeof(int32_t) * R);
-    const size_t tiles = static_cast<size_t>((ld + TILE_M - 1) / TILE_M);
+    const size_t tiles = static_cast<size_t>(((ld + TILE_M - 1) / TILE_M + 3) / 4 * 4);
     L.cand_cnt = take(static_cast<size_t>(R) * tiles * 4);
     L.cand = take(sizeof(uint2) * static_cast<size_t>(R) * tiles * 4 * CAND_SLOTS);
     L.total = o;
@@ -509,7 +509,8 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     float *tau = reinterpret_cast<float *>(at(s.L.tau));
     uint8_t *cand_cnt = reinterpret_cast<uint8_t *>(at(s.L.cand_cnt));
     uint2 *cand = reinterpret_cast<uint2 *>(at(s.L.cand));
-    const int32_t tiles_ld = static_cast<int32_t>((ld + TILE_M - 1) / TILE_M);
+    // multiple of 4 so that every row's count bytes start 16-byte aligned
+    const int32_t tiles_ld = static_cast<int32_t>(((ld + TILE_M - 1) / TILE_M + 3) / 4 * 4);
 
     // 1. scores of every stride-th key tile
     s.sp.mode = SCORE_SAMPLE;

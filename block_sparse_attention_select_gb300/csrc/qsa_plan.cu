@@ -95,18 +95,30 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     }
     const int32_t n_groups = carry_gid;
 
-    // Phase 2: rows and longest visible length of each group.
-    for (int32_t g = tid; g < n_groups; g += PLAN_THREADS) {
-        const int32_t r0 = groups[g].row0;
-        const int32_t r1 = g + 1 < n_groups ? groups[g + 1].row0 : R;
-        int32_t vmax = 0, vmin = INT32_MAX;
-        for (int32_t r = r0; r < r1; ++r) {
-            vmax = max(vmax, row_vis[r]);
-            vmin = min(vmin, row_vis[r]);
+    // Phase 2: rows and longest / shortest visible length of each group, one
+    // warp per group.
+    {
+        const int wid = tid >> 5, lane = tid & 31;
+        for (int32_t g = wid; g < n_groups; g += PLAN_THREADS / 32) {
+            const int32_t r0 = groups[g].row0;
+            const int32_t r1 = g + 1 < n_groups ? groups[g + 1].row0 : R;
+            int32_t vmax = 0, vmin = INT32_MAX;
+            for (int32_t r = r0 + lane; r < r1; r += 32) {
+                const int32_t v = row_vis[r];
+                vmax = max(vmax, v);
+                vmin = min(vmin, v);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+                vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+            }
+            if (lane == 0) {
+                groups[g].nrows = r1 - r0;
+                groups[g].vmax = vmax;
+                groups[g].vmin = vmin;
+            }
         }
-        groups[g].nrows = r1 - r0;
-        groups[g].vmax = vmax;
-        groups[g].vmin = vmin;
     }
     __syncthreads();
 

@@ -18,9 +18,12 @@
 namespace qsa {
 namespace {
 
-constexpr int NT = 512;               // threads per row
+constexpr int NT = 256;               // threads per row
 constexpr int NBINS = 2048;           // 11-bit digits
+constexpr int BPT = NBINS / NT;       // bins per thread in scans
 constexpr int SMALL_BUCKET = 16;      // buckets up to this size: one thread sorts them
+constexpr int SLACK = 512;            // room past k for the bucket holding the k-th element
+constexpr uint32_t RANK_MAX = 32;     // buckets up to this size are ordered by rank counting
 
 struct SelShared {
     uint32_t hist[NBINS];
@@ -28,7 +31,7 @@ struct SelShared {
     uint32_t wtot[32];
     uint32_t red_min[32], red_max[32];
     uint32_t cut_digit, cut_above, count, total, taken, nbig, flag, pad_;
-    uint32_t big[NBINS / 4];          // buckets needing a warp sort (at most k / 17 <= 482)
+    uint32_t big[512];                // buckets needing a warp sort
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -45,17 +48,17 @@ __device__ __forceinline__ void clear_hist(SelShared &sh)
 __device__ __forceinline__ void find_cut(SelShared &sh, uint32_t k_rem)
 {
     const int t = threadIdx.x;
-    uint32_t c[4], sum = 0;
+    uint32_t c[BPT], sum = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        c[i] = sh.hist[NBINS - 1 - (4 * t + i)];
+    for (int i = 0; i < BPT; ++i) {
+        c[i] = sh.hist[NBINS - 1 - (BPT * t + i)];
         sum += c[i];
     }
     uint32_t before = block_excl_scan<NT>(sum, sh.wtot, nullptr);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < BPT; ++i) {
         if (before < k_rem && k_rem <= before + c[i]) {
-            sh.cut_digit = static_cast<uint32_t>(NBINS - 1 - (4 * t + i));
+            sh.cut_digit = static_cast<uint32_t>(NBINS - 1 - (BPT * t + i));
             sh.cut_above = before;
         }
         before += c[i];
@@ -161,6 +164,170 @@ __device__ void warp_sort_desc(uint64_t *a, int32_t m)
     }
 }
 
+// bstart[b] = elements in buckets before b (bucket 0 holds the largest keys);
+// hist[] becomes the scatter cursors.
+__device__ __forceinline__ void bucket_starts(SelShared &sh)
+{
+    const int t = threadIdx.x;
+    uint32_t c[BPT], sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) { c[i] = sh.hist[BPT * t + i]; sum += c[i]; }
+    uint32_t before = block_excl_scan<NT>(sum, sh.wtot, nullptr);
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) { sh.bstart[BPT * t + i] = before; before += c[i]; }
+    if (t == 0) sh.nbig = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) sh.hist[BPT * t + i] = sh.bstart[BPT * t + i];   // cursors
+    __syncthreads();
+}
+
+// Descending sort of a[0, m), m <= 32, by one warp in registers.
+__device__ __forceinline__ void warp_sort32_desc(uint64_t *a, int32_t m)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t x = lane < m ? a[lane] : 0ull;          // 0 sorts last (real keys are > 0)
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, x, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0 || size == 32);
+            x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
+    }
+    if (lane < m) a[lane] = x;
+}
+
+// Descending sort of N 64-bit keys held in registers (bitonic network,
+// fully unrolled: no memory traffic, no divergence inside the network).
+template <int N>
+__device__ __forceinline__ void reg_sort_desc(uint64_t (&x)[N])
+{
+#pragma unroll
+    for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const uint64_t a = x[i], b = x[j];
+                    const bool swap = desc ? a < b : a > b;
+                    x[i] = swap ? b : a;
+                    x[j] = swap ? a : b;
+                }
+            }
+        }
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void small_sort(uint64_t *a, uint32_t m)
+{
+    uint64_t x[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = static_cast<uint32_t>(i) < m ? a[i] : 0ull;   // 0 sorts last
+    reg_sort_desc<N>(x);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (static_cast<uint32_t>(i) < m) a[i] = x[i];
+}
+
+// Orders every bucket b < nb in place (buckets were filled by scatter;
+// hist[b] is its end): buckets of up to 16 by one thread with a register
+// sorting network, larger ones by a warp.
+__device__ void sort_buckets(SelShared &sh, uint64_t *out64, int nb)
+{
+    for (int b = threadIdx.x; b < nb; b += NT) {
+        const uint32_t s0 = sh.bstart[b], m = sh.hist[b] - s0;
+        if (m <= 1) continue;
+        if (m > SMALL_BUCKET) {
+            sh.big[atomicAdd(&sh.nbig, 1u)] = b;
+            continue;
+        }
+        if (m <= 4) small_sort<4>(out64 + s0, m);
+        else if (m <= 8) small_sort<8>(out64 + s0, m);
+        else small_sort<16>(out64 + s0, m);
+    }
+    __syncthreads();
+    for (uint32_t q = threadIdx.x >> 5; q < sh.nbig; q += NT / 32) {
+        const uint32_t b = sh.big[q];
+        const int32_t m = static_cast<int32_t>(sh.hist[b] - sh.bstart[b]);
+        if (m <= 32) warp_sort32_desc(out64 + sh.bstart[b], m);
+        else warp_sort_desc(out64 + sh.bstart[b], m);
+    }
+    __syncthreads();
+}
+
+// Top kk of the n elements in one counting-sort pass: buckets are the top 11
+// bits of (key32 - min key); only the buckets down to the one holding the
+// kk-th element are written to out64 (capacity out_cap) and ordered.
+// Returns false, touching nothing, when those buckets would not fit.
+__device__ bool bucket_topk(SelShared &sh, const uint32_t *keys, const uint32_t *inv, int32_t n,
+                            int32_t kk, uint64_t *out64, int32_t out_cap, uint64_t *ranked)
+{
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (int32_t i = threadIdx.x; i < n; i += NT) {
+        kmin = min(kmin, keys[i]);
+        kmax = max(kmax, keys[i]);
+    }
+    block_minmax(sh, kmin, kmax, kmin, kmax);
+    const int shift = span_shift(kmax - kmin);
+    clear_hist(sh);
+    for (int32_t i = threadIdx.x; i < n; i += NT)
+        atomicAdd(&sh.hist[NBINS - 1 - ((keys[i] - kmin) >> shift)], 1u);
+    __syncthreads();
+    bucket_starts(sh);
+    // boundary bucket: the one whose range [bstart, end) contains position kk - 1
+    if (threadIdx.x == 0) sh.cut_digit = NBINS;
+    __syncthreads();
+    for (int b = threadIdx.x; b < NBINS; b += NT) {
+        const uint32_t s0 = sh.bstart[b];
+        const uint32_t e = (b + 1 < NBINS) ? sh.bstart[b + 1] : static_cast<uint32_t>(n);
+        if (s0 < static_cast<uint32_t>(kk) && static_cast<uint32_t>(kk) <= e) sh.cut_digit = b;
+    }
+    __syncthreads();
+    const int bb = static_cast<int>(sh.cut_digit);
+    const uint32_t need = (bb + 1 < NBINS) ? sh.bstart[bb + 1] : static_cast<uint32_t>(n);
+    if (bb >= NBINS || need > static_cast<uint32_t>(out_cap)) return false;   // uniform
+    for (int32_t i = threadIdx.x; i < n; i += NT) {
+        const uint32_t b = NBINS - 1 - ((keys[i] - kmin) >> shift);
+        if (b > static_cast<uint32_t>(bb)) continue;
+        const uint32_t pos = atomicAdd(&sh.hist[b], 1u);
+        out64[pos] = (static_cast<uint64_t>(keys[i]) << 32) | inv[i];
+    }
+    if (threadIdx.x == 0) sh.nbig = 0;
+    __syncthreads();
+    // Order inside buckets by rank counting: the thread of position p counts
+    // the larger keys of its bucket.  Positions are handed out in bucket
+    // order, so neighbouring threads scan the same bucket (no divergence);
+    // buckets above RANK_MAX go to a warp sort instead.  keys/inv are dead
+    // now, and `ranked` reuses their space.
+    for (uint32_t pos = threadIdx.x; pos < need; pos += NT) {
+        const uint64_t x = out64[pos];
+        const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - kmin) >> shift);
+        const uint32_t s0 = sh.bstart[b], e = sh.hist[b];
+        if (e - s0 > RANK_MAX) {
+            if (pos == s0) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
+            continue;
+        }
+        uint32_t rk = 0;
+        for (uint32_t q = s0; q < e; ++q) rk += out64[q] > x;
+        ranked[s0 + rk] = x;
+    }
+    __syncthreads();
+    for (uint32_t q = threadIdx.x >> 5; q < sh.nbig; q += NT / 32) {
+        const uint32_t b = sh.big[q];
+        const uint32_t s0 = sh.bstart[b], m = sh.hist[b] - s0;
+        warp_sort_desc(out64 + s0, static_cast<int32_t>(m));
+        for (uint32_t t = threadIdx.x & 31; t < m; t += 32) ranked[s0 + t] = out64[s0 + t];
+    }
+    __syncthreads();
+    return true;
+}
+
 // Selects the top kk of the n elements (keys, inv) in shared memory and
 // writes them, ordered, into out64 (as (key32 << 32) | inv).
 __device__ void select_and_sort(SelShared &sh, const uint32_t *keys, const uint32_t *inv, int32_t n,
@@ -198,20 +365,7 @@ __device__ void select_and_sort(SelShared &sh, const uint32_t *keys, const uint3
     for (int32_t i = threadIdx.x; i < n; i += NT)
         if (selected(i)) atomicAdd(&sh.hist[NBINS - 1 - ((keys[i] - T) >> shift)], 1u);
     __syncthreads();
-    {   // bstart[b] = elements in buckets before b (bucket 0 = largest keys)
-        const int t = threadIdx.x;
-        uint32_t c[4], sum = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { c[i] = sh.hist[4 * t + i]; sum += c[i]; }
-        uint32_t before = block_excl_scan<NT>(sum, sh.wtot, nullptr);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { sh.bstart[4 * t + i] = before; before += c[i]; }
-        if (t == 0) sh.nbig = 0;
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) sh.hist[4 * t + i] = sh.bstart[4 * t + i];   // cursors
-        __syncthreads();
-    }
+    bucket_starts(sh);
     for (int32_t i = threadIdx.x; i < n; i += NT) {
         if (!selected(i)) continue;
         const uint32_t b = NBINS - 1 - ((keys[i] - T) >> shift);
@@ -219,28 +373,7 @@ __device__ void select_and_sort(SelShared &sh, const uint32_t *keys, const uint3
         out64[pos] = (static_cast<uint64_t>(keys[i]) << 32) | inv[i];
     }
     __syncthreads();
-    // in-bucket order: small buckets by one thread each, larger ones by a warp
-    for (int b = threadIdx.x; b < NBINS; b += NT) {
-        const uint32_t s0 = sh.bstart[b], m = sh.hist[b] - s0;
-        if (m <= 1) continue;
-        if (m > SMALL_BUCKET) {
-            sh.big[atomicAdd(&sh.nbig, 1u)] = b;
-            continue;
-        }
-        uint64_t *a = out64 + s0;
-        for (uint32_t x = 1; x < m; ++x) {
-            const uint64_t v = a[x];
-            uint32_t y = x;
-            while (y > 0 && a[y - 1] < v) { a[y] = a[y - 1]; --y; }
-            a[y] = v;
-        }
-    }
-    __syncthreads();
-    for (uint32_t q = threadIdx.x >> 5; q < sh.nbig; q += NT / 32) {
-        const uint32_t b = sh.big[q];
-        warp_sort_desc(out64 + sh.bstart[b], static_cast<int32_t>(sh.hist[b] - sh.bstart[b]));
-    }
-    __syncthreads();
+    sort_buckets(sh, out64, NBINS);
 }
 
 __device__ void write_row(const SelectParams &p, int32_t r, const uint64_t *buf, int32_t kk)
@@ -384,13 +517,27 @@ __device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, floa
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(NT, 2)
+// Entries of the ordered-output buffer: k plus room for the bucket holding
+// the k-th element; in candidate mode also big enough to stage the row's
+// count bytes (16-byte padded).
+__host__ __device__ __forceinline__ int32_t out_capacity(const SelectParams &p)
+{
+    if (p.mode == SEL_THRESH) return 0;
+    int32_t cap = p.k + SLACK;
+    if (p.mode == SEL_CAND) {
+        const int32_t stage = (p.tiles_ld * 4 + 15) / 16 * 2;   // 16-byte vectors, 8 bytes per entry
+        cap = cap > stage ? cap : stage;
+    }
+    return cap;
+}
+
+__global__ void __launch_bounds__(NT, 4)
 select_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     SelShared &sh = *reinterpret_cast<SelShared *>(smem_raw);
     uint64_t *out64 = reinterpret_cast<uint64_t *>(smem_raw + sizeof(SelShared));
-    uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + (p.mode == SEL_THRESH ? 0 : p.k));
+    uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + out_capacity(p));
     uint32_t *inv = keys + p.smem_cap;
 
     const int32_t r = blockIdx.x;
@@ -417,17 +564,36 @@ select_kernel(const SelectParams p)
             const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
             uint32_t T;
             if (n_s <= p.smem_cap) {
+                // one histogram level suffices: tau only has to keep about m
+                // sampled scores; the candidate count is verified afterwards
                 uint32_t lo = 0xffffffffu, hi = 0u;
                 for (int32_t i = threadIdx.x; i < n_s; i += NT) {
-                    const uint32_t kv = score_key(__ldcg(row + i));
+                    const uint32_t kv = score_key(__ldg(row + i));
                     keys[i] = kv;
                     lo = min(lo, kv);
                     hi = max(hi, kv);
                 }
                 block_minmax(sh, lo, hi, lo, hi);
-                uint32_t k2, eq2;
-                T = kth_largest(sh, n_s, static_cast<uint32_t>(m), lo, hi, static_cast<uint32_t>(n_s),
-                                [&](int32_t i) { return keys[i]; }, [&](int32_t) { return true; }, k2, eq2);
+                // two range-adaptive levels: the sample's range includes the
+                // spike of zero scores, so one level is too coarse near tau
+                uint32_t k_left = static_cast<uint32_t>(m);
+                for (int lv = 0; lv < 2 && lo != hi; ++lv) {
+                    const int shift = span_shift(hi - lo);
+                    clear_hist(sh);
+                    for (int32_t i = threadIdx.x; i < n_s; i += NT) {
+                        const uint32_t kv = keys[i];
+                        if (kv >= lo && kv <= hi) atomicAdd(&sh.hist[(kv - lo) >> shift], 1u);
+                    }
+                    __syncthreads();
+                    find_cut(sh, k_left);
+                    k_left -= sh.cut_above;
+                    const uint32_t nlo = lo + (sh.cut_digit << shift);
+                    const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
+                    hi = static_cast<uint32_t>(min(static_cast<uint64_t>(hi), nhi));
+                    lo = nlo;
+                    __syncthreads();
+                }
+                T = lo;
             } else {
                 uint32_t k2;
                 stream_narrow(sh, row, n_s, static_cast<uint32_t>(m), 0, nullptr, nullptr, T, k2, false);
@@ -442,20 +608,26 @@ select_kernel(const SelectParams p)
     const int32_t kk_target = min(p.k, V);
     const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
     if (p.mode == SEL_CAND) {
-        // gather the candidate slots of the row's key tiles, in position order
+        // the candidate slots of the row's key tiles: one (tile, 32-position
+        // part) list per entry, its length in cnt[]
         const int32_t ne = ((V + TILE_M - 1) / TILE_M) * 4;
         const uint8_t *cnt = p.cand_cnt + static_cast<int64_t>(r) * p.tiles_ld * 4;
         const uint2 *slots = p.cand + static_cast<int64_t>(r) * p.tiles_ld * 4 * CAND_SLOTS;
-        const int32_t per = (ne + NT - 1) / NT;
-        const int32_t e0 = min(ne, static_cast<int32_t>(threadIdx.x) * per), e1 = min(ne, e0 + per);
+        // stage the count bytes in shared memory (out64 is free until the
+        // selection) with 16-byte loads: one round trip for the whole row
+        uint8_t *cnt_s = reinterpret_cast<uint8_t *>(out64);
+        const int32_t nvec = (ne + 15) / 16;
+        for (int32_t v16 = threadIdx.x; v16 < nvec; v16 += NT)
+            reinterpret_cast<uint4 *>(cnt_s)[v16] = __ldcg(reinterpret_cast<const uint4 *>(cnt) + v16);
+        __syncthreads();
         uint32_t sum = 0;
         bool over = false;
-        for (int32_t e = e0; e < e1; ++e) {
-            const uint32_t c = cnt[e];
+        for (int32_t e = threadIdx.x; e < ne; e += NT) {
+            const uint32_t c = cnt_s[e];
             over |= c > CAND_SLOTS;
-            sum += min(c, static_cast<uint32_t>(CAND_SLOTS));
+            sum += c;
         }
-        uint32_t base = block_excl_scan<NT>(sum, sh.wtot, &sh.total);
+        block_excl_scan<NT>(sum, sh.wtot, &sh.total);
         const bool any_over = __syncthreads_or(over) != 0;
         const uint32_t total = sh.total;
         if (any_over || total < static_cast<uint32_t>(kk_target) || total > static_cast<uint32_t>(p.smem_cap)) {
@@ -469,16 +641,41 @@ select_kernel(const SelectParams p)
             row = fb;
         } else {
             if (threadIdx.x == 0) p.row_flag[r] = 0;
-            for (int32_t e = e0; e < e1; ++e) {
-                const uint32_t c = cnt[e];
-                for (uint32_t s = 0; s < c; ++s) {
-                    const uint2 v = slots[static_cast<int64_t>(e) * CAND_SLOTS + s];
-                    keys[base] = score_key(__uint_as_float(v.x));
-                    inv[base] = ~v.y;
-                    ++base;
+            uint32_t done = 0;
+            for (int32_t e0 = 0; e0 < ne; e0 += NBINS) {
+                const int32_t chunk = min(NBINS, ne - e0);
+                for (int32_t i = threadIdx.x; i < NBINS; i += NT) sh.hist[i] = i < chunk ? cnt_s[e0 + i] : 0u;
+                __syncthreads();
+                bucket_starts(sh);                        // bstart = offsets within the chunk
+                // owner map: candidate slot id of every output position
+                for (int32_t i = threadIdx.x; i < chunk; i += NT) {
+                    const uint32_t c = cnt_s[e0 + i];
+                    for (uint32_t q = 0; q < c; ++q)
+                        inv[done + sh.bstart[i] + q] = static_cast<uint32_t>(e0 + i) * CAND_SLOTS + q;
+                    if (i == chunk - 1) sh.taken = sh.bstart[i] + c;   // chunk total
                 }
+                __syncthreads();
+                const uint32_t ctot = sh.taken;
+                // every thread fetches its candidates, eight loads in flight
+                for (uint32_t t0 = threadIdx.x; t0 < ctot; t0 += 8 * NT) {
+                    uint2 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t t = t0 + u * NT;
+                        if (t < ctot) v[u] = slots[inv[done + t]];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t t = t0 + u * NT;
+                        if (t < ctot) {
+                            keys[done + t] = score_key(__uint_as_float(v[u].x));
+                            inv[done + t] = ~v[u].y;
+                        }
+                    }
+                }
+                __syncthreads();
+                done += ctot;
             }
-            __syncthreads();
             n = static_cast<int32_t>(total);
         }
     }
@@ -498,8 +695,15 @@ select_kernel(const SelectParams p)
         }
     }
     const int32_t kk = min(p.k, n);
-    select_and_sort(sh, keys, inv, n, kk, out64);
-    write_row(p, r, out64, kk);
+    const uint64_t *result = out64;
+    if (kk > 0) {
+        uint64_t *ranked = reinterpret_cast<uint64_t *>(keys);   // keys + inv: smem_cap 8-byte slots
+        if (bucket_topk(sh, keys, inv, n, kk, out64, min(out_capacity(p), p.smem_cap), ranked))
+            result = ranked;
+        else
+            select_and_sort(sh, keys, inv, n, kk, out64);
+    }
+    write_row(p, r, result, kk);
 }
 
 }  // namespace
@@ -511,8 +715,8 @@ size_t select_smem_bytes(int32_t smem_cap)
 
 int launch_select(const SelectParams &p, void *stream)
 {
-    const size_t smem = sizeof(SelShared) + static_cast<size_t>(p.mode == SEL_THRESH ? 0 : p.k) * 8 +
-                        static_cast<size_t>(p.smem_cap) * 8;
+    const size_t smem = sizeof(SelShared) + static_cast<size_t>(out_capacity(p)) * 8 +
+                        static_cast<size_t>(p.smem_cap) * (p.mode == SEL_THRESH ? 4 : 8);
     static size_t attr_bytes[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
