@@ -379,7 +379,7 @@ def measure_e2e(args, wl, qsa, keys_dev, stream, dev):
 
     for _ in range(3):
         one()
-    n = max(5, args.steps)
+    n = max(5, min(args.steps, 500))
     t0 = time.perf_counter()
     for _ in range(n):
         one()
@@ -391,8 +391,8 @@ def measure_e2e(args, wl, qsa, keys_dev, stream, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(W.CONFIGS), default="bench")
     ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
