@@ -325,6 +325,7 @@ const char *qsa_status_string(qsa_status s)
     case QSA_ERR_TIMEOUT: return "a device pipeline wait timed out";
     case QSA_ERR_CUDA: return "CUDA runtime error";
     case QSA_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case QSA_ERR_STATIC_LIMIT: return "call needs more scratch than the library's static buffer (QSA_STATIC_SCRATCH_BYTES)";
     }
     return "unknown status";
 }
@@ -558,3 +559,55 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the workspace is a buffer inside the library.
+
+namespace {
+
+static __device__ __align__(256) uint8_t g_static_scratch[QSA_STATIC_SCRATCH_BYTES];
+
+struct StaticScratch {
+    bool ready = false;
+    void *ptr = nullptr;
+};
+StaticScratch g_static[MAX_DEVICES];
+
+}  // namespace
+
+extern "C" qsa_status qsa_select_paged_tokens_noalloc(const void *q, const float *w, int32_t rows,
+                                                      int32_t H, const qsa_paged_keys *keys,
+                                                      const int32_t *row_req,
+                                                      const int32_t *row_visible, int32_t k,
+                                                      int32_t *out_idx, float *out_val, void *stream)
+{
+    g_launches = 0;
+    if (!keys || keys->max_pages_per_req < 1 || keys->page_positions < 1 || rows < 0 || k < 0)
+        return QSA_ERR_INVALID_ARG;
+    const int64_t ld = static_cast<int64_t>(keys->max_pages_per_req) * keys->page_positions;
+    if (ld > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    const size_t need = qsa_workspace_bytes(rows, static_cast<int32_t>(ld), k, 0);
+    if (need > QSA_STATIC_SCRATCH_BYTES) return QSA_ERR_STATIC_LIMIT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return QSA_ERR_NO_DEVICE;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        StaticScratch &st = g_static[dev];
+        if (!st.ready) {
+            // In host code g_static_scratch names a host-side stand-in; the
+            // kernels need this device's address of the buffer.
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+                cudaGetLastError();
+                return QSA_ERR_CUDA;
+            }
+            st.ptr = ptr;
+            st.ready = true;
+        }
+    }
+    return qsa_select_paged_tokens(q, w, rows, H, keys, row_req, row_visible, k, out_idx, out_val,
+                                   g_static[dev].ptr, QSA_STATIC_SCRATCH_BYTES, stream);
+}

@@ -29,6 +29,7 @@ QSA_ERR_BAD_PAGE = 5
 QSA_ERR_TIMEOUT = 6
 QSA_ERR_CUDA = 7
 QSA_ERR_NO_DEVICE = 8
+QSA_ERR_STATIC_LIMIT = 9
 
 QSA_CFG_PATH = 1
 QSA_CFG_WAIT_LIMIT_NS = 2
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH):
     lib.qsa_set_config.argtypes = [i32, i64]
     lib.qsa_last_launch_count.restype = i32
     lib.qsa_last_launch_count.argtypes = []
+    lib.qsa_select_paged_tokens_noalloc.restype = ctypes.c_int
+    lib.qsa_select_paged_tokens_noalloc.argtypes = [vp, vp, i32, i32, kp, vp, vp, i32, vp, vp, vp]
     lib.qsa_kernel_times.restype = ctypes.c_int
     lib.qsa_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), i32]
     _lib = lib
@@ -197,6 +200,22 @@ def select_paged_tokens(q, w, keys: PagedKeys, row_req, row_visible, k: int, out
                                         _ptr(row_req), _ptr(row_visible), int(k), _ptr(out_idx),
                                         _ptr(out_val), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "qsa_select_paged_tokens")
+    return out_idx, out_val
+
+
+def select_paged_tokens_noalloc(q, w, keys: PagedKeys, row_req, row_visible, k: int, out_idx,
+                                out_val=None, stream=None):
+    """select_paged_tokens without a workspace: the library's own static scratch
+    buffer is used (for callers that cannot allocate device memory).  Outputs
+    must be passed in; calls on one device must not overlap."""
+    _need(q, torch.float16, "q"), _need(w, torch.float32, "w")
+    _need(row_req, torch.int32, "row_req"), _need(row_visible, torch.int32, "row_visible")
+    _need(out_idx, torch.int32, "out_idx")
+    R, H = int(q.shape[0]), int(q.shape[1])
+    st = load().qsa_select_paged_tokens_noalloc(_ptr(q), _ptr(w), R, H, ctypes.byref(keys.c),
+                                                _ptr(row_req), _ptr(row_visible), int(k),
+                                                _ptr(out_idx), _ptr(out_val), _stream(stream))
+    _check(st, "qsa_select_paged_tokens_noalloc")
     return out_idx, out_val
 
 

@@ -56,7 +56,8 @@ typedef enum {
     QSA_ERR_BAD_PAGE = 5,      /* (device) a block-table entry outside [0, num_pages) */
     QSA_ERR_TIMEOUT = 6,       /* (device) a pipeline wait ran past its time limit */
     QSA_ERR_CUDA = 7,          /* another CUDA runtime error */
-    QSA_ERR_NO_DEVICE = 8      /* no usable sm_100-family device */
+    QSA_ERR_NO_DEVICE = 8,     /* no usable sm_100-family device */
+    QSA_ERR_STATIC_LIMIT = 9   /* the call needs more scratch than QSA_STATIC_SCRATCH_BYTES */
 } qsa_status;
 
 /* Paged index-key side cache: one FP16 key of head_dim values per compressed
@@ -133,6 +134,31 @@ qsa_status qsa_kernel_times(double *ms, int32_t *launches, int32_t n);
 /* Launches made by the most recent qsa_* call on this host thread (kernels of
  * this library only). */
 int32_t qsa_last_launch_count(void);
+
+/* qsa_select_paged_tokens for callers that cannot allocate device memory.
+ * (This entry point has no counterpart in the pages; it is a convenience of
+ * this library.)  Some callers have no device allocator on their hot path:
+ * runtimes whose whole device memory is planned once at start-up (a fixed
+ * arena, an embedded or safety-certified deployment) must not call
+ * cudaMalloc, and may have nowhere to keep a caller-owned workspace either.
+ * This variant takes the same arguments minus the workspace and uses a
+ * scratch buffer of QSA_STATIC_SCRATCH_BYTES that lives in the library itself
+ * (a file-scope __device__ array, present on every GPU that loads the library
+ * until the process exits).  It calls no allocating routine.
+ *  - The first call on a device looks up that buffer's device address for the
+ *    current device; make that first call before any stream capture.
+ *  - Calls whose workspace (qsa_workspace_bytes for the same rows, k and
+ *    max_pages_per_req * page_positions) exceeds QSA_STATIC_SCRATCH_BYTES
+ *    return QSA_ERR_STATIC_LIMIT and launch nothing.
+ *  - Every call on a device shares the one buffer and it keeps the previous
+ *    call's contents; nothing in it needs to start at zero (each call writes
+ *    every region before reading it).  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on the buffer: serialise them. */
+#define QSA_STATIC_SCRATCH_BYTES (64u << 20)
+qsa_status qsa_select_paged_tokens_noalloc(const void *q, const float *w, int32_t rows, int32_t H,
+                                           const qsa_paged_keys *keys, const int32_t *row_req,
+                                           const int32_t *row_visible, int32_t k, int32_t *out_idx,
+                                           float *out_val, void *stream);
 
 #ifdef __cplusplus
 }
