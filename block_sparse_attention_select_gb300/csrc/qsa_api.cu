@@ -216,7 +216,7 @@ qsa_status check_keys(const qsa_paged_keys *keys)
 struct ScoreSetup {
     Layout L;
     uint8_t *ws;
-    CUtensorMap tq, tk;
+    CUtensorMap tq, tk, tk128;   // queries, key boxes of one page, key boxes of one tile
     ScoreParams sp;
     bool rows_kernel;   // query rows on TMEM lanes (prefill-sized groups)
     const void *q;
@@ -237,7 +237,7 @@ bool want_rows_kernel(int32_t rows, int32_t H, int32_t num_reqs)
 int launch_scorer(const ScoreSetup &s, int grid, void *stream)
 {
     return s.rows_kernel ? launch_score_rows(s.sp, &s.tk, s.q, grid, stream)
-                         : launch_score(s.sp, &s.tq, &s.tk, grid, stream);
+                         : launch_score(s.sp, &s.tq, &s.tk, &s.tk128, grid, stream);
 }
 
 qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
@@ -254,6 +254,12 @@ qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t row
     st = make_tmap(&s.tk, keys->k_cache,
                    static_cast<uint64_t>(keys->num_pages) * keys->page_positions,
                    static_cast<uint32_t>(std::min(keys->page_positions, TILE_M)));
+    if (st != QSA_OK) return st;
+    // (with fewer than 128 cache rows no run of a whole tile exists; the map
+    // is then never used and only has to be valid)
+    const uint64_t cache_rows = static_cast<uint64_t>(keys->num_pages) * keys->page_positions;
+    st = make_tmap(&s.tk128, keys->k_cache, cache_rows,
+                   cache_rows >= TILE_M ? TILE_M : static_cast<uint32_t>(std::min(keys->page_positions, TILE_M)));
     if (st != QSA_OK) return st;
     auto at = [&](size_t off) { return s.ws + off; };
     s.rows_kernel = want_rows_kernel(rows, H, keys->num_reqs);

@@ -116,8 +116,8 @@ int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, i
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
                 uint32_t *status, void *stream);
-int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid,
-                 void *stream);
+int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
+                 int grid, void *stream);
 int launch_score_rows(const ScoreParams &p, const void *tmap_k, const void *q, int grid, void *stream);
 int launch_select(const SelectParams &p, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);

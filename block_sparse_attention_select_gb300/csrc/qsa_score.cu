@@ -129,7 +129,7 @@ __device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
 // Drains this warp's 64 accumulator columns (64 / H query rows) of one tile.
 // Lane i holds key position tile * 128 + quarter * 32 + i.  FULL: every row
 // of the group sees the whole tile, so no per-element visibility test.
-template <int H, int MODE, bool FULL>
+template <int H, int MODE, bool FULL, bool ALLROWS>
 __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRows &e, const Group &gr,
                                               int32_t tile, uint32_t taddr, int cq, int quarter,
                                               int lane, uint32_t lt_mask, int32_t nmine)
@@ -140,23 +140,32 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
     const int32_t p_in_tile = quarter * 32 + lane;
     const int32_t j = tile * TILE_M + p_in_tile;
     const int64_t r0 = static_cast<int64_t>(gr.row0) + cq * RPW;     // first row of this warp
-    const int64_t slot0 = (r0 * p.tiles_ld + tile) * 4 + quarter;   // FILTER
+    // FILTER: candidate slots and count bytes of (row r0, tile, quarter); a row
+    // further is slot_stride entries further
+    const int64_t slot0 = (r0 * p.tiles_ld + tile) * 4 + quarter;
     const int64_t slot_stride = static_cast<int64_t>(p.tiles_ld) * 4;
+    uint2 *cand0 = nullptr;
+    uint8_t *cnt0 = nullptr;
     float *out0 = nullptr;
-    if constexpr (MODE == SCORE_SAMPLE)
+    if constexpr (MODE == SCORE_FILTER) {
+        cand0 = p.cand + slot0 * CAND_SLOTS + __popc(lt_mask);   // this lane's slot if all lanes took
+        cnt0 = p.cand_cnt + slot0;
+    } else if constexpr (MODE == SCORE_SAMPLE) {
         out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
-    else if constexpr (MODE != SCORE_FILTER)
+    } else {
         out0 = p.out + r0 * p.ld + j;
+    }
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int32_t c0 = ch * RPC;
-        if (c0 >= nmine) break;                              // warp-uniform
+        if (!ALLROWS && c0 >= nmine) break;                  // warp-uniform
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + ch * 32), v);
         tmem_ld_wait();
+        uint32_t my_count = 0;                                 // FILTER: count of row (c0 + lane)
 #pragma unroll
         for (int b0 = 0; b0 < RPC; b0 += B) {
-            if (c0 + b0 >= nmine) break;                     // warp-uniform
+            if (!ALLROWS && c0 + b0 >= nmine) break;         // warp-uniform
             float s[B];
 #pragma unroll
             for (int i = 0; i < B; ++i) {
@@ -167,16 +176,15 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
 #pragma unroll
             for (int i = 0; i < B; ++i) {
                 const int32_t el = c0 + b0 + i;
-                const bool live = el < nmine;                 // warp-uniform
+                const bool live = ALLROWS || el < nmine;      // warp-uniform
                 const bool ok = live && (FULL || j < e.vis[el]);
                 if constexpr (MODE == SCORE_FILTER) {
                     const bool take = ok && s[i] >= e.tau[el];
                     const uint32_t m = __ballot_sync(0xffffffffu, take);
-                    const int64_t q_slot = slot0 + el * slot_stride;
-                    if (live && lane == 0) p.cand_cnt[q_slot] = static_cast<uint8_t>(__popc(m));
+                    if (lane == b0 + i) my_count = __popc(m);
                     static_assert(CAND_SLOTS >= 32, "one slot per lane");
                     if (take)
-                        p.cand[q_slot * CAND_SLOTS + __popc(m & lt_mask)] =
+                        cand0[el * slot_stride * CAND_SLOTS + __popc(m & lt_mask) - __popc(lt_mask)] =
                             make_uint2(__float_as_uint(s[i]), static_cast<uint32_t>(j));
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
@@ -186,6 +194,10 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                     else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
                 }
             }
+        }
+        if constexpr (MODE == SCORE_FILTER) {
+            // one store for the chunk: lane i writes the count of row c0 + i
+            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) cnt0[(c0 + lane) * slot_stride] = static_cast<uint8_t>(my_count);
         }
     }
 }
@@ -198,16 +210,20 @@ __device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRow
     constexpr int RPW = 64 / H;
     const int32_t nmine = min(RPW, gr.nrows - cq * RPW);
     if (nmine <= 0) return;
-    if ((tile + 1) * TILE_M <= gr.vmin)
-        epilogue_rows<H, MODE, true>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
-    else
-        epilogue_rows<H, MODE, false>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+    const bool full = (tile + 1) * TILE_M <= gr.vmin;
+    if (nmine == RPW) {
+        if (full) epilogue_rows<H, MODE, true, true>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+        else epilogue_rows<H, MODE, false, true>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+    } else {
+        if (full) epilogue_rows<H, MODE, true, false>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+        else epilogue_rows<H, MODE, false, false>(p, e, gr, tile, taddr, cq, quarter, lane, lt_mask, nmine);
+    }
 }
 
 template <int H>
 __global__ void __launch_bounds__(SCORE_THREADS, 1)
 score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-             const ScoreParams p)
+             const __grid_constant__ CUtensorMap tmap_k128, const ScoreParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -252,6 +268,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmap_q);
         tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_k128);
     }
     tc_fence_before();
     __syncthreads();
@@ -323,15 +340,22 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 if (lane == 0)
                     mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
                 __syncwarp();
-                if (lane < nbox) {
-                    const int32_t pos = pos0 + lane * p.page_box;
-                    int32_t y;
-                    if (pid >= 0 && pid < p.num_pages) {
-                        y = pid * p.page_pos + (pos % p.page_pos);
-                    } else {
-                        record_error(p.status, ST_BAD_PAGE);
-                        y = p.num_pages * p.page_pos;      // past the end: TMA fills zeros
+                const int32_t pos = pos0 + lane * p.page_box;
+                const bool good = pid >= 0 && pid < p.num_pages;
+                int32_t y = good ? pid * p.page_pos + (pos % p.page_pos)
+                                 : p.num_pages * p.page_pos;   // past the end: TMA fills zeros
+                if (lane < nbox && !good) record_error(p.status, ST_BAD_PAGE);
+                // a full tile whose pages are physically consecutive is one box per K half
+                const int32_t y0 = __shfl_sync(0xffffffffu, y, 0);
+                const bool run = nbox * p.page_box == TILE_M &&
+                                 __all_sync(0xffffffffu, lane >= nbox || (good && y == y0 + lane * p.page_box));
+                if (run) {
+                    if (lane == 0) {
+                        uint8_t *dst = k_s + stage * K_STAGE_BYTES;
+                        tma_load_2d(dst, &tmap_k128, &c.full[stage], 0, y0);
+                        tma_load_2d(dst + K_HALF_BYTES, &tmap_k128, &c.full[stage], 64, y0);
                     }
+                } else if (lane < nbox) {
                     uint8_t *dst = k_s + stage * K_STAGE_BYTES + lane * p.page_box * 128;
                     tma_load_2d(dst, &tmap_k, &c.full[stage], 0, y);
                     tma_load_2d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, y);
@@ -439,7 +463,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
 }
 
 template <int H>
-int launch_h(const ScoreParams &p, const void *tq, const void *tk, int grid, cudaStream_t s)
+int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *tk128, int grid, cudaStream_t s)
 {
     static bool attr_done[64] = {};
     int dev = 0;
@@ -452,7 +476,8 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, int grid, cud
         attr_done[dev] = true;
     }
     score_kernel<H><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(
-        *static_cast<const CUtensorMap *>(tq), *static_cast<const CUtensorMap *>(tk), p);
+        *static_cast<const CUtensorMap *>(tq), *static_cast<const CUtensorMap *>(tk),
+        *static_cast<const CUtensorMap *>(tk128), p);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -460,14 +485,15 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, int grid, cud
 
 uint32_t score_smem_bytes() { return SMEM_BYTES; }
 
-int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, int grid, void *stream)
+int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
+                 int grid, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (p.H) {
-    case 1: return launch_h<1>(p, tmap_q, tmap_k, grid, s);
-    case 2: return launch_h<2>(p, tmap_q, tmap_k, grid, s);
-    case 4: return launch_h<4>(p, tmap_q, tmap_k, grid, s);
-    case 8: return launch_h<8>(p, tmap_q, tmap_k, grid, s);
+    case 1: return launch_h<1>(p, tmap_q, tmap_k, tmap_k128, grid, s);
+    case 2: return launch_h<2>(p, tmap_q, tmap_k, tmap_k128, grid, s);
+    case 4: return launch_h<4>(p, tmap_q, tmap_k, tmap_k128, grid, s);
+    case 8: return launch_h<8>(p, tmap_q, tmap_k, tmap_k128, grid, s);
     default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
