@@ -32,7 +32,6 @@ std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int64_t g_cfg_path = 0;
-int64_t g_cfg_scorer = 0;
 uint64_t g_wait_ns = 2000000000ull;
 thread_local int32_t g_launches = 0;
 
@@ -150,8 +149,12 @@ bool use_filter(int64_t max_len, int32_t k)
     return f.stride >= 4 && max_len >= 8LL * k;
 }
 
+// Key tiles per row in the candidate arrays: a multiple of 8, so that every
+// row's mask words fill whole 128-byte lines.
+int64_t cand_tiles_ld(int64_t ld) { return ((ld + TILE_M - 1) / TILE_M + 7) / 8 * 8; }
+
 struct Layout {
-    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_cnt, cand;
+    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_mask, cand_score, cand_over;
     size_t total;
 };
 
@@ -170,9 +173,10 @@ Layout layout(int32_t R, int64_t ld, int32_t k)
     L.sample = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(f.sample_ld));
     L.tau = take(sizeof(float) * R);
     L.flag = take(sizeof(int32_t) * R);
-    const size_t tiles = static_cast<size_t>(((ld + TILE_M - 1) / TILE_M + 3) / 4 * 4);
-    L.cand_cnt = take(static_cast<size_t>(R) * tiles * 4);
-    L.cand = take(sizeof(uint2) * static_cast<size_t>(R) * tiles * 4 * CAND_SLOTS);
+    const size_t tiles = static_cast<size_t>(cand_tiles_ld(ld));
+    L.cand_mask = take(sizeof(uint32_t) * static_cast<size_t>(R) * tiles * 4);
+    L.cand_score = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_MAIN);
+    L.cand_over = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_OVER);
     L.total = o;
     return L;
 }
@@ -218,26 +222,11 @@ struct ScoreSetup {
     uint8_t *ws;
     CUtensorMap tq, tk, tk128;   // queries, key boxes of one page, key boxes of one tile
     ScoreParams sp;
-    bool rows_kernel;   // query rows on TMEM lanes (prefill-sized groups)
-    const void *q;
 };
-
-// Rows-on-lanes scorer for prefill-like batches (many rows per request, at
-// most 4 heads); the positions-on-lanes scorer otherwise (decode batches).
-bool want_rows_kernel(int32_t rows, int32_t H, int32_t num_reqs)
-{
-    // The rows-on-lanes scorer issues M=128 x N=32 MMAs, which measured at
-    // about a quarter of the tensor rate of the N=256 positions-on-lanes
-    // tiles, so it is only used when asked for.
-    (void)rows;
-    (void)num_reqs;
-    return H <= 4 && g_cfg_scorer == 2;
-}
 
 int launch_scorer(const ScoreSetup &s, int grid, void *stream)
 {
-    return s.rows_kernel ? launch_score_rows(s.sp, &s.tk, s.q, grid, stream)
-                         : launch_score(s.sp, &s.tq, &s.tk, &s.tk128, grid, stream);
+    return launch_score(s.sp, &s.tq, &s.tk, &s.tk128, grid, stream);
 }
 
 qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
@@ -262,9 +251,7 @@ qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t row
                    cache_rows >= TILE_M ? TILE_M : static_cast<uint32_t>(std::min(keys->page_positions, TILE_M)));
     if (st != QSA_OK) return st;
     auto at = [&](size_t off) { return s.ws + off; };
-    s.rows_kernel = want_rows_kernel(rows, H, keys->num_reqs);
-    s.q = q;
-    const int32_t group_rows = s.rows_kernel ? 128 : N_MAX / H;
+    const int32_t group_rows = N_MAX / H;
     st = launch_rc(timed(K_PLAN, stream, [&] {
         return launch_plan(row_req, row_visible, rows, group_rows, keys->num_reqs, max_len, sample_stride,
                            reinterpret_cast<int32_t *>(at(s.L.row_vis)),
@@ -341,11 +328,6 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
     if (key == QSA_CFG_PATH) {
         if (value < 0 || value > 2) return QSA_ERR_INVALID_ARG;
         g_cfg_path = value;
-        return QSA_OK;
-    }
-    if (key == QSA_CFG_SCORER) {
-        if (value < 0 || value > 2) return QSA_ERR_INVALID_ARG;
-        g_cfg_scorer = value;
         return QSA_OK;
     }
     if (key == QSA_CFG_KERNEL_TIMING) {
@@ -461,7 +443,7 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
     p.out_val = out_val;
     p.smem_cap = std::max(8192, k);
     p.status = d->status;
-    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, stream); }));
+    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, rows, stream); }));
 }
 
 qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, int32_t H,
@@ -509,15 +491,15 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
         sel.logits = logits;
         sel.ld = ld;
         sel.smem_cap = std::max(8192, k);
-        return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, stream); }));
+        return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, rows, stream); }));
     }
 
     float *sample = reinterpret_cast<float *>(at(s.L.sample));
     float *tau = reinterpret_cast<float *>(at(s.L.tau));
-    uint8_t *cand_cnt = reinterpret_cast<uint8_t *>(at(s.L.cand_cnt));
-    uint2 *cand = reinterpret_cast<uint2 *>(at(s.L.cand));
-    // multiple of 4 so that every row's count bytes start 16-byte aligned
-    const int32_t tiles_ld = static_cast<int32_t>(((ld + TILE_M - 1) / TILE_M + 3) / 4 * 4);
+    uint32_t *cand_mask = reinterpret_cast<uint32_t *>(at(s.L.cand_mask));
+    float *cand_score = reinterpret_cast<float *>(at(s.L.cand_score));
+    float *cand_over = reinterpret_cast<float *>(at(s.L.cand_over));
+    const int32_t tiles_ld = static_cast<int32_t>(cand_tiles_ld(ld));
 
     // 1. scores of every stride-th key tile
     s.sp.mode = SCORE_SAMPLE;
@@ -533,35 +515,46 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     th.sample_stride = f.stride;
     th.tau = tau;
     th.oversample = OVERSAMPLE;
-    th.smem_cap = static_cast<int32_t>(f.sample_ld);
-    if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, stream); }))) != QSA_OK) return st;
+    th.smem_cap = static_cast<int32_t>(std::min<int64_t>(f.sample_ld, 4096));   // staged scores per row
+    if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, rows, stream); }))) != QSA_OK) return st;
     // 3. full scoring pass keeping only scores >= tau_r
     s.sp.mode = SCORE_FILTER;
     s.sp.tau = tau;
-    s.sp.cand = cand;
-    s.sp.cand_cnt = cand_cnt;
+    s.sp.cand_score = cand_score;
+    s.sp.cand_over = cand_over;
+    s.sp.cand_mask = cand_mask;
     s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
     // 4. exact top-k of each candidate list; a row whose list cannot be trusted
-    //    (fewer than k candidates, or a slot overflow) is re-scored in full by
-    //    the selector itself and selected densely
+    //    (fewer than min(k, V) candidates, more than the selector holds, or a
+    //    tie bucket at the cut too large to order there) is flagged ...
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
-    cs.cand = cand;
-    cs.cand_cnt = cand_cnt;
+    cs.cand_score = cand_score;
+    cs.cand_over = cand_over;
+    cs.cand_mask = cand_mask;
     cs.tiles_ld = tiles_ld;
-    cs.smem_cap = f.cap;
-    cs.q = static_cast<const uint16_t *>(q);
-    cs.w = w;
-    cs.k_cache = static_cast<const uint16_t *>(keys->k_cache);
-    cs.block_table = keys->block_table;
-    cs.row_req = row_req;
-    cs.H = H;
-    cs.max_pages = keys->max_pages_per_req;
-    cs.num_pages = keys->num_pages;
-    cs.page_pos = keys->page_positions;
-    cs.fb_logits = logits;
-    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, stream); }));
+    cs.cap = f.cap;
+    if ((st = launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, stream); }))) != QSA_OK) return st;
+    // 5. ... and re-scored in full here (plain FP32) then selected densely; the
+    //    launch ends at once when no row was flagged
+    SelectParams fb = sel;
+    fb.mode = SEL_FALLBACK;
+    fb.logits = logits;
+    fb.ld = ld;
+    fb.smem_cap = std::max(8192, k);
+    fb.q = static_cast<const uint16_t *>(q);
+    fb.w = w;
+    fb.k_cache = static_cast<const uint16_t *>(keys->k_cache);
+    fb.block_table = keys->block_table;
+    fb.row_req = row_req;
+    fb.H = H;
+    fb.max_pages = keys->max_pages_per_req;
+    fb.num_pages = keys->num_pages;
+    fb.page_pos = keys->page_positions;
+    fb.fb_logits = logits;
+    const int fb_grid = std::min(rows, 2 * d->sms);
+    return launch_rc(timed(K_SEL_FLAGGED, stream, [&] { return launch_select(fb, fb_grid, stream); }));
 }
 
 }  // extern "C"

@@ -18,7 +18,22 @@ constexpr int N_MAX = 256;       // MMA N: (query rows of a group) x heads
 constexpr int KSTAGES = 4;       // key tiles in flight per CTA
 constexpr int EPI_WARPS = 16;    // 4 per TMEM lane quarter, each owning 64 accumulator columns
 constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, then epilogue
-constexpr int CAND_SLOTS = 32;   // candidate slots per (row, key tile, 32-position quarter): one per lane, so a quarter never overflows
+
+// Candidate lists of the filter pass.  Key tile t of row r has four quarters
+// q of 32 positions (t*128 + q*32 + i, i < 32); quarter e = 4*t + q of row r:
+//   cand_mask[r*tiles_ld*4 + e], bit i: position t*128 + q*32 + i passed;
+//   the j-th passing position of the quarter (ascending i) has its score at
+//   cand_score[(r*tiles_ld*4 + e)*8 + j]              for j < 8,
+//   cand_over[(r*tiles_ld*4 + e)*24 + j - 8]          for 8 <= j < 32.
+// A row's first eight slots per quarter are one contiguous run (one 128-byte
+// line per key tile), so the selector streams them like any dense array;
+// slots 0..7 of a quarter are always written (lanes that did not pass fill
+// the unused ones), so every sector is written whole.  More than eight
+// candidates in one quarter is rare (the filter keeps a few percent of the
+// positions) and goes to the overflow array.  tiles_ld is a multiple of 8,
+// which keeps each row's mask words in lines of its own.
+constexpr int CAND_MAIN = 8;     // score slots per quarter in cand_score
+constexpr int CAND_OVER = 24;    // further slots per quarter in cand_over
 
 // A group: consecutive query rows of one request that share every key tile.
 struct Group {
@@ -64,17 +79,19 @@ struct ScoreParams {
     int64_t ld;
     int32_t pad_inf;            // LOGITS: write -inf for V_r <= j < tile end (j < ld)
     const float *tau;           // FILTER: per-row threshold
-    uint2 *cand;                // FILTER: [R, tiles_ld, 4, CAND_SLOTS] (score bits, position)
-    uint8_t *cand_cnt;          // FILTER: [R, tiles_ld, 4] candidates found per quarter tile
-    int32_t tiles_ld;           // key tiles per row in the candidate arrays
+    float *cand_score;          // FILTER: [R, tiles_ld * 4, CAND_MAIN] candidate scores (layout above)
+    float *cand_over;           // FILTER: [R, tiles_ld * 4, CAND_OVER]
+    uint32_t *cand_mask;        // FILTER: [R, tiles_ld * 4] passing positions of each quarter
+    int32_t tiles_ld;           // key tiles per row in the candidate arrays (multiple of 8)
     uint32_t *status;
     uint64_t wait_limit_ns;
 };
 
 enum SelectMode : int32_t {
     SEL_DENSE = 0,      // row r = logits[r, 0:V_r]
-    SEL_CAND = 1,       // row r = candidate list; flags the row when it is unusable
+    SEL_FALLBACK = 1,   // flagged rows only: re-scored in full, then selected as dense rows
     SEL_THRESH = 2,     // row r = sample row; writes tau_r
+    SEL_CAND = 3,       // row r = candidate list; flags the row when it cannot be trusted
 };
 
 struct SelectParams {
@@ -85,14 +102,15 @@ struct SelectParams {
     int64_t ld;
     int64_t max_len;            // largest valid V_r (longer rows are clamped and flagged)
     const int32_t *row_vis;     // V_r
-    const uint2 *cand;          // CAND: slots written by the filter scorer
-    const uint8_t *cand_cnt;
+    const float *cand_score;    // CAND: lists written by the filter scorer
+    const float *cand_over;
+    const uint32_t *cand_mask;
     int32_t tiles_ld;
-    int32_t cap;                // THRESH: rows up to this length keep every position
-    int32_t *row_flag;          // CAND: set for rows that took the dense fallback
+    int32_t cap;                // THRESH: rows up to this length keep every position; CAND: list capacity
+    int32_t *row_flag;          // CAND: 1 for rows left to the fallback launch, else 0
     Plan *plan;
-    // CAND fallback: a row whose candidate list cannot be trusted is re-scored
-    // here (plain FP32 arithmetic) into fb_logits[r * max_len ...] and selected densely
+    // FALLBACK: a flagged row is re-scored (plain FP32 arithmetic) into
+    // fb_logits[r * max_len ...] and selected densely
     const uint16_t *q;          // FP16 bits [R, H, 128]
     const float *w;             // [R, H]
     const uint16_t *k_cache;    // FP16 bits [num_pages, page_pos, 128]
@@ -118,8 +136,7 @@ int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, i
                 uint32_t *status, void *stream);
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
                  int grid, void *stream);
-int launch_score_rows(const ScoreParams &p, const void *tmap_k, const void *q, int grid, void *stream);
-int launch_select(const SelectParams &p, void *stream);
+int launch_select(const SelectParams &p, int grid, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream);

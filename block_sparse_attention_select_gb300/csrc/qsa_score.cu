@@ -140,16 +140,16 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
     const int32_t p_in_tile = quarter * 32 + lane;
     const int32_t j = tile * TILE_M + p_in_tile;
     const int64_t r0 = static_cast<int64_t>(gr.row0) + cq * RPW;     // first row of this warp
-    // FILTER: candidate slots and count bytes of (row r0, tile, quarter); a row
-    // further is slot_stride entries further
-    const int64_t slot0 = (r0 * p.tiles_ld + tile) * 4 + quarter;
-    const int64_t slot_stride = static_cast<int64_t>(p.tiles_ld) * 4;
-    uint2 *cand0 = nullptr;
-    uint8_t *cnt0 = nullptr;
+    // FILTER: quarter e0 of row r0 (score slots and mask word); a row further
+    // is tiles_ld * 4 quarters further
+    const int64_t e0 = (r0 * p.tiles_ld + tile) * 4 + quarter;
+    const int64_t q_stride = static_cast<int64_t>(p.tiles_ld) * 4;
+    float *score0 = nullptr;
+    uint32_t *mask0 = nullptr;
     float *out0 = nullptr;
     if constexpr (MODE == SCORE_FILTER) {
-        cand0 = p.cand + slot0 * CAND_SLOTS + __popc(lt_mask);   // this lane's slot if all lanes took
-        cnt0 = p.cand_cnt + slot0;
+        score0 = p.cand_score + e0 * CAND_MAIN;
+        mask0 = p.cand_mask + e0;
     } else if constexpr (MODE == SCORE_SAMPLE) {
         out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
     } else {
@@ -162,7 +162,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + ch * 32), v);
         tmem_ld_wait();
-        uint32_t my_count = 0;                                 // FILTER: count of row (c0 + lane)
+        uint32_t my_mask = 0;                                  // FILTER: mask word of row (c0 + lane)
 #pragma unroll
         for (int b0 = 0; b0 < RPC; b0 += B) {
             if (!ALLROWS && c0 + b0 >= nmine) break;         // warp-uniform
@@ -181,11 +181,18 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                 if constexpr (MODE == SCORE_FILTER) {
                     const bool take = ok && s[i] >= e.tau[el];
                     const uint32_t m = __ballot_sync(0xffffffffu, take);
-                    if (lane == b0 + i) my_count = __popc(m);
-                    static_assert(CAND_SLOTS >= 32, "one slot per lane");
-                    if (take)
-                        cand0[el * slot_stride * CAND_SLOTS + __popc(m & lt_mask) - __popc(lt_mask)] =
-                            make_uint2(__float_as_uint(s[i]), static_cast<uint32_t>(j));
+                    if (lane == b0 + i) my_mask = m;
+                    // a passing lane takes slot (passing lanes below it); the
+                    // others fill slots popc(m), popc(m)+1, ... so that slots
+                    // 0..7 are all written (their contents are never read)
+                    const int c = __popc(m);
+                    const int rk = __popc(m & lt_mask);
+                    const int slot = take ? rk : c + lane - rk;
+                    if (live && slot < CAND_MAIN) score0[el * q_stride * CAND_MAIN + slot] = s[i];
+                    if (c > CAND_MAIN) {                          // warp-uniform, rare
+                        if (take && rk >= CAND_MAIN)
+                            p.cand_over[(e0 + el * q_stride) * CAND_OVER + rk - CAND_MAIN] = s[i];
+                    }
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
                 } else {
@@ -196,8 +203,8 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
             }
         }
         if constexpr (MODE == SCORE_FILTER) {
-            // one store for the chunk: lane i writes the count of row c0 + i
-            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) cnt0[(c0 + lane) * slot_stride] = static_cast<uint8_t>(my_count);
+            // one store for the chunk: lane i writes the mask word of row c0 + i
+            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) mask0[(c0 + lane) * q_stride] = my_mask;
         }
     }
 }

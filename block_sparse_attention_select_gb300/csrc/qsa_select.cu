@@ -518,19 +518,12 @@ __device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, floa
 }
 
 // Entries of the ordered-output buffer: k plus room for the bucket holding
-// the k-th element; in candidate mode also big enough to stage the row's
-// count bytes (16-byte padded).
-__host__ __device__ __forceinline__ int32_t out_capacity(const SelectParams &p)
-{
-    if (p.mode == SEL_THRESH) return 0;
-    int32_t cap = p.k + SLACK;
-    if (p.mode == SEL_CAND) {
-        const int32_t stage = (p.tiles_ld * 4 + 15) / 16 * 2;   // 16-byte vectors, 8 bytes per entry
-        cap = cap > stage ? cap : stage;
-    }
-    return cap;
-}
+// the k-th element.
+__host__ __device__ __forceinline__ int32_t out_capacity(const SelectParams &p) { return p.k + SLACK; }
 
+// Dense rows (logits in HBM), or, in fallback mode, the rows the candidate
+// selector flagged: those are re-scored here first.  Rows r = blockIdx.x,
+// blockIdx.x + gridDim.x, ...
 __global__ void __launch_bounds__(NT, 4)
 select_kernel(const SelectParams p)
 {
@@ -540,146 +533,22 @@ select_kernel(const SelectParams p)
     uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + out_capacity(p));
     uint32_t *inv = keys + p.smem_cap;
 
-    const int32_t r = blockIdx.x;
-    if (r >= p.R) return;
-    int32_t V = p.row_vis[r];
-    if (V < 0 || V > p.max_len) {
-        if (threadIdx.x == 0) record_error(p.status, ST_BAD_ROW);
-        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
-    }
-
-    if (p.mode == SEL_THRESH) {
-        // tau_r from the sampled scores of row r (columns [0, n_s) of its sample row)
-        const int32_t tiles = (V + TILE_M - 1) / TILE_M;
-        int32_t n_s = 0;
-        if (tiles > 0) {
-            const int32_t t_last = ((tiles - 1) / p.sample_stride) * p.sample_stride;
-            n_s = (t_last / p.sample_stride) * TILE_M + min(TILE_M, V - t_last * TILE_M);
+    if (p.mode == SEL_FALLBACK && __ldcg(&p.plan->any_fallback) == 0) return;
+    for (int32_t r = blockIdx.x; r < p.R; r += gridDim.x) {
+        if (p.mode == SEL_FALLBACK && __ldcg(p.row_flag + r) == 0) continue;   // uniform
+        int32_t V = p.row_vis[r];
+        if (V < 0 || V > p.max_len) {
+            if (threadIdx.x == 0) record_error(p.status, ST_BAD_ROW);
+            V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
         }
-        float tau = -__int_as_float(0x7f800000);
-        if (V > p.cap && n_s > 0) {
-            const double want = static_cast<double>(p.oversample) * p.k * n_s / V;
-            int32_t m = static_cast<int32_t>(ceil(want)) + 8;
-            m = max(1, min(m, n_s));
-            const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
-            uint32_t T;
-            if (n_s <= p.smem_cap) {
-                // one histogram level suffices: tau only has to keep about m
-                // sampled scores; the candidate count is verified afterwards
-                uint32_t lo = 0xffffffffu, hi = 0u;
-                for (int32_t i = threadIdx.x; i < n_s; i += NT) {
-                    const uint32_t kv = score_key(__ldg(row + i));
-                    keys[i] = kv;
-                    lo = min(lo, kv);
-                    hi = max(hi, kv);
-                }
-                block_minmax(sh, lo, hi, lo, hi);
-                // two range-adaptive levels: the sample's range includes the
-                // spike of zero scores, so one level is too coarse near tau
-                uint32_t k_left = static_cast<uint32_t>(m);
-                for (int lv = 0; lv < 2 && lo != hi; ++lv) {
-                    const int shift = span_shift(hi - lo);
-                    clear_hist(sh);
-                    for (int32_t i = threadIdx.x; i < n_s; i += NT) {
-                        const uint32_t kv = keys[i];
-                        if (kv >= lo && kv <= hi) atomicAdd(&sh.hist[(kv - lo) >> shift], 1u);
-                    }
-                    __syncthreads();
-                    find_cut(sh, k_left);
-                    k_left -= sh.cut_above;
-                    const uint32_t nlo = lo + (sh.cut_digit << shift);
-                    const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
-                    hi = static_cast<uint32_t>(min(static_cast<uint64_t>(hi), nhi));
-                    lo = nlo;
-                    __syncthreads();
-                }
-                T = lo;
-            } else {
-                uint32_t k2;
-                stream_narrow(sh, row, n_s, static_cast<uint32_t>(m), 0, nullptr, nullptr, T, k2, false);
-            }
-            tau = key_score(T);
-        }
-        if (threadIdx.x == 0) p.tau[r] = tau;
-        return;
-    }
-
-    int32_t n = -1;
-    const int32_t kk_target = min(p.k, V);
-    const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
-    if (p.mode == SEL_CAND) {
-        // the candidate slots of the row's key tiles: one (tile, 32-position
-        // part) list per entry, its length in cnt[]
-        const int32_t ne = ((V + TILE_M - 1) / TILE_M) * 4;
-        const uint8_t *cnt = p.cand_cnt + static_cast<int64_t>(r) * p.tiles_ld * 4;
-        const uint2 *slots = p.cand + static_cast<int64_t>(r) * p.tiles_ld * 4 * CAND_SLOTS;
-        // stage the count bytes in shared memory (out64 is free until the
-        // selection) with 16-byte loads: one round trip for the whole row
-        uint8_t *cnt_s = reinterpret_cast<uint8_t *>(out64);
-        const int32_t nvec = (ne + 15) / 16;
-        for (int32_t v16 = threadIdx.x; v16 < nvec; v16 += NT)
-            reinterpret_cast<uint4 *>(cnt_s)[v16] = __ldcg(reinterpret_cast<const uint4 *>(cnt) + v16);
-        __syncthreads();
-        uint32_t sum = 0;
-        bool over = false;
-        for (int32_t e = threadIdx.x; e < ne; e += NT) {
-            const uint32_t c = cnt_s[e];
-            over |= c > CAND_SLOTS;
-            sum += c;
-        }
-        block_excl_scan<NT>(sum, sh.wtot, &sh.total);
-        const bool any_over = __syncthreads_or(over) != 0;
-        const uint32_t total = sh.total;
-        if (any_over || total < static_cast<uint32_t>(kk_target) || total > static_cast<uint32_t>(p.smem_cap)) {
-            // the sample misled the threshold for this row: score it in full here
-            if (threadIdx.x == 0) {
-                p.row_flag[r] = 1;
-                atomicExch(&p.plan->any_fallback, 1);
-            }
+        const int32_t kk_target = min(p.k, V);
+        const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+        if (p.mode == SEL_FALLBACK) {
             float *fb = p.fb_logits + static_cast<int64_t>(r) * p.max_len;
             simt_score_row(p, r, V, fb, reinterpret_cast<float *>(keys));
             row = fb;
-        } else {
-            if (threadIdx.x == 0) p.row_flag[r] = 0;
-            uint32_t done = 0;
-            for (int32_t e0 = 0; e0 < ne; e0 += NBINS) {
-                const int32_t chunk = min(NBINS, ne - e0);
-                for (int32_t i = threadIdx.x; i < NBINS; i += NT) sh.hist[i] = i < chunk ? cnt_s[e0 + i] : 0u;
-                __syncthreads();
-                bucket_starts(sh);                        // bstart = offsets within the chunk
-                // owner map: candidate slot id of every output position
-                for (int32_t i = threadIdx.x; i < chunk; i += NT) {
-                    const uint32_t c = cnt_s[e0 + i];
-                    for (uint32_t q = 0; q < c; ++q)
-                        inv[done + sh.bstart[i] + q] = static_cast<uint32_t>(e0 + i) * CAND_SLOTS + q;
-                    if (i == chunk - 1) sh.taken = sh.bstart[i] + c;   // chunk total
-                }
-                __syncthreads();
-                const uint32_t ctot = sh.taken;
-                // every thread fetches its candidates, eight loads in flight
-                for (uint32_t t0 = threadIdx.x; t0 < ctot; t0 += 8 * NT) {
-                    uint2 v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t t = t0 + u * NT;
-                        if (t < ctot) v[u] = slots[inv[done + t]];
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t t = t0 + u * NT;
-                        if (t < ctot) {
-                            keys[done + t] = score_key(__uint_as_float(v[u].x));
-                            inv[done + t] = ~v[u].y;
-                        }
-                    }
-                }
-                __syncthreads();
-                done += ctot;
-            }
-            n = static_cast<int32_t>(total);
         }
-    }
-    if (n < 0) {
+        int32_t n;
         if (V <= p.smem_cap) {
             for (int32_t i = threadIdx.x; i < V; i += NT) {
                 keys[i] = score_key(__ldcg(row + i));
@@ -693,17 +562,428 @@ select_kernel(const SelectParams p)
                               k_rem, true);
             if (n < 0) n = gather_cut_in_order(sh, row, V, T, k_rem, keys, inv);
         }
+        const int32_t kk = min(p.k, n);
+        const uint64_t *result = out64;
+        if (kk > 0) {
+            uint64_t *ranked = reinterpret_cast<uint64_t *>(keys);   // keys + inv: smem_cap 8-byte slots
+            if (bucket_topk(sh, keys, inv, n, kk, out64, min(out_capacity(p), p.smem_cap), ranked))
+                result = ranked;
+            else
+                select_and_sort(sh, keys, inv, n, kk, out64);
+        }
+        write_row(p, r, result, kk);
+        __syncthreads();
     }
-    const int32_t kk = min(p.k, n);
-    const uint64_t *result = out64;
+}
+
+// ------------------------------------------------------------ candidates --
+//
+// One CTA per row.  The row's mask words and the first score line of every
+// quarter are loaded together (one round trip), each thread appends its
+// quarters' candidates as full keys (key32 << 32 | ~position) at its
+// exclusive-scan offset, and the top kk are ordered by one counting pass on
+// the top 11 bits of (key32 - smallest key) plus rank counting inside the
+// buckets; each element's rank is its output index, so the result goes
+// straight to HBM.  A row whose list cannot be trusted (fewer than min(k, V)
+// candidates, more than cap, or a cut bucket too large to order here) is
+// flagged and left to the fallback launch.
+constexpr int CT = 256;               // threads per row
+constexpr int QPT = 12;               // half quarters per thread and gather round
+constexpr int BIG_MAX = 320;          // > (QSA_MAX_K + SLACK) / (RANK_MAX + 1)
+
+struct CandShared {
+    uint32_t hist[NBINS];
+    uint32_t wtot[2][CT / 32];
+    uint32_t red_min[CT / 32], red_max[CT / 32];
+    uint32_t cut, need, nbig, pad_;
+    uint32_t big[BIG_MAX];
+};
+
+// Exclusive prefix of v over the block with a single barrier; wt alternates
+// between two buffers so that consecutive calls need no barrier in between.
+__device__ __forceinline__ uint32_t cand_scan(uint32_t v, uint32_t *wt, uint32_t &total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wt[wid] = x;
+    __syncthreads();
+    uint32_t before = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < CT / 32; ++w) {
+        const uint32_t c = wt[w];
+        before += w < wid ? c : 0u;
+        tot += c;
+    }
+    total = tot;
+    return before + x - v;
+}
+
+// Loads kept where they are written: all of a thread's loads are in flight
+// before the first of them is used (the compiler would otherwise move each
+// load next to its first use, inside the per-candidate loop).
+__device__ __forceinline__ uint32_t ld_issue_u32(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_issue_f4(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void discard_l2_line(const void *p)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+__global__ void __launch_bounds__(CT, 3)
+cand_kernel(const SelectParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    CandShared &sh = *reinterpret_cast<CandShared *>(smem_raw);
+    uint64_t *a = reinterpret_cast<uint64_t *>(smem_raw + sizeof(CandShared));   // cap entries
+    uint64_t *bq = a + p.cap;                                                     // k + SLACK entries
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const int32_t r = blockIdx.x;
+    if (r >= p.R) return;
+    int32_t V = p.row_vis[r];
+    if (V < 0 || V > p.max_len) {
+        if (t == 0) record_error(p.status, ST_BAD_ROW);
+        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
+    }
+    const int32_t kk_target = min(p.k, V);
+    const int32_t ntile = (V + TILE_M - 1) / TILE_M;
+    const int32_t nh = ntile * 8;                  // half quarters: 4 slots each
+    const int64_t q_row = static_cast<int64_t>(r) * p.tiles_ld * 4;
+    const uint32_t *mrow = p.cand_mask + q_row;
+    const float *srow = p.cand_score + q_row * CAND_MAIN;
+    const float *orow = p.cand_over + q_row * CAND_OVER;
+    for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
+    if (t == 0) sh.nbig = 0;
+
+    // ---- gather.  Thread pair (2i, 2i+1) takes quarter e: the even thread
+    //      its candidates 0..3, the odd one 4..7 and any overflow; a warp's
+    //      load covers 512 contiguous bytes of the row's slots.
+    const uint32_t par = static_cast<uint32_t>(t & 1);
+    uint32_t kmin = 0xffffffffu, kmax = 0u, done = 0;
+    bool overflow = false;
+    int sbuf = 0;
+    for (int32_t h0 = 0; h0 < nh; h0 += QPT * CT) {
+        uint32_t m[QPT];
+        float4 f[QPT];
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            const int32_t h = h0 + t + u * CT;
+            m[u] = 0u;
+            if (h < nh) {
+                m[u] = ld_issue_u32(mrow + (h >> 1));
+                f[u] = ld_issue_f4(srow + 4 * h);
+            }
+        }
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            const uint32_t c = __popc(m[u]);
+            cnt += par ? (c > 4u ? c - 4u : 0u) : min(c, 4u);
+        }
+        uint32_t ctot;
+        const uint32_t base = cand_scan(cnt, sh.wtot[sbuf], ctot);
+        sbuf ^= 1;
+        if (done + ctot > static_cast<uint32_t>(p.cap)) { overflow = true; break; }   // uniform
+        uint32_t o = done + base;
+#pragma unroll
+        for (int u = 0; u < QPT; ++u) {
+            uint32_t mm = m[u];
+            if (par) {
+#pragma unroll
+                for (int z = 0; z < 4; ++z) mm &= mm - 1u;       // skip the even thread's four
+            }
+            if (mm == 0u) continue;
+            const int32_t e = (h0 + t + u * CT) >> 1;
+            const uint32_t pos0 = static_cast<uint32_t>(e) * 32u;
+            const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {                     // slots 4*par + jj, in registers
+                if (mm == 0u) break;
+                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                mm &= mm - 1u;
+                const uint32_t key = score_key(fv[jj]);
+                kmin = min(kmin, key);
+                kmax = max(kmax, key);
+                a[o++] = (static_cast<uint64_t>(key) << 32) | ~(pos0 + bit);
+            }
+            if (par && mm != 0u) {
+                // more than eight candidates in this quarter (rare): the
+                // overflow slots, kept out of the loop above so that its
+                // iterations carry no global load
+                const float *ov_q = orow + static_cast<int64_t>(e) * CAND_OVER;
+#pragma unroll 1
+                for (uint32_t j = 0; mm != 0u; ++j) {
+                    const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                    mm &= mm - 1u;
+                    const uint32_t key = score_key(__ldcg(ov_q + j));
+                    kmin = min(kmin, key);
+                    kmax = max(kmax, key);
+                    a[o++] = (static_cast<uint64_t>(key) << 32) | ~(pos0 + bit);
+                }
+            }
+        }
+        done += ctot;
+    }
+    // block min / max of the keys; the barrier also publishes a[]
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) { sh.red_min[wid] = kmin; sh.red_max[wid] = kmax; }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < CT / 32; ++w) { kmin = min(kmin, sh.red_min[w]); kmax = max(kmax, sh.red_max[w]); }
+    // every candidate line of the row has been read: drop it from L2 unwritten
+    for (int32_t tl = t; tl < ntile; tl += CT) discard_l2_line(srow + static_cast<int64_t>(tl) * 4 * CAND_MAIN);
+    for (int32_t l = t; l < (ntile * 16 + 127) / 128; l += CT) discard_l2_line(mrow + l * 32);
+
+    const uint32_t n = done;
+    if (overflow || n < static_cast<uint32_t>(kk_target)) {
+        if (t == 0) {
+            p.row_flag[r] = 1;
+            atomicExch(&p.plan->any_fallback, 1);
+        }
+        return;
+    }
+    const uint32_t kk = min(static_cast<uint32_t>(p.k), n);
+    int32_t *oi = p.out_idx + static_cast<int64_t>(r) * p.k;
+    float *ov = p.out_val ? p.out_val + static_cast<int64_t>(r) * p.k : nullptr;
     if (kk > 0) {
-        uint64_t *ranked = reinterpret_cast<uint64_t *>(keys);   // keys + inv: smem_cap 8-byte slots
-        if (bucket_topk(sh, keys, inv, n, kk, out64, min(out_capacity(p), p.smem_cap), ranked))
-            result = ranked;
-        else
-            select_and_sort(sh, keys, inv, n, kk, out64);
+        // ---- counting pass: bucket 0 holds the largest keys
+        const int shift = span_shift(kmax - kmin);
+        for (uint32_t i = t; i < n; i += CT)
+            atomicAdd(&sh.hist[NBINS - 1 - ((static_cast<uint32_t>(a[i] >> 32) - kmin) >> shift)], 1u);
+        __syncthreads();
+        uint32_t c[BPT], sum = 0;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) { c[i] = sh.hist[BPT * t + i]; sum += c[i]; }
+        uint32_t all;
+        uint32_t start = cand_scan(sum, sh.wtot[sbuf], all);
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+            if (start < kk && kk <= start + c[i]) { sh.cut = BPT * t + i; sh.need = start + c[i]; }
+            sh.hist[BPT * t + i] = start;        // scatter cursor
+            start += c[i];
+        }
+        __syncthreads();
+        const uint32_t bb = sh.cut, need = sh.need;
+        if (need > static_cast<uint32_t>(p.k + SLACK)) {           // uniform: huge tie bucket at the cut
+            if (t == 0) {
+                p.row_flag[r] = 1;
+                atomicExch(&p.plan->any_fallback, 1);
+            }
+            return;
+        }
+        // ---- scatter the buckets down to the cut
+        for (uint32_t i = t; i < n; i += CT) {
+            const uint64_t x = a[i];
+            const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - kmin) >> shift);
+            if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = x;
+        }
+        __syncthreads();
+        // ---- rank inside the bucket = place in the output (hist[b] is now
+        //      the end of bucket b, hence the start of bucket b + 1)
+        for (uint32_t pos = t; pos < need; pos += CT) {
+            const uint64_t x = bq[pos];
+            const uint32_t key = static_cast<uint32_t>(x >> 32);
+            const uint32_t b = NBINS - 1 - ((key - kmin) >> shift);
+            const uint32_t s0 = b ? sh.hist[b - 1] : 0u, e = sh.hist[b];
+            if (e - s0 > RANK_MAX) {
+                if (pos == s0) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
+                continue;
+            }
+            uint32_t rk = s0;
+            for (uint32_t q = s0; q < e; ++q) rk += bq[q] > x;
+            if (rk < kk) {
+                oi[rk] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+                if (ov) ov[rk] = key_score(key);
+            }
+        }
+        __syncthreads();
+        for (uint32_t q = wid; q < sh.nbig; q += CT / 32) {
+            const uint32_t b = sh.big[q];
+            const uint32_t s0 = b ? sh.hist[b - 1] : 0u, m = sh.hist[b] - s0;
+            warp_sort_desc(bq + s0, static_cast<int32_t>(m));
+            for (uint32_t i = lane; i < m && s0 + i < kk; i += 32) {
+                const uint64_t x = bq[s0 + i];
+                oi[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+                if (ov) ov[s0 + i] = key_score(static_cast<uint32_t>(x >> 32));
+            }
+        }
     }
-    write_row(p, r, result, kk);
+    for (int32_t i = static_cast<int32_t>(kk) + t; i < p.k; i += CT) {
+        oi[i] = -1;
+        if (ov) ov[i] = -__int_as_float(0x7f800000);
+    }
+    if (t == 0) p.row_flag[r] = 0;
+}
+
+// ------------------------------------------------------------- threshold --
+//
+// tau_r for the filter pass: a value with about m sampled scores at or above
+// it, m = oversample * k * n_s / V_r (+8), the expected share of the top k in
+// the sample.  tau only has to be low enough; the candidate count it yields
+// is checked by the candidate selector, so the search stops as soon as the
+// bin holding the m-th sampled key is small.  One warp per row: the sample is
+// a few thousand scores, too little work for a block and its barriers.  The
+// row is copied to shared memory with every copy in flight at once (rows
+// longer than the staging area are read from global memory instead).
+constexpr int TH_WARPS = 4;
+constexpr int TH_BINS = 256;
+constexpr int TH_STAGE = 4096;        // sampled scores of one row held in shared memory
+
+__device__ __forceinline__ uint32_t warp_min(uint32_t v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t warp_max(uint32_t v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(TH_WARPS * 32)
+thresh_kernel(const SelectParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int32_t r = blockIdx.x * TH_WARPS + wid;
+    if (r >= p.R) return;                       // whole warps leave; only warp-level sync below
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem_raw) + wid * TH_BINS;
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw) + TH_WARPS * TH_BINS + wid * p.smem_cap;
+    int32_t V = p.row_vis[r];
+    if (V < 0 || V > p.max_len) {
+        if (lane == 0) record_error(p.status, ST_BAD_ROW);
+        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
+    }
+    // sampled tiles 0, s, 2s, ... of the row, the last one possibly partial
+    const int32_t tiles = (V + TILE_M - 1) / TILE_M;
+    int32_t n_s = 0;
+    if (tiles > 0) {
+        const int32_t t_last = ((tiles - 1) / p.sample_stride) * p.sample_stride;
+        n_s = (t_last / p.sample_stride) * TILE_M + min(TILE_M, V - t_last * TILE_M);
+    }
+    float tau = -__int_as_float(0x7f800000);
+    if (V > p.cap && n_s > 0) {
+        const double want = static_cast<double>(p.oversample) * p.k * n_s / V;
+        const uint32_t m = static_cast<uint32_t>(max(1, min(static_cast<int32_t>(ceil(want)) + 8, n_s)));
+        const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+        const bool staged = n_s <= p.smem_cap;
+        if (staged) {
+            const int32_t nv = n_s >> 2;                       // row start is 16-byte aligned
+            for (int32_t v = lane; v < nv; v += 32)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             ::"r"(smem_u32(stage + 4 * v)), "l"(row + 4 * v) : "memory");
+            for (int32_t i = 4 * nv + lane; i < n_s; i += 32) stage[i] = __float_as_uint(__ldcg(row + i));
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            __syncwarp();
+            for (int32_t i = lane; i < n_s; i += 32) stage[i] = score_key(__uint_as_float(stage[i]));
+            __syncwarp();
+        }
+        auto key_at = [&](int32_t i) { return staged ? stage[i] : score_key(__ldcg(row + i)); };
+        // key range of the sample, and of its scores above zero: when at
+        // least m are positive the spike of exact zeros (every head clipped)
+        // lies below the cut and is left out of the range
+        const uint32_t zk = score_key(0.0f);
+        uint32_t lo = 0xffffffffu, hi = 0u, lo_pos = 0xffffffffu, npos = 0;
+        for (int32_t i = lane; i < n_s; i += 32) {
+            const uint32_t kv = key_at(i);
+            lo = min(lo, kv);
+            hi = max(hi, kv);
+            if (kv > zk) { lo_pos = min(lo_pos, kv); ++npos; }
+        }
+        lo = warp_min(lo);
+        hi = warp_max(hi);
+        lo_pos = warp_min(lo_pos);
+        npos = warp_sum(npos);
+        if (npos >= m) lo = lo_pos;
+        const uint32_t stop = max(8u, m / 16);
+        uint32_t k_left = m;
+        while (lo != hi) {
+            const uint32_t span = hi - lo;
+            const int bits = 32 - __clz(span);
+            const int shift = bits > 8 ? bits - 8 : 0;        // (hi - lo) >> shift < TH_BINS
+#pragma unroll
+            for (int b = 0; b < TH_BINS / 32; ++b) hist[lane + 32 * b] = 0;
+            __syncwarp();
+            for (int32_t i = lane; i < n_s; i += 32) {
+                const uint32_t kv = key_at(i);
+                if (kv >= lo && kv <= hi) atomicAdd(&hist[(kv - lo) >> shift], 1u);
+            }
+            __syncwarp();
+            // lane l holds bins 255-8l down to 248-8l: lanes in descending key order
+            uint32_t c[8], s = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = hist[TH_BINS - 1 - 8 * lane - j];
+                s += c[j];
+            }
+            uint32_t incl = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t excl = incl - s;
+            const uint32_t hit = __ballot_sync(0xffffffffu, excl < k_left && k_left <= incl);
+            if (hit == 0u) break;                              // cannot happen: k_left <= keys in range
+            const int src = __ffs(hit) - 1;
+            uint32_t d = 0, above = excl, eq = 0;
+            if (lane == src) {
+                bool found = false;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (!found && k_left <= above + c[j]) {
+                        found = true;
+                        d = static_cast<uint32_t>(TH_BINS - 1 - 8 * lane - j);
+                        eq = c[j];
+                    } else if (!found) {
+                        above += c[j];
+                    }
+                }
+            }
+            d = __shfl_sync(0xffffffffu, d, src);
+            above = __shfl_sync(0xffffffffu, above, src);
+            eq = __shfl_sync(0xffffffffu, eq, src);
+            k_left -= above;
+            const uint32_t nlo = lo + (d << shift);
+            const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
+            hi = static_cast<uint32_t>(min(static_cast<uint64_t>(hi), nhi));
+            lo = nlo;
+            __syncwarp();
+            if (eq <= stop) break;
+        }
+        tau = key_score(lo);
+    }
+    if (lane == 0) p.tau[r] = tau;
 }
 
 }  // namespace
@@ -713,21 +993,50 @@ size_t select_smem_bytes(int32_t smem_cap)
     return sizeof(SelShared) + static_cast<size_t>(smem_cap) * 8;
 }
 
-int launch_select(const SelectParams &p, void *stream)
+namespace {
+
+template <typename K>
+int set_smem(K kernel, size_t smem, size_t (&done)[64])
 {
-    const size_t smem = sizeof(SelShared) + static_cast<size_t>(out_capacity(p)) * 8 +
-                        static_cast<size_t>(p.smem_cap) * (p.mode == SEL_THRESH ? 4 : 8);
-    static size_t attr_bytes[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
-    if (smem > attr_bytes[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (smem > done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return static_cast<int>(e);
-        attr_bytes[dev] = smem;
+        done[dev] = smem;
     }
-    select_kernel<<<p.R, NT, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    return 0;
+}
+
+}  // namespace
+
+int launch_select(const SelectParams &p, int grid, void *stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (grid <= 0) return static_cast<int>(cudaGetLastError());
+    if (p.mode == SEL_THRESH) {
+        // p.smem_cap: staged scores per row, a multiple of 4 and at most TH_STAGE
+        if (p.smem_cap < 0 || p.smem_cap > TH_STAGE || (p.smem_cap & 3)) return static_cast<int>(cudaErrorInvalidValue);
+        static size_t done[64] = {};
+        const size_t smem = static_cast<size_t>(TH_WARPS) * (TH_BINS + p.smem_cap) * 4;
+        if (int rc = set_smem(thresh_kernel, smem, done)) return rc;
+        thresh_kernel<<<(p.R + TH_WARPS - 1) / TH_WARPS, TH_WARPS * 32, smem, st>>>(p);
+        return static_cast<int>(cudaGetLastError());
+    }
+    if (p.mode == SEL_CAND) {
+        static size_t done[64] = {};
+        const size_t smem = sizeof(CandShared) + (static_cast<size_t>(p.cap) + p.k + SLACK) * 8;
+        if (int rc = set_smem(cand_kernel, smem, done)) return rc;
+        cand_kernel<<<p.R, CT, smem, st>>>(p);
+        return static_cast<int>(cudaGetLastError());
+    }
+    static size_t done[64] = {};
+    const size_t smem = sizeof(SelShared) + static_cast<size_t>(out_capacity(p)) * 8 +
+                        static_cast<size_t>(p.smem_cap) * 8;
+    if (int rc = set_smem(select_kernel, smem, done)) return rc;
+    select_kernel<<<grid, NT, smem, st>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 

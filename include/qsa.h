@@ -116,7 +116,6 @@ const char *qsa_status_string(qsa_status status);
 #define QSA_CFG_PATH 1
 #define QSA_CFG_WAIT_LIMIT_NS 2
 #define QSA_CFG_KERNEL_TIMING 3   /* 1: bracket every launch with CUDA events on its stream */
-#define QSA_CFG_SCORER 4          /* 0 automatic, 1 key positions on TMEM lanes, 2 query rows on TMEM lanes (H <= 4) */
 qsa_status qsa_set_config(int32_t key, int64_t value);
 
 /* Kernel kinds reported by qsa_kernel_times(). */

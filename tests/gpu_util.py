@@ -23,30 +23,24 @@ def to_device(wl, dev="cuda"):
     return d
 
 
-def gpu_select(wl, d=None, k=None, path=qsa.PATH_AUTO, scorer=qsa.SCORER_AUTO):
+def gpu_select(wl, d=None, k=None, path=qsa.PATH_AUTO):
     d = d or to_device(wl)
     qsa.set_config(qsa.QSA_CFG_PATH, path)
-    qsa.set_config(qsa.QSA_CFG_SCORER, scorer)
     try:
         idx, val = qsa.select_paged_tokens(d["q"], d["w"], d["keys"], d["row_req"],
                                            d["row_visible"], wl.k if k is None else k)
     finally:
         qsa.set_config(qsa.QSA_CFG_PATH, qsa.PATH_AUTO)
-        qsa.set_config(qsa.QSA_CFG_SCORER, qsa.SCORER_AUTO)
     st = qsa.get_device_status()
     assert st == qsa.QSA_OK, qsa.status_string(st)
     return idx.cpu().numpy(), val.cpu().numpy()
 
 
-def gpu_logits(wl, d=None, ld=None, scorer=qsa.SCORER_AUTO):
+def gpu_logits(wl, d=None, ld=None):
     d = d or to_device(wl)
     ld = wl.ld if ld is None else ld
     lg = torch.empty((wl.rows, ld), dtype=torch.float32, device="cuda")
-    qsa.set_config(qsa.QSA_CFG_SCORER, scorer)
-    try:
-        qsa.index_score(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"], lg)
-    finally:
-        qsa.set_config(qsa.QSA_CFG_SCORER, qsa.SCORER_AUTO)
+    qsa.index_score(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"], lg)
     st = qsa.get_device_status()
     assert st == qsa.QSA_OK, qsa.status_string(st)
     return lg.cpu().numpy()

@@ -41,25 +41,23 @@ def _oracle_rows(wl, rows, ld=None):
 
 # ------------------------------------------------------------ tiny, exact ----
 
-@pytest.mark.parametrize("scorer", [qsa.SCORER_POSITIONS, qsa.SCORER_ROWS])
 @pytest.mark.parametrize("path", [qsa.PATH_DENSE, qsa.PATH_FILTER])
-def test_tiny_config_bit_exact(path, scorer):
+def test_tiny_config_bit_exact(path):
     wl = W.tiny()
     oi, ov, ol = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
                                             wl.row_visible, wl.k, ld=wl.ld)
-    gi, gv = gpu_select(wl, path=path, scorer=scorer)
+    gi, gv = gpu_select(wl, path=path)
     np.testing.assert_array_equal(gi, oi)
     np.testing.assert_array_equal(gv, ov)
 
 
-@pytest.mark.parametrize("scorer", [qsa.SCORER_POSITIONS, qsa.SCORER_ROWS])
-def test_tiny_config_logits_bit_exact(scorer):
+def test_tiny_config_logits_bit_exact():
     wl = W.tiny()
     ol = oracle.score(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req, wl.row_visible, wl.ld)
-    np.testing.assert_array_equal(gpu_logits(wl, scorer=scorer), ol)
+    np.testing.assert_array_equal(gpu_logits(wl), ol)
     # a wider logit row than the cache: the tail is -inf
     ol2 = oracle.score(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req, wl.row_visible, 300)
-    np.testing.assert_array_equal(gpu_logits(wl, ld=300, scorer=scorer), ol2)
+    np.testing.assert_array_equal(gpu_logits(wl, ld=300), ol2)
 
 
 # ------------------------------------------------- ragged, multi-request ----
@@ -79,16 +77,15 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
-@pytest.mark.parametrize("scorer", [qsa.SCORER_POSITIONS, qsa.SCORER_ROWS])
 @pytest.mark.parametrize("path", [qsa.PATH_DENSE, qsa.PATH_FILTER])
-def test_ragged_cases_against_oracle(case, path, scorer):
+def test_ragged_cases_against_oracle(case, path):
     ctx, rows, k, dist, H, P = case
     wl = W.make_workload("ragged", seed=hash((tuple(ctx), k, H, P)) % 1000, ctx_tokens=ctx,
                          rows_per_req=rows, k=k, dist=dist, heads=H, page_positions=P)
     d = to_device(wl)
     ol, oi, ov = _oracle_rows(wl, np.arange(wl.rows))
-    gl = gpu_logits(wl, d, scorer=scorer)
-    gi, gv = gpu_select(wl, d, path=path, scorer=scorer)
+    gl = gpu_logits(wl, d)
+    gi, gv = gpu_select(wl, d, path=path)
     check_sorted_valid(gi, gv, wl.row_visible, k)
     if dist == "int4":
         np.testing.assert_array_equal(gl, ol)
@@ -244,10 +241,9 @@ def test_full_size_config(name):
         print(f"{name}: disagreement rate {rate:.2e}, identical rows {same:.3f}")
     if name == "bench":
         # both paths select exactly the same positions on the same logits
-        for scorer in (qsa.SCORER_POSITIONS, qsa.SCORER_ROWS):
-            gi2, gv2 = gpu_select(wl, d, path=qsa.PATH_DENSE, scorer=scorer)
-            gi3, gv3 = gpu_select(wl, d, path=qsa.PATH_FILTER, scorer=scorer)
-            np.testing.assert_array_equal(gi2, gi3)
-            np.testing.assert_array_equal(gv2, gv3)
-            rate, same = near_tie_disagreement(gi2[rows], oi, ol, wl.row_visible[rows], wl.k)
-            print(f"{name} scorer {scorer}: disagreement rate {rate:.2e}, identical rows {same:.3f}")
+        gi2, gv2 = gpu_select(wl, d, path=qsa.PATH_DENSE)
+        gi3, gv3 = gpu_select(wl, d, path=qsa.PATH_FILTER)
+        np.testing.assert_array_equal(gi2, gi3)
+        np.testing.assert_array_equal(gv2, gv3)
+        rate, same = near_tie_disagreement(gi2[rows], oi, ol, wl.row_visible[rows], wl.k)
+        print(f"{name} dense path: disagreement rate {rate:.2e}, identical rows {same:.3f}")
