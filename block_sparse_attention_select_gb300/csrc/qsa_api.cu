@@ -141,17 +141,19 @@ FilterShape filter_shape(int64_t max_len, int32_t k)
     return f;
 }
 
+// Key tiles per row in the candidate arrays: a multiple of 8, so that every
+// row's mask words fill whole 128-byte lines.
+int64_t cand_tiles_ld(int64_t ld) { return ((ld + TILE_M - 1) / TILE_M + 7) / 8 * 8; }
+
 bool use_filter(int64_t max_len, int32_t k)
 {
+    // the filter scorer addresses a group's candidate slots with 32-bit offsets
+    if (cand_tiles_ld(max_len) * 4 * CAND_MAIN * 64 >= (int64_t{1} << 32)) return false;
     if (g_cfg_path == 1) return false;
     if (g_cfg_path == 2) return true;
     const FilterShape f = filter_shape(max_len, k);
     return f.stride >= 4 && max_len >= 8LL * k;
 }
-
-// Key tiles per row in the candidate arrays: a multiple of 8, so that every
-// row's mask words fill whole 128-byte lines.
-int64_t cand_tiles_ld(int64_t ld) { return ((ld + TILE_M - 1) / TILE_M + 7) / 8 * 8; }
 
 struct Layout {
     size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_mask, cand_score, cand_over;

@@ -144,6 +144,9 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
     // is tiles_ld * 4 quarters further
     const int64_t e0 = (r0 * p.tiles_ld + tile) * 4 + quarter;
     const int64_t q_stride = static_cast<int64_t>(p.tiles_ld) * 4;
+    // score slots from one row to the next, as a 32-bit offset: the host uses
+    // the filter path only while 64 rows of slots span less than 2^32 floats
+    const uint32_t slot_row = static_cast<uint32_t>(q_stride * CAND_MAIN);
     float *score0 = nullptr;
     uint32_t *mask0 = nullptr;
     float *out0 = nullptr;
@@ -173,6 +176,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                 load_w<H>(e.w, c0 + b0 + i, wv);
                 s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
             }
+            int cmax = 0;                                     // FILTER: largest count of the block
 #pragma unroll
             for (int i = 0; i < B; ++i) {
                 const int32_t el = c0 + b0 + i;
@@ -188,17 +192,30 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                     const int c = __popc(m);
                     const int rk = __popc(m & lt_mask);
                     const int slot = take ? rk : c + lane - rk;
-                    if (live && slot < CAND_MAIN) score0[el * q_stride * CAND_MAIN + slot] = s[i];
-                    if (c > CAND_MAIN) {                          // warp-uniform, rare
-                        if (take && rk >= CAND_MAIN)
-                            p.cand_over[(e0 + el * q_stride) * CAND_OVER + rk - CAND_MAIN] = s[i];
-                    }
+                    if (live && slot < CAND_MAIN) score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(slot)] = s[i];
+                    cmax = max(cmax, c);
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
                 } else {
                     float *dst = out0 + el * p.ld;
                     if (ok) *dst = s[i];
                     else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
+                }
+            }
+            if constexpr (MODE == SCORE_FILTER) {
+                // candidates 8.. of a quarter (rare): kept out of the per-row
+                // code above, whose rows then schedule as one straight block
+                if (cmax > CAND_MAIN) {                           // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < B; ++i) {
+                        const int32_t el = c0 + b0 + i;
+                        const bool ok = (ALLROWS || el < nmine) && (FULL || j < e.vis[el]);
+                        const bool take = ok && s[i] >= e.tau[el];
+                        const uint32_t m = __ballot_sync(0xffffffffu, take);
+                        const int rk = __popc(m & lt_mask);
+                        if (take && rk >= CAND_MAIN)
+                            p.cand_over[(e0 + el * q_stride) * CAND_OVER + rk - CAND_MAIN] = s[i];
+                    }
                 }
             }
         }

@@ -841,47 +841,116 @@ cand_kernel(const SelectParams p)
 // it, m = oversample * k * n_s / V_r (+8), the expected share of the top k in
 // the sample.  tau only has to be low enough; the candidate count it yields
 // is checked by the candidate selector, so the search stops as soon as the
-// bin holding the m-th sampled key is small.  One warp per row: the sample is
-// a few thousand scores, too little work for a block and its barriers.  The
-// row is copied to shared memory with every copy in flight at once (rows
-// longer than the staging area are read from global memory instead).
-constexpr int TH_WARPS = 4;
+// bin holding the m-th sampled key is small.  One CTA of TH_THREADS per row:
+// the row's keys are staged in shared memory (rows longer than the staging
+// area are read from global memory in every pass instead).
+constexpr int TH_THREADS = 128;
 constexpr int TH_BINS = 256;
 constexpr int TH_STAGE = 4096;        // sampled scores of one row held in shared memory
 
-__device__ __forceinline__ uint32_t warp_min(uint32_t v)
+struct ThShared {
+    uint32_t hist[TH_BINS];
+    uint32_t red[4][TH_THREADS / 32];
+    uint32_t cut_d, cut_above, cut_eq, pad_;
+};
+
+// Block-wide min, max, min and sum of four per-thread values (one barrier).
+__device__ __forceinline__ void th_reduce(ThShared &sh, uint32_t &a_min, uint32_t &b_max, uint32_t &c_min,
+                                          uint32_t &d_sum)
 {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    for (int o = 16; o > 0; o >>= 1) {
+        a_min = min(a_min, __shfl_xor_sync(0xffffffffu, a_min, o));
+        b_max = max(b_max, __shfl_xor_sync(0xffffffffu, b_max, o));
+        c_min = min(c_min, __shfl_xor_sync(0xffffffffu, c_min, o));
+        d_sum += __shfl_xor_sync(0xffffffffu, d_sum, o);
+    }
+    if (lane == 0) { sh.red[0][wid] = a_min; sh.red[1][wid] = b_max; sh.red[2][wid] = c_min; sh.red[3][wid] = d_sum; }
+    __syncthreads();
+    a_min = sh.red[0][0]; b_max = sh.red[1][0]; c_min = sh.red[2][0]; d_sum = sh.red[3][0];
+#pragma unroll
+    for (int w = 1; w < TH_THREADS / 32; ++w) {
+        a_min = min(a_min, sh.red[0][w]);
+        b_max = max(b_max, sh.red[1][w]);
+        c_min = min(c_min, sh.red[2][w]);
+        d_sum += sh.red[3][w];
+    }
 }
 
-__device__ __forceinline__ uint32_t warp_max(uint32_t v)
+// The key that about m of the n_s keys key_at(i) reach, searched in [lo, hi]
+// (every key counted lies there).
+template <typename KeyAt>
+__device__ uint32_t thresh_search(ThShared &sh, KeyAt key_at, int32_t n_s, uint32_t m, uint32_t lo,
+                                  uint32_t hi)
 {
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const uint32_t stop = max(8u, m / 16);
+    uint32_t k_left = m;
+    while (lo != hi) {
+        const uint32_t span = hi - lo;
+        const int bits = 32 - __clz(span);
+        const int shift = bits > 8 ? bits - 8 : 0;            // (hi - lo) >> shift < TH_BINS
+        for (int b = t; b < TH_BINS; b += TH_THREADS) sh.hist[b] = 0;
+        __syncthreads();
+        for (int32_t i = t; i < n_s; i += TH_THREADS) {
+            const uint32_t kv = key_at(i);
+            if (kv >= lo && kv <= hi) atomicAdd(&sh.hist[(kv - lo) >> shift], 1u);
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // lane l holds bins 255-8l down to 248-8l: lanes in descending key order
+            uint32_t c[8], s = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+            for (int j = 0; j < 8; ++j) {
+                c[j] = sh.hist[TH_BINS - 1 - 8 * lane - j];
+                s += c[j];
+            }
+            uint32_t incl = s;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            uint32_t above = incl - s;
+            if (above < k_left && k_left <= incl) {
+                // exactly one lane: k_left lies in one of its bins
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (k_left <= above + c[j]) {
+                        sh.cut_d = static_cast<uint32_t>(TH_BINS - 1 - 8 * lane - j);
+                        sh.cut_above = above;
+                        sh.cut_eq = c[j];
+                        break;
+                    }
+                    above += c[j];
+                }
+            }
+        }
+        __syncthreads();
+        const uint32_t d = sh.cut_d, eq = sh.cut_eq;
+        k_left -= sh.cut_above;
+        const uint32_t nlo = lo + (d << shift);
+        const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
+        hi = static_cast<uint32_t>(min(static_cast<uint64_t>(hi), nhi));
+        lo = nlo;
+        if (eq <= stop) break;                                // uniform
+    }
+    return lo;
 }
 
-__device__ __forceinline__ uint32_t warp_sum(uint32_t v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__global__ void __launch_bounds__(TH_WARPS * 32)
+__global__ void __launch_bounds__(TH_THREADS)
 thresh_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int32_t r = blockIdx.x * TH_WARPS + wid;
-    if (r >= p.R) return;                       // whole warps leave; only warp-level sync below
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem_raw) + wid * TH_BINS;
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw) + TH_WARPS * TH_BINS + wid * p.smem_cap;
+    ThShared &sh = *reinterpret_cast<ThShared *>(smem_raw);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw + sizeof(ThShared));
+    const int t = threadIdx.x;
+    const int32_t r = blockIdx.x;
+    if (r >= p.R) return;
     int32_t V = p.row_vis[r];
     if (V < 0 || V > p.max_len) {
-        if (lane == 0) record_error(p.status, ST_BAD_ROW);
+        if (t == 0) record_error(p.status, ST_BAD_ROW);
         V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
     }
     // sampled tiles 0, s, 2s, ... of the row, the last one possibly partial
@@ -892,98 +961,42 @@ thresh_kernel(const SelectParams p)
         n_s = (t_last / p.sample_stride) * TILE_M + min(TILE_M, V - t_last * TILE_M);
     }
     float tau = -__int_as_float(0x7f800000);
-    if (V > p.cap && n_s > 0) {
-        const double want = static_cast<double>(p.oversample) * p.k * n_s / V;
-        const uint32_t m = static_cast<uint32_t>(max(1, min(static_cast<int32_t>(ceil(want)) + 8, n_s)));
+    if (V > p.cap && n_s > 0) {                               // uniform
+        // (single precision: this is a sizing heuristic, and FP64 is slow here)
+        const float want = p.oversample * static_cast<float>(p.k) * static_cast<float>(n_s) / static_cast<float>(V);
+        const uint32_t m = static_cast<uint32_t>(max(1, min(static_cast<int32_t>(ceilf(want)) + 8, n_s)));
         const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
         const bool staged = n_s <= p.smem_cap;
-        if (staged) {
-            const int32_t nv = n_s >> 2;                       // row start is 16-byte aligned
-            for (int32_t v = lane; v < nv; v += 32)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             ::"r"(smem_u32(stage + 4 * v)), "l"(row + 4 * v) : "memory");
-            for (int32_t i = 4 * nv + lane; i < n_s; i += 32) stage[i] = __float_as_uint(__ldcg(row + i));
-            asm volatile("cp.async.wait_all;" ::: "memory");
-            __syncwarp();
-            for (int32_t i = lane; i < n_s; i += 32) stage[i] = score_key(__uint_as_float(stage[i]));
-            __syncwarp();
-        }
-        auto key_at = [&](int32_t i) { return staged ? stage[i] : score_key(__ldcg(row + i)); };
-        // key range of the sample, and of its scores above zero: when at
-        // least m are positive the spike of exact zeros (every head clipped)
-        // lies below the cut and is left out of the range
+        // one pass: keys, their range, and the range of the keys above zero;
+        // when at least m are positive the spike of exact zeros (every head
+        // clipped) lies below the cut and is left out of the range
         const uint32_t zk = score_key(0.0f);
         uint32_t lo = 0xffffffffu, hi = 0u, lo_pos = 0xffffffffu, npos = 0;
-        for (int32_t i = lane; i < n_s; i += 32) {
-            const uint32_t kv = key_at(i);
+        auto take_key = [&](uint32_t kv) {
             lo = min(lo, kv);
             hi = max(hi, kv);
             if (kv > zk) { lo_pos = min(lo_pos, kv); ++npos; }
+        };
+        const int32_t nv = n_s >> 2;                          // row start is 16-byte aligned
+        for (int32_t v = t; v < nv; v += TH_THREADS) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(row) + v);
+            const uint4 kq = make_uint4(score_key(x.x), score_key(x.y), score_key(x.z), score_key(x.w));
+            take_key(kq.x); take_key(kq.y); take_key(kq.z); take_key(kq.w);
+            if (staged) reinterpret_cast<uint4 *>(stage)[v] = kq;
         }
-        lo = warp_min(lo);
-        hi = warp_max(hi);
-        lo_pos = warp_min(lo_pos);
-        npos = warp_sum(npos);
+        for (int32_t i = 4 * nv + t; i < n_s; i += TH_THREADS) {
+            const uint32_t kv = score_key(__ldcg(row + i));
+            take_key(kv);
+            if (staged) stage[i] = kv;
+        }
+        th_reduce(sh, lo, hi, lo_pos, npos);                  // its barrier also publishes stage[]
         if (npos >= m) lo = lo_pos;
-        const uint32_t stop = max(8u, m / 16);
-        uint32_t k_left = m;
-        while (lo != hi) {
-            const uint32_t span = hi - lo;
-            const int bits = 32 - __clz(span);
-            const int shift = bits > 8 ? bits - 8 : 0;        // (hi - lo) >> shift < TH_BINS
-#pragma unroll
-            for (int b = 0; b < TH_BINS / 32; ++b) hist[lane + 32 * b] = 0;
-            __syncwarp();
-            for (int32_t i = lane; i < n_s; i += 32) {
-                const uint32_t kv = key_at(i);
-                if (kv >= lo && kv <= hi) atomicAdd(&hist[(kv - lo) >> shift], 1u);
-            }
-            __syncwarp();
-            // lane l holds bins 255-8l down to 248-8l: lanes in descending key order
-            uint32_t c[8], s = 0;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                c[j] = hist[TH_BINS - 1 - 8 * lane - j];
-                s += c[j];
-            }
-            uint32_t incl = s;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const uint32_t excl = incl - s;
-            const uint32_t hit = __ballot_sync(0xffffffffu, excl < k_left && k_left <= incl);
-            if (hit == 0u) break;                              // cannot happen: k_left <= keys in range
-            const int src = __ffs(hit) - 1;
-            uint32_t d = 0, above = excl, eq = 0;
-            if (lane == src) {
-                bool found = false;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (!found && k_left <= above + c[j]) {
-                        found = true;
-                        d = static_cast<uint32_t>(TH_BINS - 1 - 8 * lane - j);
-                        eq = c[j];
-                    } else if (!found) {
-                        above += c[j];
-                    }
-                }
-            }
-            d = __shfl_sync(0xffffffffu, d, src);
-            above = __shfl_sync(0xffffffffu, above, src);
-            eq = __shfl_sync(0xffffffffu, eq, src);
-            k_left -= above;
-            const uint32_t nlo = lo + (d << shift);
-            const uint64_t nhi = static_cast<uint64_t>(nlo) + ((1ull << shift) - 1);
-            hi = static_cast<uint32_t>(min(static_cast<uint64_t>(hi), nhi));
-            lo = nlo;
-            __syncwarp();
-            if (eq <= stop) break;
-        }
-        tau = key_score(lo);
+        const uint32_t T = staged
+            ? thresh_search(sh, [&](int32_t i) { return stage[i]; }, n_s, m, lo, hi)
+            : thresh_search(sh, [&](int32_t i) { return score_key(__ldcg(row + i)); }, n_s, m, lo, hi);
+        tau = key_score(T);
     }
-    if (lane == 0) p.tau[r] = tau;
+    if (t == 0) p.tau[r] = tau;
 }
 
 }  // namespace
@@ -1020,9 +1033,9 @@ int launch_select(const SelectParams &p, int grid, void *stream)
         // p.smem_cap: staged scores per row, a multiple of 4 and at most TH_STAGE
         if (p.smem_cap < 0 || p.smem_cap > TH_STAGE || (p.smem_cap & 3)) return static_cast<int>(cudaErrorInvalidValue);
         static size_t done[64] = {};
-        const size_t smem = static_cast<size_t>(TH_WARPS) * (TH_BINS + p.smem_cap) * 4;
+        const size_t smem = sizeof(ThShared) + static_cast<size_t>(p.smem_cap) * 4;
         if (int rc = set_smem(thresh_kernel, smem, done)) return rc;
-        thresh_kernel<<<(p.R + TH_WARPS - 1) / TH_WARPS, TH_WARPS * 32, smem, st>>>(p);
+        thresh_kernel<<<p.R, TH_THREADS, smem, st>>>(p);
         return static_cast<int>(cudaGetLastError());
     }
     if (p.mode == SEL_CAND) {
