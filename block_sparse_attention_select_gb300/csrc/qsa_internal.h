@@ -22,16 +22,15 @@ constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, 
 // Candidate lists of the filter pass.  Key tile t of row r has four quarters
 // q of 32 positions (t*128 + q*32 + i, i < 32); quarter e = 4*t + q of row r:
 //   cand_mask[r*tiles_ld*4 + e], bit i: position t*128 + q*32 + i passed;
-//   the j-th passing position of the quarter (ascending i) has its score at
+//   the j-th passing position of the quarter (ascending i) has twice its
+//   score (an exact scaling) at
 //   cand_score[(r*tiles_ld*4 + e)*8 + j]              for j < 8,
 //   cand_over[(r*tiles_ld*4 + e)*24 + j - 8]          for 8 <= j < 32.
 // A row's first eight slots per quarter are one contiguous run (one 128-byte
-// line per key tile), so the selector streams them like any dense array;
-// slots 0..7 of a quarter are always written (lanes that did not pass fill
-// the unused ones), so every sector is written whole.  More than eight
-// candidates in one quarter is rare (the filter keeps a few percent of the
-// positions) and goes to the overflow array.  tiles_ld is a multiple of 8,
-// which keeps each row's mask words in lines of its own.
+// line per key tile), so the selector streams them like any dense array.
+// More than eight candidates in one quarter is rare (the filter keeps a few
+// percent of the positions) and goes to the overflow array.  tiles_ld is a
+// multiple of 8, which keeps each row's mask words in lines of its own.
 constexpr int CAND_MAIN = 8;     // score slots per quarter in cand_score
 constexpr int CAND_OVER = 24;    // further slots per quarter in cand_over
 

@@ -109,6 +109,25 @@ __device__ __forceinline__ float weighted_relu_sum(const float *w, const uint32_
     }
 }
 
+// 2 * sum_h w[h] * max(acc[h], 0), the filter pass's form: d + |d| is
+// exactly 2 * max(d, 0) (+0 for d <= 0) and is an add on the FMA pipe rather
+// than a max on the integer pipe; scaling by 2 commutes with every rounding
+// (short of overflow or subnormal results), so the value is exactly twice
+// weighted_relu_sum's.
+template <int H>
+__device__ __forceinline__ float weighted_relu_sum2(const float *w, const uint32_t *acc)
+{
+    auto t = [&](int h) { const float d = __uint_as_float(acc[h]); return d + fabsf(d); };
+    if constexpr (H == 1) {
+        return fmaf(w[0], t(0), 0.0f);
+    } else {
+        float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int h = 0; h < H; h += 2) s = ffma2(make_float2(w[h], w[h + 1]), make_float2(t(h), t(h + 1)), s);
+        return s.x + s.y;
+    }
+}
+
 template <int H>
 __device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
 {
@@ -147,6 +166,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
     // score slots from one row to the next, as a 32-bit offset: the host uses
     // the filter path only while 64 rows of slots span less than 2^32 floats
     const uint32_t slot_row = static_cast<uint32_t>(q_stride * CAND_MAIN);
+    const uint32_t mask_row = static_cast<uint32_t>(q_stride);
     float *score0 = nullptr;
     uint32_t *mask0 = nullptr;
     float *out0 = nullptr;
@@ -174,26 +194,25 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
             for (int i = 0; i < B; ++i) {
                 float wv[H];
                 load_w<H>(e.w, c0 + b0 + i, wv);
-                s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
+                if constexpr (MODE == SCORE_FILTER) s[i] = weighted_relu_sum2<H>(wv, v + (b0 + i) * H);
+                else s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
             }
-            int cmax = 0;                                     // FILTER: largest count of the block
+            int rkmax = 0;                                    // FILTER: >= CAND_MAIN when a quarter may overflow
 #pragma unroll
             for (int i = 0; i < B; ++i) {
                 const int32_t el = c0 + b0 + i;
                 const bool live = ALLROWS || el < nmine;      // warp-uniform
                 const bool ok = live && (FULL || j < e.vis[el]);
                 if constexpr (MODE == SCORE_FILTER) {
+                    // s and tau are both doubled here; the stored slot value
+                    // is 2 * score (halved exactly by the selector)
                     const bool take = ok && s[i] >= e.tau[el];
                     const uint32_t m = __ballot_sync(0xffffffffu, take);
                     if (lane == b0 + i) my_mask = m;
-                    // a passing lane takes slot (passing lanes below it); the
-                    // others fill slots popc(m), popc(m)+1, ... so that slots
-                    // 0..7 are all written (their contents are never read)
-                    const int c = __popc(m);
+                    // a passing lane's slot: the passing lanes below it
                     const int rk = __popc(m & lt_mask);
-                    const int slot = take ? rk : c + lane - rk;
-                    if (live && slot < CAND_MAIN) score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(slot)] = s[i];
-                    cmax = max(cmax, c);
+                    if (take && rk < CAND_MAIN) score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(rk)] = s[i];
+                    rkmax = max(rkmax, rk);
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
                 } else {
@@ -205,7 +224,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
             if constexpr (MODE == SCORE_FILTER) {
                 // candidates 8.. of a quarter (rare): kept out of the per-row
                 // code above, whose rows then schedule as one straight block
-                if (cmax > CAND_MAIN) {                           // warp-uniform
+                if (__any_sync(0xffffffffu, rkmax >= CAND_MAIN)) {
 #pragma unroll
                     for (int i = 0; i < B; ++i) {
                         const int32_t el = c0 + b0 + i;
@@ -221,7 +240,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         }
         if constexpr (MODE == SCORE_FILTER) {
             // one store for the chunk: lane i writes the mask word of row c0 + i
-            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) mask0[(c0 + lane) * q_stride] = my_mask;
+            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) mask0[static_cast<uint32_t>(c0 + lane) * mask_row] = my_mask;
         }
     }
 }
@@ -458,7 +477,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 for (int32_t i = lane; i < nmine; i += 32) {
                     const int32_t r = gr.row0 + first + i;
                     er.vis[i] = __ldg(p.row_vis + r);
-                    er.tau[i] = p.mode == SCORE_FILTER ? __ldg(p.tau + r) : 0.0f;
+                    er.tau[i] = p.mode == SCORE_FILTER ? 2.0f * __ldg(p.tau + r) : 0.0f;   // see weighted_relu_sum2
                 }
                 __syncwarp();
             }

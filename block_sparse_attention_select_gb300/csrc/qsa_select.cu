@@ -588,7 +588,7 @@ select_kernel(const SelectParams p)
 // candidates, more than cap, or a cut bucket too large to order here) is
 // flagged and left to the fallback launch.
 constexpr int CT = 256;               // threads per row
-constexpr int QPT = 12;               // half quarters per thread and gather round
+constexpr int QPT = 8;                // half quarters per thread and gather round
 constexpr int BIG_MAX = 320;          // > (QSA_MAX_K + SLACK) / (RANK_MAX + 1)
 
 struct CandShared {
@@ -700,41 +700,57 @@ cand_kernel(const SelectParams p)
         const uint32_t base = cand_scan(cnt, sh.wtot[sbuf], ctot);
         sbuf ^= 1;
         if (done + ctot > static_cast<uint32_t>(p.cap)) { overflow = true; break; }   // uniform
-        uint32_t o = done + base;
+        // per half quarter: candidates held in registers (up to 4) and, for
+        // odd threads, overflow ones; their offsets in this thread's run
+        uint32_t off[QPT], nreg[QPT];
+        uint32_t run = done + base;
 #pragma unroll
         for (int u = 0; u < QPT; ++u) {
-            uint32_t mm = m[u];
+            const uint32_t c = __popc(m[u]);
+            nreg[u] = par ? min(c > 4u ? c - 4u : 0u, 4u) : min(c, 4u);
+            off[u] = run;
+            run += par ? (c > 4u ? c - 4u : 0u) : nreg[u];
             if (par) {
 #pragma unroll
-                for (int z = 0; z < 4; ++z) mm &= mm - 1u;       // skip the even thread's four
+                for (int z = 0; z < 4; ++z) m[u] &= m[u] - 1u;   // skip the even thread's four
             }
-            if (mm == 0u) continue;
-            const int32_t e = (h0 + t + u * CT) >> 1;
-            const uint32_t pos0 = static_cast<uint32_t>(e) * 32u;
-            const float fv[4] = {f[u].x, f[u].y, f[u].z, f[u].w};
+        }
+        // slot jj of every half quarter at once: independent chains
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {                     // slots 4*par + jj, in registers
-                if (mm == 0u) break;
-                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
-                mm &= mm - 1u;
-                const uint32_t key = score_key(fv[jj]);
-                kmin = min(kmin, key);
-                kmax = max(kmax, key);
-                a[o++] = (static_cast<uint64_t>(key) << 32) | ~(pos0 + bit);
+        for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                if (static_cast<uint32_t>(jj) < nreg[u]) {
+                    const float sc = 0.5f * (jj == 0 ? f[u].x : (jj == 1 ? f[u].y : (jj == 2 ? f[u].z : f[u].w)));
+                    const uint32_t bit = static_cast<uint32_t>(__ffs(m[u]) - 1);
+                    m[u] &= m[u] - 1u;
+                    const uint32_t key = score_key(sc);
+                    kmin = min(kmin, key);
+                    kmax = max(kmax, key);
+                    const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
+                    a[off[u] + jj] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
+                }
             }
-            if (par && mm != 0u) {
+        }
+        if (par) {
+#pragma unroll
+            for (int u = 0; u < QPT; ++u) {
+                uint32_t mm = m[u];
+                if (mm == 0u) continue;
                 // more than eight candidates in this quarter (rare): the
-                // overflow slots, kept out of the loop above so that its
+                // overflow slots, kept out of the loops above so that their
                 // iterations carry no global load
+                const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
                 const float *ov_q = orow + static_cast<int64_t>(e) * CAND_OVER;
+                uint32_t o = off[u] + 4u;
 #pragma unroll 1
                 for (uint32_t j = 0; mm != 0u; ++j) {
                     const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
                     mm &= mm - 1u;
-                    const uint32_t key = score_key(__ldcg(ov_q + j));
+                    const uint32_t key = score_key(0.5f * __ldcg(ov_q + j));
                     kmin = min(kmin, key);
                     kmax = max(kmax, key);
-                    a[o++] = (static_cast<uint64_t>(key) << 32) | ~(pos0 + bit);
+                    a[o++] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
                 }
             }
         }
@@ -800,20 +816,42 @@ cand_kernel(const SelectParams p)
         __syncthreads();
         // ---- rank inside the bucket = place in the output (hist[b] is now
         //      the end of bucket b, hence the start of bucket b + 1)
-        for (uint32_t pos = t; pos < need; pos += CT) {
-            const uint64_t x = bq[pos];
-            const uint32_t key = static_cast<uint32_t>(x >> 32);
-            const uint32_t b = NBINS - 1 - ((key - kmin) >> shift);
-            const uint32_t s0 = b ? sh.hist[b - 1] : 0u, e = sh.hist[b];
-            if (e - s0 > RANK_MAX) {
-                if (pos == s0) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
-                continue;
+        // two positions per iteration: two independent chains
+        for (uint32_t p0 = t; p0 < need; p0 += 2 * CT) {
+            uint64_t x[2];
+            uint32_t s0[2], m[2], rk[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t pos = p0 + h * CT;
+                m[h] = 0u;
+                s0[h] = 0xffffffffu;                              // no output unless ranked below
+                x[h] = 0ull;
+                if (pos < need) {
+                    x[h] = bq[pos];
+                    const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x[h] >> 32) - kmin) >> shift);
+                    s0[h] = b ? sh.hist[b - 1] : 0u;
+                    const uint32_t e = sh.hist[b];
+                    if (e - s0[h] > RANK_MAX) {
+                        if (pos == s0[h]) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
+                        s0[h] = 0xffffffffu;                      // ordered by the warp sort below
+                    } else {
+                        m[h] = e - s0[h];
+                    }
+                }
+                rk[h] = s0[h];
             }
-            uint32_t rk = s0;
-            for (uint32_t q = s0; q < e; ++q) rk += bq[q] > x;
-            if (rk < kk) {
-                oi[rk] = static_cast<int32_t>(~static_cast<uint32_t>(x));
-                if (ov) ov[rk] = key_score(key);
+            const uint32_t mx = max(m[0], m[1]);
+            for (uint32_t q = 0; q < mx; ++q) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (q < m[h]) rk[h] += bq[s0[h] + q] > x[h];
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (rk[h] < kk) {
+                    oi[rk[h]] = static_cast<int32_t>(~static_cast<uint32_t>(x[h]));
+                    if (ov) ov[rk[h]] = key_score(static_cast<uint32_t>(x[h] >> 32));
+                }
             }
         }
         __syncthreads();
