@@ -145,10 +145,11 @@ FilterShape filter_shape(int64_t max_len, int32_t k)
 // row's mask words fill whole 128-byte lines.
 int64_t cand_tiles_ld(int64_t ld) { return ((ld + TILE_M - 1) / TILE_M + 7) / 8 * 8; }
 
-bool use_filter(int64_t max_len, int32_t k)
+bool use_filter(int32_t rows, int64_t max_len, int32_t k)
 {
-    // the filter scorer addresses a group's candidate slots with 32-bit offsets
-    if (cand_tiles_ld(max_len) * 4 * CAND_MAIN * 64 >= (int64_t{1} << 32)) return false;
+    // the filter scorer addresses the candidate slots (4 planes) with 32-bit
+    // offsets from a group's plane-0 run
+    if (static_cast<int64_t>(rows) * cand_tiles_ld(max_len) * 4 * CAND_SLOTS >= (int64_t{1} << 32)) return false;
     if (g_cfg_path == 1) return false;
     if (g_cfg_path == 2) return true;
     const FilterShape f = filter_shape(max_len, k);
@@ -156,7 +157,7 @@ bool use_filter(int64_t max_len, int32_t k)
 }
 
 struct Layout {
-    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_mask, cand_score, cand_over;
+    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_mask, cand_score;
     size_t total;
 };
 
@@ -177,8 +178,7 @@ Layout layout(int32_t R, int64_t ld, int32_t k)
     L.flag = take(sizeof(int32_t) * R);
     const size_t tiles = static_cast<size_t>(cand_tiles_ld(ld));
     L.cand_mask = take(sizeof(uint32_t) * static_cast<size_t>(R) * tiles * 4);
-    L.cand_score = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_MAIN);
-    L.cand_over = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_OVER);
+    L.cand_score = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_SLOTS);   // 4 planes
     L.total = o;
     return L;
 }
@@ -463,7 +463,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != QSA_OK) return st;
     const int64_t ld = static_cast<int64_t>(keys->max_pages_per_req) * keys->page_positions;
-    const bool filter = use_filter(ld, k);
+    const bool filter = use_filter(rows, ld, k);
     const FilterShape f = filter_shape(ld, k);
     ScoreSetup s;
     st = setup_score(s, q, w, rows, H, keys, row_req, row_visible, ld, ld, k,
@@ -500,7 +500,6 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     float *tau = reinterpret_cast<float *>(at(s.L.tau));
     uint32_t *cand_mask = reinterpret_cast<uint32_t *>(at(s.L.cand_mask));
     float *cand_score = reinterpret_cast<float *>(at(s.L.cand_score));
-    float *cand_over = reinterpret_cast<float *>(at(s.L.cand_over));
     const int32_t tiles_ld = static_cast<int32_t>(cand_tiles_ld(ld));
 
     // 1. scores of every stride-th key tile
@@ -523,7 +522,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.mode = SCORE_FILTER;
     s.sp.tau = tau;
     s.sp.cand_score = cand_score;
-    s.sp.cand_over = cand_over;
+    s.sp.cand_plane = static_cast<uint32_t>(static_cast<int64_t>(rows) * tiles_ld * 4 * 8);
     s.sp.cand_mask = cand_mask;
     s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
@@ -533,7 +532,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
     cs.cand_score = cand_score;
-    cs.cand_over = cand_over;
+    cs.cand_plane = s.sp.cand_plane;
     cs.cand_mask = cand_mask;
     cs.tiles_ld = tiles_ld;
     cs.cap = f.cap;

@@ -24,15 +24,16 @@ constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, 
 //   cand_mask[r*tiles_ld*4 + e], bit i: position t*128 + q*32 + i passed;
 //   the j-th passing position of the quarter (ascending i) has twice its
 //   score (an exact scaling) at
-//   cand_score[(r*tiles_ld*4 + e)*8 + j]              for j < 8,
-//   cand_over[(r*tiles_ld*4 + e)*24 + j - 8]          for 8 <= j < 32.
-// A row's first eight slots per quarter are one contiguous run (one 128-byte
-// line per key tile), so the selector streams them like any dense array.
-// More than eight candidates in one quarter is rare (the filter keeps a few
-// percent of the positions) and goes to the overflow array.  tiles_ld is a
-// multiple of 8, which keeps each row's mask words in lines of its own.
-constexpr int CAND_MAIN = 8;     // score slots per quarter in cand_score
-constexpr int CAND_OVER = 24;    // further slots per quarter in cand_over
+//   cand_score[(j / 8) * plane + (r*tiles_ld*4 + e)*8 + j % 8],
+//   plane = R * tiles_ld * 4 * 8 floats.
+// Plane 0 holds every quarter's first eight slots, one contiguous run per
+// row that the selector streams like a dense array; a quarter rarely has
+// more than eight candidates (the filter keeps a few percent of the
+// positions), and those go to planes 1..3 at the same offset.  The scorer
+// addresses slot j as j + (j / 8) * (plane - 8) from the plane-0 run, one
+// store per row with no test for the rare case.  tiles_ld is a multiple of
+// 8, which keeps each row's mask words in lines of their own.
+constexpr int CAND_SLOTS = 32;   // score slots per quarter (4 planes of 8)
 
 // A group: consecutive query rows of one request that share every key tile.
 struct Group {
@@ -78,8 +79,8 @@ struct ScoreParams {
     int64_t ld;
     int32_t pad_inf;            // LOGITS: write -inf for V_r <= j < tile end (j < ld)
     const float *tau;           // FILTER: per-row threshold
-    float *cand_score;          // FILTER: [R, tiles_ld * 4, CAND_MAIN] candidate scores (layout above)
-    float *cand_over;           // FILTER: [R, tiles_ld * 4, CAND_OVER]
+    float *cand_score;          // FILTER: [4, R, tiles_ld * 4, 8] candidate scores (layout above)
+    uint32_t cand_plane;        // floats per plane of cand_score (host keeps 4 planes below 2^32)
     uint32_t *cand_mask;        // FILTER: [R, tiles_ld * 4] passing positions of each quarter
     int32_t tiles_ld;           // key tiles per row in the candidate arrays (multiple of 8)
     uint32_t *status;
@@ -102,7 +103,7 @@ struct SelectParams {
     int64_t max_len;            // largest valid V_r (longer rows are clamped and flagged)
     const int32_t *row_vis;     // V_r
     const float *cand_score;    // CAND: lists written by the filter scorer
-    const float *cand_over;
+    uint32_t cand_plane;
     const uint32_t *cand_mask;
     int32_t tiles_ld;
     int32_t cap;                // THRESH: rows up to this length keep every position; CAND: list capacity

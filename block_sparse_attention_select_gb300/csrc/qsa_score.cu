@@ -51,10 +51,14 @@ static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
 constexpr uint32_t SMEM_BYTES = SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// Walks the same (group, tile) sequence in every role of a CTA.
+// Walks the same (group, tile) sequence in every role of a CTA.  The current
+// group's item range is kept in registers: with most of the SM's unified
+// L1/shared memory taken by shared memory, a per-item reload of the prefix
+// would be an L2 round trip on every role's critical path.
 struct ItemCursor {
     const int32_t *prefix;
     int32_t g, it, it_end, stride;
+    int32_t g_first, g_next;     // items of group g: [g_first, g_next)
     __device__ void init(const int32_t *pre, int32_t n_groups, int32_t it0, int32_t it1, int32_t s)
     {
         prefix = pre;
@@ -68,13 +72,19 @@ struct ItemCursor {
             if (__ldg(prefix + mid) <= it0) lo = mid; else hi = mid - 1;
         }
         g = lo;
+        g_first = __ldg(prefix + g);
+        g_next = __ldg(prefix + g + 1);
     }
     __device__ bool valid() const { return it < it_end; }
     __device__ void settle()
     {
-        while (it >= __ldg(prefix + g + 1)) ++g;
+        while (it >= g_next) {
+            ++g;
+            g_first = g_next;
+            g_next = __ldg(prefix + g + 1);
+        }
     }
-    __device__ int32_t tile() const { return (it - __ldg(prefix + g)) * stride; }
+    __device__ int32_t tile() const { return (it - g_first) * stride; }
     __device__ void next() { ++it; }
 };
 
@@ -165,13 +175,14 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
     const int64_t q_stride = static_cast<int64_t>(p.tiles_ld) * 4;
     // score slots from one row to the next, as a 32-bit offset: the host uses
     // the filter path only while 64 rows of slots span less than 2^32 floats
-    const uint32_t slot_row = static_cast<uint32_t>(q_stride * CAND_MAIN);
+    const uint32_t slot_row = static_cast<uint32_t>(q_stride * 8);   // plane-0 floats per row
+    const uint32_t plane_step = p.cand_plane - 8u;                        // slot 8 -> plane 1, ...
     const uint32_t mask_row = static_cast<uint32_t>(q_stride);
     float *score0 = nullptr;
     uint32_t *mask0 = nullptr;
     float *out0 = nullptr;
     if constexpr (MODE == SCORE_FILTER) {
-        score0 = p.cand_score + e0 * CAND_MAIN;
+        score0 = p.cand_score + e0 * 8;
         mask0 = p.cand_mask + e0;
     } else if constexpr (MODE == SCORE_SAMPLE) {
         out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
@@ -197,7 +208,6 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                 if constexpr (MODE == SCORE_FILTER) s[i] = weighted_relu_sum2<H>(wv, v + (b0 + i) * H);
                 else s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
             }
-            int rkmax = 0;                                    // FILTER: >= CAND_MAIN when a quarter may overflow
 #pragma unroll
             for (int i = 0; i < B; ++i) {
                 const int32_t el = c0 + b0 + i;
@@ -211,30 +221,15 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                     if (lane == b0 + i) my_mask = m;
                     // a passing lane's slot: the passing lanes below it
                     const int rk = __popc(m & lt_mask);
-                    if (take && rk < CAND_MAIN) score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(rk)] = s[i];
-                    rkmax = max(rkmax, rk);
+                    if (take)
+                        score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(rk) +
+                               (static_cast<uint32_t>(rk) >> 3) * plane_step] = s[i];
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
                 } else {
                     float *dst = out0 + el * p.ld;
                     if (ok) *dst = s[i];
                     else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
-                }
-            }
-            if constexpr (MODE == SCORE_FILTER) {
-                // candidates 8.. of a quarter (rare): kept out of the per-row
-                // code above, whose rows then schedule as one straight block
-                if (__any_sync(0xffffffffu, rkmax >= CAND_MAIN)) {
-#pragma unroll
-                    for (int i = 0; i < B; ++i) {
-                        const int32_t el = c0 + b0 + i;
-                        const bool ok = (ALLROWS || el < nmine) && (FULL || j < e.vis[el]);
-                        const bool take = ok && s[i] >= e.tau[el];
-                        const uint32_t m = __ballot_sync(0xffffffffu, take);
-                        const int rk = __popc(m & lt_mask);
-                        if (take && rk >= CAND_MAIN)
-                            p.cand_over[(e0 + el * q_stride) * CAND_OVER + rk - CAND_MAIN] = s[i];
-                    }
                 }
             }
         }
@@ -325,14 +320,19 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         // The whole warp walks the items; lane i owns key box i of a tile.
         // Block-table entries are loaded PREFETCH items ahead so that the
         // page-id round trip never sits in front of a TMA issue.
-        constexpr int PREFETCH = 4;
+        constexpr int PREFETCH = 8;
         ItemCursor cur, ahead;
         cur.init(prefix, n_groups, it0, it1, stride);
         ahead = cur;
+        Group ga{};
+        int32_t ga_g = -1;                      // group held in ga (reloaded on a change only)
         auto page_id = [&](ItemCursor &a) -> int32_t {
             if (!a.valid()) return -1;
             a.settle();
-            const Group ga = p.groups[a.g];
+            if (a.g != ga_g) {
+                ga_g = a.g;
+                ga = p.groups[a.g];
+            }
             const int32_t pos0 = a.tile() * TILE_M;
             const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) / p.page_box;
             if (lane >= nbox || ga.req < 0) return -1;

@@ -666,14 +666,13 @@ cand_kernel(const SelectParams p)
     const int32_t nh = ntile * 8;                  // half quarters: 4 slots each
     const int64_t q_row = static_cast<int64_t>(r) * p.tiles_ld * 4;
     const uint32_t *mrow = p.cand_mask + q_row;
-    const float *srow = p.cand_score + q_row * CAND_MAIN;
-    const float *orow = p.cand_over + q_row * CAND_OVER;
+    const float *srow = p.cand_score + q_row * 8;          // plane 0: slots 0..7 of each quarter
     for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
     if (t == 0) sh.nbig = 0;
 
     // ---- gather.  Thread pair (2i, 2i+1) takes quarter e: the even thread
-    //      its candidates 0..3, the odd one 4..7 and any overflow; a warp's
-    //      load covers 512 contiguous bytes of the row's slots.
+    //      its candidates 0..3, the odd one 4..7 and any further ones (rare);
+    //      a warp's load covers 512 contiguous bytes of the row's plane 0.
     const uint32_t par = static_cast<uint32_t>(t & 1);
     uint32_t kmin = 0xffffffffu, kmax = 0u, done = 0;
     bool overflow = false;
@@ -737,17 +736,17 @@ cand_kernel(const SelectParams p)
             for (int u = 0; u < QPT; ++u) {
                 uint32_t mm = m[u];
                 if (mm == 0u) continue;
-                // more than eight candidates in this quarter (rare): the
-                // overflow slots, kept out of the loops above so that their
-                // iterations carry no global load
+                // more than eight candidates in this quarter (rare): slots
+                // 8.., kept out of the loops above so that their iterations
+                // carry no global load
                 const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
-                const float *ov_q = orow + static_cast<int64_t>(e) * CAND_OVER;
+                const float *ov_q = srow + static_cast<int64_t>(e) * 8;
                 uint32_t o = off[u] + 4u;
 #pragma unroll 1
                 for (uint32_t j = 0; mm != 0u; ++j) {
                     const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
                     mm &= mm - 1u;
-                    const uint32_t key = score_key(0.5f * __ldcg(ov_q + j));
+                    const uint32_t key = score_key(0.5f * __ldcg(ov_q + (j / 8 + 1) * static_cast<int64_t>(p.cand_plane) + j % 8));
                     kmin = min(kmin, key);
                     kmax = max(kmax, key);
                     a[o++] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
@@ -767,7 +766,7 @@ cand_kernel(const SelectParams p)
 #pragma unroll
     for (int w = 0; w < CT / 32; ++w) { kmin = min(kmin, sh.red_min[w]); kmax = max(kmax, sh.red_max[w]); }
     // every candidate line of the row has been read: drop it from L2 unwritten
-    for (int32_t tl = t; tl < ntile; tl += CT) discard_l2_line(srow + static_cast<int64_t>(tl) * 4 * CAND_MAIN);
+    for (int32_t tl = t; tl < ntile; tl += CT) discard_l2_line(srow + static_cast<int64_t>(tl) * 32);
     for (int32_t l = t; l < (ntile * 16 + 127) / 128; l += CT) discard_l2_line(mrow + l * 32);
 
     const uint32_t n = done;
