@@ -526,9 +526,10 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.cand_mask = cand_mask;
     s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
-    // 4. exact top-k of each candidate list; a row whose list cannot be trusted
-    //    (fewer than min(k, V) candidates, more than the selector holds, or a
-    //    tie bucket at the cut too large to order there) is flagged ...
+    // 4. exact top-k of each candidate list; a row whose list cannot be
+    //    trusted (fewer than min(k, V) candidates, more than the selector
+    //    holds, or a tie bucket at the cut too large to order there) is
+    //    re-scored in plain FP32 by its CTA and selected densely
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
     cs.cand_score = cand_score;
@@ -536,26 +537,19 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     cs.cand_mask = cand_mask;
     cs.tiles_ld = tiles_ld;
     cs.cap = f.cap;
-    if ((st = launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, stream); }))) != QSA_OK) return st;
-    // 5. ... and re-scored in full here (plain FP32) then selected densely; the
-    //    launch ends at once when no row was flagged
-    SelectParams fb = sel;
-    fb.mode = SEL_FALLBACK;
-    fb.logits = logits;
-    fb.ld = ld;
-    fb.smem_cap = std::max(8192, k);
-    fb.q = static_cast<const uint16_t *>(q);
-    fb.w = w;
-    fb.k_cache = static_cast<const uint16_t *>(keys->k_cache);
-    fb.block_table = keys->block_table;
-    fb.row_req = row_req;
-    fb.H = H;
-    fb.max_pages = keys->max_pages_per_req;
-    fb.num_pages = keys->num_pages;
-    fb.page_pos = keys->page_positions;
-    fb.fb_logits = logits;
-    const int fb_grid = std::min(rows, 2 * d->sms);
-    return launch_rc(timed(K_SEL_FLAGGED, stream, [&] { return launch_select(fb, fb_grid, stream); }));
+    cs.logits = logits;
+    cs.ld = ld;
+    cs.q = static_cast<const uint16_t *>(q);
+    cs.w = w;
+    cs.k_cache = static_cast<const uint16_t *>(keys->k_cache);
+    cs.block_table = keys->block_table;
+    cs.row_req = row_req;
+    cs.H = H;
+    cs.max_pages = keys->max_pages_per_req;
+    cs.num_pages = keys->num_pages;
+    cs.page_pos = keys->page_positions;
+    cs.fb_logits = logits;
+    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, stream); }));
 }
 
 }  // extern "C"

@@ -89,7 +89,6 @@ struct ScoreParams {
 
 enum SelectMode : int32_t {
     SEL_DENSE = 0,      // row r = logits[r, 0:V_r]
-    SEL_FALLBACK = 1,   // flagged rows only: re-scored in full, then selected as dense rows
     SEL_THRESH = 2,     // row r = sample row; writes tau_r
     SEL_CAND = 3,       // row r = candidate list; flags the row when it cannot be trusted
 };
@@ -107,10 +106,10 @@ struct SelectParams {
     const uint32_t *cand_mask;
     int32_t tiles_ld;
     int32_t cap;                // THRESH: rows up to this length keep every position; CAND: list capacity
-    int32_t *row_flag;          // CAND: 1 for rows left to the fallback launch, else 0
+    int32_t *row_flag;          // CAND: 1 for rows that took the in-kernel fallback, else 0
     Plan *plan;
-    // FALLBACK: a flagged row is re-scored (plain FP32 arithmetic) into
-    // fb_logits[r * max_len ...] and selected densely
+    // CAND fallback: a row whose list cannot be trusted is re-scored (plain
+    // FP32 arithmetic) into fb_logits[r * max_len ...] and selected densely
     const uint16_t *q;          // FP16 bits [R, H, 128]
     const float *w;             // [R, H]
     const uint16_t *k_cache;    // FP16 bits [num_pages, page_pos, 128]

@@ -11,6 +11,8 @@ namespace qsa {
 namespace {
 
 constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_SMEM_ROWS = 4096;    // rows whose sanitised V stays in shared memory
+constexpr int PLAN_SMEM_GROUPS = 1024;  // groups whose first row / length bound stay there
 
 template <typename Op>
 __device__ int32_t block_incl_scan(int32_t v, int32_t *wbuf, Op op, int32_t ident)
@@ -52,6 +54,9 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
 {
     __shared__ int32_t wbuf[32];
     __shared__ int32_t s_req[PLAN_THREADS];
+    __shared__ int32_t s_vis[PLAN_SMEM_ROWS];     // row_vis of rows < PLAN_SMEM_ROWS
+    __shared__ int32_t s_row0[PLAN_SMEM_GROUPS];  // first row of groups < PLAN_SMEM_GROUPS
+    __shared__ int32_t s_vmax[PLAN_SMEM_GROUPS];
     __shared__ int32_t carry_req, carry_run, carry_gid, carry_items, carry_samples;
     const int tid = threadIdx.x;
     if (tid == 0) { carry_req = -2; carry_run = 0; carry_gid = 0; }
@@ -70,6 +75,7 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
             if (v > max_len) { v = max_len; bad = true; }
             if (bad) record_error(status, ST_BAD_ROW);
             row_vis[r] = static_cast<int32_t>(v);
+            if (r < PLAN_SMEM_ROWS) s_vis[r] = static_cast<int32_t>(v);
             req = b;
         }
         s_req[tid] = req;
@@ -84,6 +90,7 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
         if (gbegin) {
             groups[gid].row0 = r;
             groups[gid].req = req;
+            if (gid < PLAN_SMEM_GROUPS) s_row0[gid] = r;
         }
         __syncthreads();
         if (tid == min(PLAN_THREADS - 1, R - 1 - base)) {
@@ -100,11 +107,11 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     {
         const int wid = tid >> 5, lane = tid & 31;
         for (int32_t g = wid; g < n_groups; g += PLAN_THREADS / 32) {
-            const int32_t r0 = groups[g].row0;
-            const int32_t r1 = g + 1 < n_groups ? groups[g + 1].row0 : R;
+            const int32_t r0 = g < PLAN_SMEM_GROUPS ? s_row0[g] : groups[g].row0;
+            const int32_t r1 = g + 1 < n_groups ? (g + 1 < PLAN_SMEM_GROUPS ? s_row0[g + 1] : groups[g + 1].row0) : R;
             int32_t vmax = 0, vmin = INT32_MAX;
             for (int32_t r = r0 + lane; r < r1; r += 32) {
-                const int32_t v = row_vis[r];
+                const int32_t v = r < PLAN_SMEM_ROWS ? s_vis[r] : row_vis[r];
                 vmax = max(vmax, v);
                 vmin = min(vmin, v);
             }
@@ -117,6 +124,7 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
                 groups[g].nrows = r1 - r0;
                 groups[g].vmax = vmax;
                 groups[g].vmin = vmin;
+                if (g < PLAN_SMEM_GROUPS) s_vmax[g] = vmax;
             }
         }
     }
@@ -129,7 +137,7 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
         const int32_t g = base + tid;
         int32_t tiles = 0, stiles = 0;
         if (g < n_groups) {
-            tiles = (groups[g].vmax + TILE_M - 1) / TILE_M;
+            tiles = ((g < PLAN_SMEM_GROUPS ? s_vmax[g] : groups[g].vmax) + TILE_M - 1) / TILE_M;
             stiles = (tiles + sample_stride - 1) / sample_stride;
         }
         const int32_t it = block_incl_scan(tiles, wbuf, OpAdd(), 0);

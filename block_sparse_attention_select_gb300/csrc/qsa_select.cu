@@ -521,10 +521,62 @@ __device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, floa
 // the k-th element.
 __host__ __device__ __forceinline__ int32_t out_capacity(const SelectParams &p) { return p.k + SLACK; }
 
-// Dense rows (logits in HBM), or, in fallback mode, the rows the candidate
-// selector flagged: those are re-scored here first.  Rows r = blockIdx.x,
-// blockIdx.x + gridDim.x, ...
-__global__ void __launch_bounds__(NT, 4)
+// One row of the dense selection: logits[r, 0:V_r] from HBM or, with
+// `rescore`, the row re-scored here first (plain FP32) into fb_logits.
+// Shared memory: sh, then out64[k + SLACK], keys[smem_cap], inv[smem_cap].
+__device__ __forceinline__ void select_row(const SelectParams &p, int32_t r, bool rescore, SelShared &sh,
+                           uint64_t *out64, uint32_t *keys, uint32_t *inv, int32_t smem_cap)
+{
+    int32_t V = p.row_vis[r];
+    if (V < 0 || V > p.max_len) {
+        if (threadIdx.x == 0) record_error(p.status, ST_BAD_ROW);
+        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
+    }
+    const int32_t kk_target = min(p.k, V);
+    const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+    if (rescore) {
+        float *fb = p.fb_logits + static_cast<int64_t>(r) * p.max_len;
+        simt_score_row(p, r, V, fb, reinterpret_cast<float *>(keys));
+        row = fb;
+    }
+    int32_t n;
+    if (V <= smem_cap) {
+        for (int32_t i = threadIdx.x; i < V; i += NT) {
+            keys[i] = score_key(__ldcg(row + i));
+            inv[i] = ~static_cast<uint32_t>(i);
+        }
+        __syncthreads();
+        n = V;
+    } else {
+        uint32_t T, k_rem;
+        n = stream_narrow(sh, row, V, static_cast<uint32_t>(kk_target), smem_cap, keys, inv, T, k_rem, true);
+        if (n < 0) n = gather_cut_in_order(sh, row, V, T, k_rem, keys, inv);
+    }
+    const int32_t kk = min(p.k, n);
+    const uint64_t *result = out64;
+    if (kk > 0) {
+        uint64_t *ranked = reinterpret_cast<uint64_t *>(keys);   // keys + inv: smem_cap 8-byte slots
+        if (bucket_topk(sh, keys, inv, n, kk, out64, min(out_capacity(p), smem_cap), ranked))
+            result = ranked;
+        else
+            select_and_sort(sh, keys, inv, n, kk, out64);
+    }
+    write_row(p, r, result, kk);
+    __syncthreads();
+}
+
+// The same, kept out of line for the candidate selector, where it runs only
+// for the rare rows whose candidate list cannot be trusted.
+__device__ __noinline__ void select_row_cold(const SelectParams &p, int32_t r, SelShared &sh,
+                                             uint64_t *out64, uint32_t *keys, uint32_t *inv,
+                                             int32_t smem_cap)
+{
+    select_row(p, r, true, sh, out64, keys, inv, smem_cap);
+}
+
+// Dense rows (logits in HBM): rows r = blockIdx.x, blockIdx.x + gridDim.x, ...
+// (shared memory allows two CTAs per SM at the usual capacity)
+__global__ void __launch_bounds__(NT, 2)
 select_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -532,48 +584,8 @@ select_kernel(const SelectParams p)
     uint64_t *out64 = reinterpret_cast<uint64_t *>(smem_raw + sizeof(SelShared));
     uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + out_capacity(p));
     uint32_t *inv = keys + p.smem_cap;
-
-    if (p.mode == SEL_FALLBACK && __ldcg(&p.plan->any_fallback) == 0) return;
-    for (int32_t r = blockIdx.x; r < p.R; r += gridDim.x) {
-        if (p.mode == SEL_FALLBACK && __ldcg(p.row_flag + r) == 0) continue;   // uniform
-        int32_t V = p.row_vis[r];
-        if (V < 0 || V > p.max_len) {
-            if (threadIdx.x == 0) record_error(p.status, ST_BAD_ROW);
-            V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
-        }
-        const int32_t kk_target = min(p.k, V);
-        const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
-        if (p.mode == SEL_FALLBACK) {
-            float *fb = p.fb_logits + static_cast<int64_t>(r) * p.max_len;
-            simt_score_row(p, r, V, fb, reinterpret_cast<float *>(keys));
-            row = fb;
-        }
-        int32_t n;
-        if (V <= p.smem_cap) {
-            for (int32_t i = threadIdx.x; i < V; i += NT) {
-                keys[i] = score_key(__ldcg(row + i));
-                inv[i] = ~static_cast<uint32_t>(i);
-            }
-            __syncthreads();
-            n = V;
-        } else {
-            uint32_t T, k_rem;
-            n = stream_narrow(sh, row, V, static_cast<uint32_t>(kk_target), p.smem_cap, keys, inv, T,
-                              k_rem, true);
-            if (n < 0) n = gather_cut_in_order(sh, row, V, T, k_rem, keys, inv);
-        }
-        const int32_t kk = min(p.k, n);
-        const uint64_t *result = out64;
-        if (kk > 0) {
-            uint64_t *ranked = reinterpret_cast<uint64_t *>(keys);   // keys + inv: smem_cap 8-byte slots
-            if (bucket_topk(sh, keys, inv, n, kk, out64, min(out_capacity(p), p.smem_cap), ranked))
-                result = ranked;
-            else
-                select_and_sort(sh, keys, inv, n, kk, out64);
-        }
-        write_row(p, r, result, kk);
-        __syncthreads();
-    }
+    for (int32_t r = blockIdx.x; r < p.R; r += gridDim.x)
+        select_row(p, r, false, sh, out64, keys, inv, p.smem_cap);
 }
 
 // ------------------------------------------------------------ candidates --
@@ -586,8 +598,10 @@ select_kernel(const SelectParams p)
 // buckets; each element's rank is its output index, so the result goes
 // straight to HBM.  A row whose list cannot be trusted (fewer than min(k, V)
 // candidates, more than cap, or a cut bucket too large to order here) is
-// flagged and left to the fallback launch.
+// re-scored in plain FP32 and selected densely by the same CTA (row_flag
+// records it).
 constexpr int CT = 256;               // threads per row
+static_assert(CT == NT, "the in-kernel fallback runs the dense selection with the same block");
 constexpr int QPT = 8;                // half quarters per thread and gather round
 constexpr int BIG_MAX = 320;          // > (QSA_MAX_K + SLACK) / (RANK_MAX + 1)
 
@@ -598,6 +612,8 @@ struct CandShared {
     uint32_t cut, need, nbig, pad_;
     uint32_t big[BIG_MAX];
 };
+
+constexpr size_t CAND_HEAD = ((sizeof(CandShared) > sizeof(SelShared) ? sizeof(CandShared) : sizeof(SelShared)) + 15) / 16 * 16;
 
 // Exclusive prefix of v over the block with a single barrier; wt alternates
 // between two buffers so that consecutive calls need no barrier in between.
@@ -651,11 +667,22 @@ cand_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     CandShared &sh = *reinterpret_cast<CandShared *>(smem_raw);
-    uint64_t *a = reinterpret_cast<uint64_t *>(smem_raw + sizeof(CandShared));   // cap entries
+    uint64_t *a = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD);             // cap entries
     uint64_t *bq = a + p.cap;                                                     // k + SLACK entries
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int32_t r = blockIdx.x;
     if (r >= p.R) return;
+    // a row whose list cannot be trusted is re-scored and selected densely
+    // right here, in the same shared memory (SelShared over the head)
+    auto fallback = [&]() {
+        if (t == 0) {
+            p.row_flag[r] = 1;
+            atomicExch(&p.plan->any_fallback, 1);
+        }
+        __syncthreads();
+        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), bq,
+                        reinterpret_cast<uint32_t *>(a), reinterpret_cast<uint32_t *>(a) + p.cap, p.cap);
+    };
     int32_t V = p.row_vis[r];
     if (V < 0 || V > p.max_len) {
         if (t == 0) record_error(p.status, ST_BAD_ROW);
@@ -770,11 +797,8 @@ cand_kernel(const SelectParams p)
     for (int32_t l = t; l < (ntile * 16 + 127) / 128; l += CT) discard_l2_line(mrow + l * 32);
 
     const uint32_t n = done;
-    if (overflow || n < static_cast<uint32_t>(kk_target)) {
-        if (t == 0) {
-            p.row_flag[r] = 1;
-            atomicExch(&p.plan->any_fallback, 1);
-        }
+    if (overflow || n < static_cast<uint32_t>(kk_target)) {   // uniform
+        fallback();
         return;
     }
     const uint32_t kk = min(static_cast<uint32_t>(p.k), n);
@@ -800,10 +824,7 @@ cand_kernel(const SelectParams p)
         __syncthreads();
         const uint32_t bb = sh.cut, need = sh.need;
         if (need > static_cast<uint32_t>(p.k + SLACK)) {           // uniform: huge tie bucket at the cut
-            if (t == 0) {
-                p.row_flag[r] = 1;
-                atomicExch(&p.plan->any_fallback, 1);
-            }
+            fallback();
             return;
         }
         // ---- scatter the buckets down to the cut
@@ -1055,6 +1076,11 @@ int set_smem(K kernel, size_t smem, size_t (&done)[64])
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return static_cast<int>(e);
+        // all of the unified L1 / shared memory as shared memory: these kernels
+        // are latency-bound and live on the number of resident CTAs
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
+        if (e != cudaSuccess) return static_cast<int>(e);
         done[dev] = smem;
     }
     return 0;
@@ -1077,7 +1103,7 @@ int launch_select(const SelectParams &p, int grid, void *stream)
     }
     if (p.mode == SEL_CAND) {
         static size_t done[64] = {};
-        const size_t smem = sizeof(CandShared) + (static_cast<size_t>(p.cap) + p.k + SLACK) * 8;
+        const size_t smem = CAND_HEAD + (static_cast<size_t>(p.cap) + p.k + SLACK) * 8;
         if (int rc = set_smem(cand_kernel, smem, done)) return rc;
         cand_kernel<<<p.R, CT, smem, st>>>(p);
         return static_cast<int>(cudaGetLastError());

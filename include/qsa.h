@@ -121,8 +121,9 @@ qsa_status qsa_set_config(int32_t key, int64_t value);
 /* Kernel kinds reported by qsa_kernel_times(). */
 #define QSA_KERNEL_KINDS 10
 /* 0 plan, 1 score (logits), 2 score (sampled tiles), 3 score (threshold filter),
- * 4 score (fallback rows), 5 select (dense rows), 6 select (threshold),
- * 7 select (candidates), 8 select (fallback rows), 9 -inf padding. */
+ * 4 and 8 reserved (not launched), 5 select (dense rows), 6 select
+ * (threshold), 7 select (candidates, including rows re-scored in place),
+ * 9 -inf padding. */
 
 /* With QSA_CFG_KERNEL_TIMING on: synchronises the pending events, adds each
  * launch's elapsed time to ms[kind] and its count to launches[kind] for the
