@@ -516,7 +516,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     th.sample_stride = f.stride;
     th.tau = tau;
     th.oversample = OVERSAMPLE;
-    th.smem_cap = static_cast<int32_t>(std::min<int64_t>(f.sample_ld, 4096));   // staged scores per row
+    th.smem_cap = static_cast<int32_t>(std::min<int64_t>(f.sample_ld, TH_STAGE));   // staged scores per row
     if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, rows, stream); }))) != QSA_OK) return st;
     // 3. full scoring pass keeping only scores >= tau_r
     s.sp.mode = SCORE_FILTER;

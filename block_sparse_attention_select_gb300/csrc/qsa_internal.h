@@ -34,6 +34,7 @@ constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, 
 // store per row with no test for the rare case.  tiles_ld is a multiple of
 // 8, which keeps each row's mask words in lines of their own.
 constexpr int CAND_SLOTS = 32;   // score slots per quarter (4 planes of 8)
+constexpr int TH_STAGE = 16384;  // sampled scores of one row the threshold kernel holds in shared memory
 
 // A group: consecutive query rows of one request that share every key tile.
 struct Group {

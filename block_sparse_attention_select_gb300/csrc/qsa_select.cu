@@ -274,26 +274,44 @@ __device__ bool bucket_topk(SelShared &sh, const uint32_t *keys, const uint32_t 
         kmax = max(kmax, keys[i]);
     }
     block_minmax(sh, kmin, kmax, kmin, kmax);
-    const int shift = span_shift(kmax - kmin);
-    clear_hist(sh);
-    for (int32_t i = threadIdx.x; i < n; i += NT)
-        atomicAdd(&sh.hist[NBINS - 1 - ((keys[i] - kmin) >> shift)], 1u);
-    __syncthreads();
-    bucket_starts(sh);
-    // boundary bucket: the one whose range [bstart, end) contains position kk - 1
-    if (threadIdx.x == 0) sh.cut_digit = NBINS;
-    __syncthreads();
-    for (int b = threadIdx.x; b < NBINS; b += NT) {
-        const uint32_t s0 = sh.bstart[b];
-        const uint32_t e = (b + 1 < NBINS) ? sh.bstart[b + 1] : static_cast<uint32_t>(n);
-        if (s0 < static_cast<uint32_t>(kk) && static_cast<uint32_t>(kk) <= e) sh.cut_digit = b;
+    // Buckets over [lo, kmax].  When the buckets down to the cut span a much
+    // smaller key range than the whole row (a long tail of low scores, or the
+    // spike of exact zeros, below the top kk), count once more over that range
+    // only, so that the buckets to be ordered are small.
+    uint32_t lo = kmin, total = static_cast<uint32_t>(n);
+    int shift = span_shift(kmax - lo);
+    int bb;
+    uint32_t need;
+    for (int level = 0;; ++level) {
+        clear_hist(sh);
+        for (int32_t i = threadIdx.x; i < n; i += NT)
+            if (keys[i] >= lo) atomicAdd(&sh.hist[NBINS - 1 - ((keys[i] - lo) >> shift)], 1u);
+        __syncthreads();
+        bucket_starts(sh);
+        // boundary bucket: the one whose range [bstart, end) contains position kk - 1
+        if (threadIdx.x == 0) sh.cut_digit = NBINS;
+        __syncthreads();
+        for (int b = threadIdx.x; b < NBINS; b += NT) {
+            const uint32_t s0 = sh.bstart[b];
+            const uint32_t e = (b + 1 < NBINS) ? sh.bstart[b + 1] : total;
+            if (s0 < static_cast<uint32_t>(kk) && static_cast<uint32_t>(kk) <= e) sh.cut_digit = b;
+        }
+        __syncthreads();
+        bb = static_cast<int>(sh.cut_digit);
+        if (bb >= NBINS) return false;                                      // uniform
+        need = (bb + 1 < NBINS) ? sh.bstart[bb + 1] : total;
+        const uint32_t lo2 = lo + (static_cast<uint32_t>(NBINS - 1 - bb) << shift);
+        const int shift2 = span_shift(kmax - lo2);
+        if (level > 0 || shift == 0 || shift2 + 3 > shift) break;          // uniform
+        lo = lo2;                          // every key >= lo2 lies in buckets <= bb: need of them
+        shift = shift2;
+        total = need;
+        __syncthreads();
     }
-    __syncthreads();
-    const int bb = static_cast<int>(sh.cut_digit);
-    const uint32_t need = (bb + 1 < NBINS) ? sh.bstart[bb + 1] : static_cast<uint32_t>(n);
-    if (bb >= NBINS || need > static_cast<uint32_t>(out_cap)) return false;   // uniform
+    if (need > static_cast<uint32_t>(out_cap)) return false;   // uniform
     for (int32_t i = threadIdx.x; i < n; i += NT) {
-        const uint32_t b = NBINS - 1 - ((keys[i] - kmin) >> shift);
+        if (keys[i] < lo) continue;
+        const uint32_t b = NBINS - 1 - ((keys[i] - lo) >> shift);
         if (b > static_cast<uint32_t>(bb)) continue;
         const uint32_t pos = atomicAdd(&sh.hist[b], 1u);
         out64[pos] = (static_cast<uint64_t>(keys[i]) << 32) | inv[i];
@@ -307,7 +325,7 @@ __device__ bool bucket_topk(SelShared &sh, const uint32_t *keys, const uint32_t 
     // now, and `ranked` reuses their space.
     for (uint32_t pos = threadIdx.x; pos < need; pos += NT) {
         const uint64_t x = out64[pos];
-        const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - kmin) >> shift);
+        const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - lo) >> shift);
         const uint32_t s0 = sh.bstart[b], e = sh.hist[b];
         if (e - s0 > RANK_MAX) {
             if (pos == s0) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
@@ -902,10 +920,9 @@ cand_kernel(const SelectParams p)
 // bin holding the m-th sampled key is small.  One CTA of TH_THREADS per row:
 // the row's keys are staged in shared memory (rows longer than the staging
 // area are read from global memory in every pass instead).
-constexpr int TH_THREADS = 128;
 constexpr int TH_BINS = 256;
-constexpr int TH_STAGE = 4096;        // sampled scores of one row held in shared memory
 
+template <int TH_THREADS>
 struct ThShared {
     uint32_t hist[TH_BINS];
     uint32_t red[4][TH_THREADS / 32];
@@ -913,7 +930,8 @@ struct ThShared {
 };
 
 // Block-wide min, max, min and sum of four per-thread values (one barrier).
-__device__ __forceinline__ void th_reduce(ThShared &sh, uint32_t &a_min, uint32_t &b_max, uint32_t &c_min,
+template <int TH_THREADS>
+__device__ __forceinline__ void th_reduce(ThShared<TH_THREADS> &sh, uint32_t &a_min, uint32_t &b_max, uint32_t &c_min,
                                           uint32_t &d_sum)
 {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -938,8 +956,8 @@ __device__ __forceinline__ void th_reduce(ThShared &sh, uint32_t &a_min, uint32_
 
 // The key that about m of the n_s keys key_at(i) reach, searched in [lo, hi]
 // (every key counted lies there).
-template <typename KeyAt>
-__device__ uint32_t thresh_search(ThShared &sh, KeyAt key_at, int32_t n_s, uint32_t m, uint32_t lo,
+template <int TH_THREADS, typename KeyAt>
+__device__ uint32_t thresh_search(ThShared<TH_THREADS> &sh, KeyAt key_at, int32_t n_s, uint32_t m, uint32_t lo,
                                   uint32_t hi)
 {
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
@@ -997,12 +1015,13 @@ __device__ uint32_t thresh_search(ThShared &sh, KeyAt key_at, int32_t n_s, uint3
     return lo;
 }
 
+template <int TH_THREADS>
 __global__ void __launch_bounds__(TH_THREADS)
 thresh_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
-    ThShared &sh = *reinterpret_cast<ThShared *>(smem_raw);
-    uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw + sizeof(ThShared));
+    ThShared<TH_THREADS> &sh = *reinterpret_cast<ThShared<TH_THREADS> *>(smem_raw);
+    uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw + sizeof(ThShared<TH_THREADS>));
     const int t = threadIdx.x;
     const int32_t r = blockIdx.x;
     if (r >= p.R) return;
@@ -1095,10 +1114,18 @@ int launch_select(const SelectParams &p, int grid, void *stream)
     if (p.mode == SEL_THRESH) {
         // p.smem_cap: staged scores per row, a multiple of 4 and at most TH_STAGE
         if (p.smem_cap < 0 || p.smem_cap > TH_STAGE || (p.smem_cap & 3)) return static_cast<int>(cudaErrorInvalidValue);
-        static size_t done[64] = {};
-        const size_t smem = sizeof(ThShared) + static_cast<size_t>(p.smem_cap) * 4;
-        if (int rc = set_smem(thresh_kernel, smem, done)) return rc;
-        thresh_kernel<<<p.R, TH_THREADS, smem, st>>>(p);
+        // a wider block for long samples (sparser sampling at small k)
+        if (p.smem_cap <= 4096) {
+            static size_t done[64] = {};
+            const size_t smem = sizeof(ThShared<128>) + static_cast<size_t>(p.smem_cap) * 4;
+            if (int rc = set_smem(thresh_kernel<128>, smem, done)) return rc;
+            thresh_kernel<128><<<p.R, 128, smem, st>>>(p);
+        } else {
+            static size_t done[64] = {};
+            const size_t smem = sizeof(ThShared<256>) + static_cast<size_t>(p.smem_cap) * 4;
+            if (int rc = set_smem(thresh_kernel<256>, smem, done)) return rc;
+            thresh_kernel<256><<<p.R, 256, smem, st>>>(p);
+        }
         return static_cast<int>(cudaGetLastError());
     }
     if (p.mode == SEL_CAND) {

@@ -140,7 +140,8 @@ def tiny(seed: int = 0) -> Workload:
 
 def bench(seed: int = 1, k: int = 2048, ctx: int = 184_320, visibility: str = "pages") -> Workload:
     """Last 1,616-row chunk of a 184,320-token context (46,080 positions), k 2,048."""
-    return make_workload(f"prefill_1x1616rows_ctx{ctx}_k{k}", seed=seed, ctx_tokens=[ctx],
+    tag = "" if visibility == "pages" else f"_vis-{visibility}"
+    return make_workload(f"prefill_1x1616rows_ctx{ctx}_k{k}{tag}", seed=seed, ctx_tokens=[ctx],
                          rows_per_req=[1616], k=k, dist="gauss", shuffle_pages=False,
                          visibility=visibility)
 
@@ -166,10 +167,28 @@ def long_prefill(seed: int = 4) -> Workload:
                          dist="gauss", shuffle_pages=True)
 
 
+def bench_k512(seed: int = 1) -> Workload:
+    """The prefill bench shape with k = 512 positions (the pages' "block top-k 512")."""
+    return bench(seed=seed, k=512)
+
+
+def bench_ctx29k(seed: int = 1) -> Workload:
+    """The prefill bench shape at the pages' other context point, 29,000 tokens (7,250 positions)."""
+    return bench(seed=seed, ctx=29_000)
+
+
+def bench_plus_one(seed: int = 1) -> Workload:
+    """The prefill bench shape with V_r = t_r // 4 + 1 (the other reading of the visible count)."""
+    return bench(seed=seed, visibility="plus_one")
+
+
 CONFIGS = {
     "tiny": tiny,
     "bench": bench,
     "decode": decode,
     "ties": tie_stress,
     "long": long_prefill,
+    "bench_k512": bench_k512,
+    "ctx29k": bench_ctx29k,
+    "bench_plus1": bench_plus_one,
 }

@@ -224,7 +224,7 @@ def _sample_rows(R, rng, n=6):
     return np.unique(np.r_[0, R - 1, rng.choice(R, size=n, replace=False)])
 
 
-@pytest.mark.parametrize("name", ["bench", "decode", "ties", "long"])
+@pytest.mark.parametrize("name", ["bench", "decode", "ties", "long", "bench_k512", "ctx29k", "bench_plus1"])
 def test_full_size_config(name):
     wl = W.CONFIGS[name]()
     d = to_device(wl)
