@@ -117,6 +117,14 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// log2 of a power of two (page sizes and the sample stride are powers of two)
+int32_t log2_exact(int32_t x)
+{
+    int32_t l = 0;
+    while ((1 << l) < x) ++l;
+    return l;
+}
+
 int32_t pow2_floor(double x)
 {
     int32_t p = 1;
@@ -276,6 +284,9 @@ qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t row
     p.num_pages = keys->num_pages;
     p.page_pos = keys->page_positions;
     p.page_box = std::min(keys->page_positions, TILE_M);
+    p.page_pos_shift = log2_exact(keys->page_positions);
+    p.page_box_shift = log2_exact(p.page_box);
+    p.sample_shift = log2_exact(sample_stride);
     p.H = H;
     p.R = rows;
     p.sample_stride = sample_stride;

@@ -71,6 +71,9 @@ struct ScoreParams {
     int32_t num_pages;
     int32_t page_pos;           // positions per page
     int32_t page_box;           // rows per TMA box = min(page_pos, TILE_M)
+    int32_t page_pos_shift;     // log2(page_pos), log2(page_box), log2(sample_stride): all
+    int32_t page_box_shift;     // three are powers of two, and divisions by runtime values
+    int32_t sample_shift;       // cost ~20 instructions on the producer's critical path
     int32_t H;
     int32_t R;
     int32_t mode;

@@ -45,6 +45,7 @@ struct EpiRows {
     __align__(16) float w[64];   // w[(row - first row of the warp) * H + h]
     __align__(16) int32_t vis[64];   // V of each row
     __align__(16) float tau[64];     // FILTER threshold of each row
+    uint32_t masks[32];              // FILTER: mask words of the chunk being drained
 };
 
 static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
@@ -159,7 +160,7 @@ __device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
 // Lane i holds key position tile * 128 + quarter * 32 + i.  FULL: every row
 // of the group sees the whole tile, so no per-element visibility test.
 template <int H, int MODE, bool FULL, bool ALLROWS>
-__device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRows &e, const Group &gr,
+__device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, const Group &gr,
                                               int32_t tile, uint32_t taddr, int cq, int quarter,
                                               int lane, uint32_t lt_mask, int32_t nmine)
 {
@@ -185,7 +186,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         score0 = p.cand_score + e0 * 8;
         mask0 = p.cand_mask + e0;
     } else if constexpr (MODE == SCORE_SAMPLE) {
-        out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile / p.sample_stride) * TILE_M + p_in_tile;
+        out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile >> p.sample_shift) * TILE_M + p_in_tile;
     } else {
         out0 = p.out + r0 * p.ld + j;
     }
@@ -196,7 +197,6 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         uint32_t v[32];
         tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + ch * 32), v);
         tmem_ld_wait();
-        uint32_t my_mask = 0;                                  // FILTER: mask word of row (c0 + lane)
 #pragma unroll
         for (int b0 = 0; b0 < RPC; b0 += B) {
             if (!ALLROWS && c0 + b0 >= nmine) break;         // warp-uniform
@@ -218,7 +218,7 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
                     // is 2 * score (halved exactly by the selector)
                     const bool take = ok && s[i] >= e.tau[el];
                     const uint32_t m = __ballot_sync(0xffffffffu, take);
-                    if (lane == b0 + i) my_mask = m;
+                    if (lane == 0) e.masks[b0 + i] = m;
                     // a passing lane's slot: the passing lanes below it
                     const int rk = __popc(m & lt_mask);
                     if (take)
@@ -235,13 +235,17 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, const EpiRow
         }
         if constexpr (MODE == SCORE_FILTER) {
             // one store for the chunk: lane i writes the mask word of row c0 + i
-            if (lane < RPC && (ALLROWS || c0 + lane < nmine)) mask0[static_cast<uint32_t>(c0 + lane) * mask_row] = my_mask;
+            // (gathered through the warp's shared-memory slots, not a select per row)
+            __syncwarp();
+            if (lane < RPC && (ALLROWS || c0 + lane < nmine))
+                mask0[static_cast<uint32_t>(c0 + lane) * mask_row] = e.masks[lane];
+            __syncwarp();
         }
     }
 }
 
 template <int H, int MODE>
-__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, const EpiRows &e, const Group &gr,
+__device__ __forceinline__ void epilogue_tile(const ScoreParams &p, EpiRows &e, const Group &gr,
                                               int32_t tile, uint32_t taddr, int cq, int quarter,
                                               int lane, uint32_t lt_mask)
 {
@@ -334,10 +338,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 ga = p.groups[a.g];
             }
             const int32_t pos0 = a.tile() * TILE_M;
-            const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) / p.page_box;
+            const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
             if (lane >= nbox || ga.req < 0) return -1;
             const int32_t pos = pos0 + lane * p.page_box;
-            return __ldg(p.block_table + static_cast<int64_t>(ga.req) * p.max_pages + pos / p.page_pos);
+            return __ldg(p.block_table + static_cast<int64_t>(ga.req) * p.max_pages + (pos >> p.page_pos_shift));
         };
         int32_t ring[PREFETCH];
 #pragma unroll
@@ -379,13 +383,13 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                     break;
                 }
                 const int32_t pos0 = cur.tile() * TILE_M;
-                const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) / p.page_box;
+                const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
                 if (lane == 0)
                     mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
                 __syncwarp();
                 const int32_t pos = pos0 + lane * p.page_box;
                 const bool good = pid >= 0 && pid < p.num_pages;
-                int32_t y = good ? pid * p.page_pos + (pos % p.page_pos)
+                int32_t y = good ? pid * p.page_pos + (pos & (p.page_pos - 1))
                                  : p.num_pages * p.page_pos;   // past the end: TMA fills zeros
                 if (lane < nbox && !good) record_error(p.status, ST_BAD_PAGE);
                 // a full tile whose pages are physically consecutive is one box per K half
@@ -412,6 +416,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         if (lane == 0) {
             ItemCursor cur;
             cur.init(prefix, n_groups, it0, it1, stride);
+            const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(q_s));
             int32_t cur_g = -1, stage = 0, q_uses = 0;
             uint32_t phase = 0, acc_cnt = 0, idesc = 0;
             bool have_q = false;
@@ -431,15 +436,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 const uint32_t b = acc_cnt & 1u;
                 if (!mbar_wait(&c.acc_empty[b], ((acc_cnt >> 1) & 1u) ^ 1u, abort, lim)) break;
                 tc_fence_after();
-                const uint32_t a_base = smem_u32(k_s + stage * K_STAGE_BYTES);
-                const uint32_t b_base = smem_u32(q_s);
+                // descriptor of base + off = descriptor of base + off / 16 (the
+                // 14-bit start-address field cannot carry within shared memory)
+                const uint64_t a0 = sw128_kmajor_desc(smem_u32(k_s + stage * K_STAGE_BYTES));
                 const uint32_t d = tmem + b * 256u;
 #pragma unroll
                 for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
                     const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
-                    const uint64_t ad = sw128_kmajor_desc(a_base + (kk >> 2) * K_HALF_BYTES + off);
-                    const uint64_t bd = sw128_kmajor_desc(b_base + (kk >> 2) * Q_HALF_BYTES + off);
-                    umma_f16(d, ad, bd, idesc, kk > 0 ? 1u : 0u);
+                    umma_f16(d, a0 + (((kk >> 2) * K_HALF_BYTES + off) >> 4),
+                             q_desc0 + (((kk >> 2) * Q_HALF_BYTES + off) >> 4), idesc, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&c.empty[stage]);
                 umma_commit(&c.acc_full[b]);
