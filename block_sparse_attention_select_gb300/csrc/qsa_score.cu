@@ -418,7 +418,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             cur.init(prefix, n_groups, it0, it1, stride);
             const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(q_s));
             int32_t cur_g = -1, stage = 0, q_uses = 0;
-            uint32_t phase = 0, acc_cnt = 0, idesc = 0;
+            uint32_t phase = 0, acc_cnt = 0, idesc = 0, idle_arrivals = 0;
             bool have_q = false;
             for (; cur.valid(); cur.next()) {
                 cur.settle();
@@ -431,6 +431,11 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                     have_q = true;
                     const int n = ((gr.nrows * H + 15) / 16) * 16;
                     idesc = umma_idesc_f16_f32(TILE_M, n);
+                    // drain warps whose 64 columns hold no row of this group
+                    // skip its tiles; their release of each accumulator is
+                    // given here, after the previous use of that buffer ended
+                    static_assert(EPI_WARPS == 16, "4 lane quarters x 4 column blocks of 64");
+                    idle_arrivals = static_cast<uint32_t>(4 * (4 - min(4, (gr.nrows + 64 / H - 1) / (64 / H))));
                 }
                 if (!mbar_wait(&c.full[stage], phase, abort, lim)) break;
                 const uint32_t b = acc_cnt & 1u;
@@ -448,6 +453,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 }
                 umma_commit(&c.empty[stage]);
                 umma_commit(&c.acc_full[b]);
+                if (idle_arrivals) mbar_arrive_cnt(&c.acc_empty[b], idle_arrivals);
                 if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
                 ++acc_cnt;
             }
@@ -487,6 +493,10 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 __syncwarp();
             }
             const uint32_t b = acc_cnt & 1u;
+            if (cq * (64 / H) >= gr.nrows) {    // no row of this group here: the MMA thread releases for us
+                ++acc_cnt;
+                continue;
+            }
             if (!mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim)) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * 256u;
