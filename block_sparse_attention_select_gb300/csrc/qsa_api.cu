@@ -143,7 +143,9 @@ FilterShape filter_shape(int64_t max_len, int32_t k)
 {
     FilterShape f;
     f.stride = std::max(1, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
-    f.cap = std::max(2 * k + 256, k + 512);   // candidates the selector holds: ~1.5 k expected
+    // candidates the selector holds (~1.5 k expected); a multiple of 4 so that
+    // the selector's arrays after the cap-sized one stay 16-byte aligned
+    f.cap = (std::max(2 * k + 256, k + 512) + 3) / 4 * 4;
     const int64_t tiles = (max_len + TILE_M - 1) / TILE_M;
     f.sample_ld = std::max<int64_t>(TILE_M, (tiles + f.stride - 1) / f.stride * TILE_M);
     return f;
