@@ -163,7 +163,7 @@ bool use_filter(int32_t rows, int64_t max_len, int32_t k)
     if (g_cfg_path == 1) return false;
     if (g_cfg_path == 2) return true;
     const FilterShape f = filter_shape(max_len, k);
-    return f.stride >= 4 && max_len >= 8LL * k;
+    return f.stride >= 4 && max_len >= 3LL * k;
 }
 
 struct Layout {

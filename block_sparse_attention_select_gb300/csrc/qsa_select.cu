@@ -787,14 +787,22 @@ cand_kernel(const SelectParams p)
                 const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
                 const float *ov_q = srow + static_cast<int64_t>(e) * 8;
                 uint32_t o = off[u] + 4u;
+                // one plane of eight slots (two 16-byte loads) per step
 #pragma unroll 1
-                for (uint32_t j = 0; mm != 0u; ++j) {
-                    const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
-                    mm &= mm - 1u;
-                    const uint32_t key = score_key(0.5f * __ldcg(ov_q + (j / 8 + 1) * static_cast<int64_t>(p.cand_plane) + j % 8));
-                    kmin = min(kmin, key);
-                    kmax = max(kmax, key);
-                    a[o++] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
+                for (uint32_t g = 1; mm != 0u; ++g) {
+                    const float4 *pl = reinterpret_cast<const float4 *>(ov_q + g * static_cast<int64_t>(p.cand_plane));
+                    const float4 lo4 = __ldcg(pl), hi4 = __ldcg(pl + 1);
+                    const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (mm == 0u) break;
+                        const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                        mm &= mm - 1u;
+                        const uint32_t key = score_key(0.5f * v[j]);
+                        kmin = min(kmin, key);
+                        kmax = max(kmax, key);
+                        a[o++] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
+                    }
                 }
             }
         }
