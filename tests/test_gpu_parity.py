@@ -73,6 +73,10 @@ CASES = [
     ([9000], [11], 128, "int4", 4, 128),
     ([9000], [11], 96, "int4", 4, 256),
     ([20000, 9000], [90, 45], 256, "gauss", 4, 16),
+    # a few rows per request: the narrow scorer (decode-like batches)
+    ([5000, 3000, 12000, 800, 20000], [1, 2, 1, 1, 3], 128, "int4", 4, 16),
+    ([7000, 900, 15000], [2, 1, 1], 96, "int4", 8, 16),
+    ([30000, 2000, 11000, 6000], [1, 1, 2, 1], 512, "gauss", 4, 16),
 ]
 
 
