@@ -56,7 +56,7 @@ typedef enum {
     QSA_ERR_BAD_PAGE = 5,      /* (device) a block-table entry outside [0, num_pages) */
     QSA_ERR_TIMEOUT = 6,       /* (device) a pipeline wait ran past its time limit */
     QSA_ERR_CUDA = 7,          /* another CUDA runtime error */
-    QSA_ERR_NO_DEVICE = 8,     /* no usable sm_100-family device */
+    QSA_ERR_NO_DEVICE = 8,     /* no usable device: the kernels are built for compute capability 10.3 only */
     QSA_ERR_STATIC_LIMIT = 9   /* the call needs more scratch than QSA_STATIC_SCRATCH_BYTES */
 } qsa_status;
 
@@ -95,7 +95,17 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
                           float *out_val, void *ws, size_t ws_bytes, void *stream);
 
 /* The whole step: score every visible position of every row, then its exact
- * top-k, without the caller seeing the logits.  Same arguments as above. */
+ * top-k, without the caller seeing the logits (the operation at the top of
+ * this file).  q, w, keys, row_req, row_visible as for qsa_index_score; k,
+ * out_idx, out_val as for qsa_topk_exact; ws must hold qsa_workspace_bytes(rows,
+ * max_pages_per_req * page_positions, k, 0) bytes, 256-byte aligned.
+ * For long rows (at least 3k positions) it scores every 16th-or-so key tile
+ * first, takes from that sample a per-row threshold expected to keep ~1.5 k
+ * positions, scores every tile keeping only the positions at or above it, and
+ * selects among those; a row that kept fewer than min(k, V_r) (or too many to
+ * hold) is re-scored in plain FP32 and selected from all its positions, so the
+ * result never depends on the sample.  Shorter rows are scored into the
+ * workspace and selected directly. */
 qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, int32_t H,
                                    const qsa_paged_keys *keys, const int32_t *row_req,
                                    const int32_t *row_visible, int32_t k, int32_t *out_idx,
