@@ -32,6 +32,7 @@ std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int64_t g_cfg_path = 0;
+bool g_overlap = true;          // dependent launches inside a call (QSA_CFG_OVERLAP)
 uint64_t g_wait_ns = 2000000000ull;
 thread_local int32_t g_launches = 0;
 
@@ -236,9 +237,11 @@ struct ScoreSetup {
     ScoreParams sp;
 };
 
+// Every scorer launch follows the call's plan kernel or another kernel of
+// the call, so it may overlap its predecessor.
 int launch_scorer(const ScoreSetup &s, int grid, void *stream)
 {
-    return launch_score(s.sp, &s.tq, &s.tk, &s.tk128, grid, stream);
+    return launch_score(s.sp, &s.tq, &s.tk, &s.tk128, grid, g_overlap, stream);
 }
 
 qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
@@ -350,6 +353,11 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
         g_timing = value != 0;
         return QSA_OK;
     }
+    if (key == QSA_CFG_OVERLAP) {
+        if (value < 0 || value > 1) return QSA_ERR_INVALID_ARG;
+        g_overlap = value != 0;
+        return QSA_OK;
+    }
     if (key == QSA_CFG_WAIT_LIMIT_NS) {
         if (value <= 0) return QSA_ERR_INVALID_ARG;
         g_wait_ns = static_cast<uint64_t>(value);
@@ -426,7 +434,7 @@ qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t 
     if (st != QSA_OK) return st;
     return launch_rc(timed(K_PAD, stream, [&] {
         return launch_pad(logits, ld_logits, rows,
-                          reinterpret_cast<const int32_t *>(s.ws + s.L.row_vis), stream);
+                          reinterpret_cast<const int32_t *>(s.ws + s.L.row_vis), g_overlap, stream);
     }));
 }
 
@@ -458,7 +466,8 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
     p.out_val = out_val;
     p.smem_cap = std::max(8192, k);
     p.status = d->status;
-    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, rows, stream); }));
+    // the call's only kernel: ordered after the caller's work as usual
+    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(p, rows, false, stream); }));
 }
 
 qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, int32_t H,
@@ -506,7 +515,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
         sel.logits = logits;
         sel.ld = ld;
         sel.smem_cap = std::max(8192, k);
-        return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, rows, stream); }));
+        return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, rows, g_overlap, stream); }));
     }
 
     float *sample = reinterpret_cast<float *>(at(s.L.sample));
@@ -530,7 +539,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     th.tau = tau;
     th.oversample = OVERSAMPLE;
     th.smem_cap = static_cast<int32_t>(std::min<int64_t>(f.sample_ld, TH_STAGE));   // staged scores per row
-    if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, rows, stream); }))) != QSA_OK) return st;
+    if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, rows, g_overlap, stream); }))) != QSA_OK) return st;
     // 3. full scoring pass keeping only scores >= tau_r
     s.sp.mode = SCORE_FILTER;
     s.sp.tau = tau;
@@ -562,7 +571,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     cs.num_pages = keys->num_pages;
     cs.page_pos = keys->page_positions;
     cs.fb_logits = logits;
-    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, stream); }));
+    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, g_overlap, stream); }));
 }
 
 }  // extern "C"

@@ -15,6 +15,42 @@ __device__ __forceinline__ void record_error(uint32_t *status, uint32_t bit)
     if (status) atomicOr(status, bit);
 }
 
+// ------------------------------------------------ dependent launches --
+// A kernel launched with programmatic stream serialization may start while
+// its predecessor in the stream is still running.  wait_prior_grid blocks
+// until that predecessor has completed and its memory operations are visible
+// (it returns at once for a kernel launched without the attribute); every
+// kernel runs it before its first access to global memory, so the chain of
+// waits also orders each kernel after all earlier ones.  allow_next_grid lets
+// the stream's next kernel be scheduled once every CTA of this grid has run it
+// or exited.  The multi-CTA kernels issue it at the end of a CTA's work, so
+// only the successor's launch and placement overlap this grid's tail and its
+// CTAs land on SMs that are already free, spread as in a plain launch (issued
+// at the start, it let the successor's CTAs pile onto the first SMs to free
+// up: up to 16 threshold CTAs on some SMs, one on others).  The single-CTA
+// plan kernel issues it at once: the scorer it precedes runs one CTA per SM.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host side: launch `kernel` with its argument pointers, with or without the
+// programmatic-serialization attribute.
+inline int launch_kernel(const void *kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         bool overlap, void **args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1u : 0u;
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
+    return static_cast<int>(e != cudaSuccess ? e : cudaGetLastError());
+}
+
 // ------------------------------------------------------- float <-> key32 --
 // Order-preserving map of a binary32 score to uint32: larger score -> larger
 // key.  -0 is folded onto +0 first so that the two zeros tie.

@@ -132,16 +132,21 @@ struct SelectParams {
     uint32_t *status;
 };
 
-// Launchers (one translation unit each); return cudaError_t as int.
+// Launchers (one translation unit each); return cudaError_t as int.  With
+// `overlap` the launch carries programmatic stream serialization: the kernel
+// may be scheduled while the previous kernel of the stream is still running
+// (once every CTA of that kernel has allowed it) and waits for that kernel's
+// completion itself before it touches global memory.  The first kernel of a
+// call is launched without it, so a call never overlaps the caller's work.
 int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t group_rows,
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
                 uint32_t *status, void *stream);
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
-                 int grid, void *stream);
-int launch_select(const SelectParams &p, int grid, void *stream);
+                 int grid, bool overlap, void *stream);
+int launch_select(const SelectParams &p, int grid, bool overlap, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);
 uint32_t score_smem_bytes();
-int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream);
+int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
 
 }  // namespace qsa

@@ -59,6 +59,8 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     __shared__ int32_t s_vmax[PLAN_SMEM_GROUPS];
     __shared__ int32_t carry_req, carry_run, carry_gid, carry_items, carry_samples;
     const int tid = threadIdx.x;
+    wait_prior_grid();
+    allow_next_grid();
     if (tid == 0) { carry_req = -2; carry_run = 0; carry_gid = 0; }
     __syncthreads();
 
@@ -187,6 +189,7 @@ __global__ void pad_kernel(float *__restrict__ logits, int64_t ld, int32_t R,
                            const int32_t *__restrict__ row_vis)
 {
     const int32_t r = blockIdx.x;
+    wait_prior_grid();                      // last kernel of its call: nothing to allow
     if (r >= R) return;
     const int64_t from = (static_cast<int64_t>(row_vis[r]) + TILE_M - 1) / TILE_M * TILE_M;
     float *row = logits + static_cast<int64_t>(r) * ld;
@@ -196,10 +199,11 @@ __global__ void pad_kernel(float *__restrict__ logits, int64_t ld, int32_t R,
 
 }  // namespace
 
-int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, void *stream)
+int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream)
 {
-    pad_kernel<<<R, 256, 0, static_cast<cudaStream_t>(stream)>>>(logits, ld, R, row_vis);
-    return static_cast<int>(cudaGetLastError());
+    void *args[] = {&logits, &ld, &R, const_cast<int32_t **>(&row_vis)};
+    return launch_kernel(reinterpret_cast<const void *>(&pad_kernel), dim3(R), dim3(256), 0,
+                         static_cast<cudaStream_t>(stream), overlap, args);
 }
 
 }  // namespace qsa

@@ -278,15 +278,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const bool sampled = p.mode == SCORE_SAMPLE;
-    const int32_t n_items = sampled ? p.plan->n_sample_items : p.plan->n_items;
-    const int32_t it0 = static_cast<int32_t>((static_cast<int64_t>(n_items) * blockIdx.x) / gridDim.x);
-    const int32_t it1 = static_cast<int32_t>((static_cast<int64_t>(n_items) * (blockIdx.x + 1)) / gridDim.x);
-    if (it0 >= it1) return;
-    const int32_t n_groups = p.plan->n_groups;
-    const int32_t *prefix = sampled ? p.sample_prefix : p.item_prefix;
-    const int32_t stride = sampled ? p.sample_stride : 1;
-
+    // prologue: barriers, TMEM and descriptor prefetch touch no global
+    // memory, so they run while the previous kernel of the stream finishes
     if (threadIdx.x == 0) {
         for (int s = 0; s < KSTAGES; ++s) {
             mbar_init(&c.full[s], 1);
@@ -318,8 +311,19 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     const uint32_t tmem = c.tmem_base;
     volatile int *abort = &c.abort;
     const uint64_t lim = p.wait_limit_ns;
+    wait_prior_grid();
 
-    if (warp == 0) {
+    const bool sampled = p.mode == SCORE_SAMPLE;
+    const int32_t n_items = sampled ? p.plan->n_sample_items : p.plan->n_items;
+    const int32_t it0 = static_cast<int32_t>((static_cast<int64_t>(n_items) * blockIdx.x) / gridDim.x);
+    const int32_t it1 = static_cast<int32_t>((static_cast<int64_t>(n_items) * (blockIdx.x + 1)) / gridDim.x);
+    const int32_t n_groups = p.plan->n_groups;
+    const int32_t *prefix = sampled ? p.sample_prefix : p.item_prefix;
+    const int32_t stride = sampled ? p.sample_stride : 1;
+
+    if (it0 >= it1) {
+        // no item for this CTA: straight to the teardown
+    } else if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         // The whole warp walks the items; lane i owns key box i of a tile.
         // Block-table entries are loaded PREFETCH items ahead so that the
@@ -516,12 +520,14 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    allow_next_grid();                      // this CTA's global writes are all issued
     if (c.abort && threadIdx.x == 0) record_error(p.status, ST_TIMEOUT);
     if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 template <int H>
-int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *tk128, int grid, cudaStream_t s)
+int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *tk128, int grid, bool overlap,
+             cudaStream_t s)
 {
     static bool attr_done[64] = {};
     int dev = 0;
@@ -533,10 +539,10 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *t
         if (e != cudaSuccess) return static_cast<int>(e);
         attr_done[dev] = true;
     }
-    score_kernel<H><<<grid, SCORE_THREADS, SMEM_BYTES, s>>>(
-        *static_cast<const CUtensorMap *>(tq), *static_cast<const CUtensorMap *>(tk),
-        *static_cast<const CUtensorMap *>(tk128), p);
-    return static_cast<int>(cudaGetLastError());
+    void *args[] = {const_cast<void *>(tq), const_cast<void *>(tk), const_cast<void *>(tk128),
+                    const_cast<ScoreParams *>(&p)};
+    return launch_kernel(reinterpret_cast<const void *>(&score_kernel<H>), dim3(grid), dim3(SCORE_THREADS),
+                         SMEM_BYTES, s, overlap, args);
 }
 
 }  // namespace
@@ -544,14 +550,14 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *t
 uint32_t score_smem_bytes() { return SMEM_BYTES; }
 
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
-                 int grid, void *stream)
+                 int grid, bool overlap, void *stream)
 {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (p.H) {
-    case 1: return launch_h<1>(p, tmap_q, tmap_k, tmap_k128, grid, s);
-    case 2: return launch_h<2>(p, tmap_q, tmap_k, tmap_k128, grid, s);
-    case 4: return launch_h<4>(p, tmap_q, tmap_k, tmap_k128, grid, s);
-    case 8: return launch_h<8>(p, tmap_q, tmap_k, tmap_k128, grid, s);
+    case 1: return launch_h<1>(p, tmap_q, tmap_k, tmap_k128, grid, overlap, s);
+    case 2: return launch_h<2>(p, tmap_q, tmap_k, tmap_k128, grid, overlap, s);
+    case 4: return launch_h<4>(p, tmap_q, tmap_k, tmap_k128, grid, overlap, s);
+    case 8: return launch_h<8>(p, tmap_q, tmap_k, tmap_k128, grid, overlap, s);
     default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }

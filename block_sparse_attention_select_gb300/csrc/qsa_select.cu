@@ -602,6 +602,7 @@ select_kernel(const SelectParams p)
     uint64_t *out64 = reinterpret_cast<uint64_t *>(smem_raw + sizeof(SelShared));
     uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + out_capacity(p));
     uint32_t *inv = keys + p.smem_cap;
+    wait_prior_grid();                      // last kernel of its call: nothing to allow
     for (int32_t r = blockIdx.x; r < p.R; r += gridDim.x)
         select_row(p, r, false, sh, out64, keys, inv, p.smem_cap);
 }
@@ -689,6 +690,7 @@ cand_kernel(const SelectParams p)
     uint64_t *bq = a + p.cap;                                                     // k + SLACK entries
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int32_t r = blockIdx.x;
+    wait_prior_grid();                      // last kernel of its call: nothing to allow
     if (r >= p.R) return;
     // a row whose list cannot be trusted is re-scored and selected densely
     // right here, in the same shared memory (SelShared over the head)
@@ -1032,6 +1034,7 @@ thresh_kernel(const SelectParams p)
     uint32_t *stage = reinterpret_cast<uint32_t *>(smem_raw + sizeof(ThShared<TH_THREADS>));
     const int t = threadIdx.x;
     const int32_t r = blockIdx.x;
+    wait_prior_grid();
     if (r >= p.R) return;
     int32_t V = p.row_vis[r];
     if (V < 0 || V > p.max_len) {
@@ -1082,6 +1085,7 @@ thresh_kernel(const SelectParams p)
         tau = key_score(T);
     }
     if (t == 0) p.tau[r] = tau;
+    allow_next_grid();
 }
 
 }  // namespace
@@ -1115,9 +1119,10 @@ int set_smem(K kernel, size_t smem, size_t (&done)[64])
 
 }  // namespace
 
-int launch_select(const SelectParams &p, int grid, void *stream)
+int launch_select(const SelectParams &p, int grid, bool overlap, void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *args[] = {const_cast<SelectParams *>(&p)};
     if (grid <= 0) return static_cast<int>(cudaGetLastError());
     if (p.mode == SEL_THRESH) {
         // p.smem_cap: staged scores per row, a multiple of 4 and at most TH_STAGE
@@ -1127,28 +1132,28 @@ int launch_select(const SelectParams &p, int grid, void *stream)
             static size_t done[64] = {};
             const size_t smem = sizeof(ThShared<128>) + static_cast<size_t>(p.smem_cap) * 4;
             if (int rc = set_smem(thresh_kernel<128>, smem, done)) return rc;
-            thresh_kernel<128><<<p.R, 128, smem, st>>>(p);
+            return launch_kernel(reinterpret_cast<const void *>(&thresh_kernel<128>), dim3(p.R), dim3(128), smem, st,
+                                 overlap, args);
         } else {
             static size_t done[64] = {};
             const size_t smem = sizeof(ThShared<256>) + static_cast<size_t>(p.smem_cap) * 4;
             if (int rc = set_smem(thresh_kernel<256>, smem, done)) return rc;
-            thresh_kernel<256><<<p.R, 256, smem, st>>>(p);
+            return launch_kernel(reinterpret_cast<const void *>(&thresh_kernel<256>), dim3(p.R), dim3(256), smem, st,
+                                 overlap, args);
         }
-        return static_cast<int>(cudaGetLastError());
     }
     if (p.mode == SEL_CAND) {
         static size_t done[64] = {};
         const size_t smem = CAND_HEAD + (static_cast<size_t>(p.cap) + p.k + SLACK) * 8;
         if (int rc = set_smem(cand_kernel, smem, done)) return rc;
-        cand_kernel<<<p.R, CT, smem, st>>>(p);
-        return static_cast<int>(cudaGetLastError());
+        return launch_kernel(reinterpret_cast<const void *>(&cand_kernel), dim3(p.R), dim3(CT), smem, st, overlap,
+                             args);
     }
     static size_t done[64] = {};
     const size_t smem = sizeof(SelShared) + static_cast<size_t>(out_capacity(p)) * 8 +
                         static_cast<size_t>(p.smem_cap) * 8;
     if (int rc = set_smem(select_kernel, smem, done)) return rc;
-    select_kernel<<<grid, NT, smem, st>>>(p);
-    return static_cast<int>(cudaGetLastError());
+    return launch_kernel(reinterpret_cast<const void *>(&select_kernel), dim3(grid), dim3(NT), smem, st, overlap, args);
 }
 
 }  // namespace qsa

@@ -34,6 +34,7 @@ QSA_ERR_STATIC_LIMIT = 9
 QSA_CFG_PATH = 1
 QSA_CFG_WAIT_LIMIT_NS = 2
 QSA_CFG_KERNEL_TIMING = 3
+QSA_CFG_OVERLAP = 4
 KERNEL_KINDS = ["plan", "score_logits", "score_sample", "score_filter", "unused4",
                 "select_dense", "select_thresh", "select_cand", "unused8", "pad"]
 PATH_AUTO, PATH_DENSE, PATH_FILTER = 0, 1, 2

@@ -126,6 +126,12 @@ const char *qsa_status_string(qsa_status status);
 #define QSA_CFG_PATH 1
 #define QSA_CFG_WAIT_LIMIT_NS 2
 #define QSA_CFG_KERNEL_TIMING 3   /* 1: bracket every launch with CUDA events on its stream */
+/* 1 (default): the second and later kernels of a call are launched with
+ * programmatic stream serialization, so each is scheduled while its
+ * predecessor finishes and waits for it on the device before touching memory;
+ * 0: plain stream order.  The first kernel of a call always waits for all of
+ * the caller's earlier work on the stream. */
+#define QSA_CFG_OVERLAP 4
 qsa_status qsa_set_config(int32_t key, int64_t value);
 
 /* Kernel kinds reported by qsa_kernel_times(). */

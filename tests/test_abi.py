@@ -86,6 +86,9 @@ def test_config_switches(lib):
     assert lib.qsa_set_config(99, 1) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_set_config(qsa.QSA_CFG_WAIT_LIMIT_NS, 0) == qsa.QSA_ERR_INVALID_ARG
     assert lib.qsa_set_config(qsa.QSA_CFG_WAIT_LIMIT_NS, 2_000_000_000) == qsa.QSA_OK
+    assert lib.qsa_set_config(qsa.QSA_CFG_OVERLAP, 0) == qsa.QSA_OK
+    assert lib.qsa_set_config(qsa.QSA_CFG_OVERLAP, 2) == qsa.QSA_ERR_INVALID_ARG
+    assert lib.qsa_set_config(qsa.QSA_CFG_OVERLAP, 1) == qsa.QSA_OK
 
 
 def test_topk_host_checks(lib):
