@@ -60,19 +60,48 @@ struct ItemCursor {
     const int32_t *prefix;
     int32_t g, it, it_end, stride;
     int32_t g_first, g_next;     // items of group g: [g_first, g_next)
+    // Halving search for the group holding item it0: the last g with
+    // prefix[g] <= it0 (prefix is non-decreasing, prefix[0] = 0).  Every
+    // value it leaves in the cursor comes from loads at uniform addresses.
+    // (With the warp-wide search below in the drain and MMA roles as well, the
+    // bounds taken from lane shuffles, the filter pass ran ~10 % slower: the
+    // drain loop is issue-bound and sensitive to how its tile numbers are
+    // derived.)
     __device__ void init(const int32_t *pre, int32_t n_groups, int32_t it0, int32_t it1, int32_t s)
+    {
+        int32_t lo = 0, hi = n_groups - 1;
+        while (lo < hi) {
+            int32_t mid = (lo + hi + 1) >> 1;
+            if (__ldg(pre + mid) <= it0) lo = mid; else hi = mid - 1;
+        }
+        set(pre, lo, it0, it1, s);
+    }
+    // The same search by all 32 lanes of a warp (same arguments): each round
+    // the lanes read 32 entries spread over the remaining range and a ballot
+    // keeps the last one <= it0, so up to 32 groups take one L2 round trip
+    // instead of one per halving.  For the producer warp, whose first loads
+    // wait for it.
+    __device__ void init_warp(const int32_t *pre, int32_t n_groups, int32_t it0, int32_t it1, int32_t s, int lane)
+    {
+        int32_t lo = 0, span = n_groups;        // g in [lo, lo + span), prefix[lo] <= it0
+        while (span > 1) {
+            const int32_t step = (span + 31) >> 5;
+            const int32_t i = lo + lane * step;
+            const bool le = i < lo + span && __ldg(pre + i) <= it0;
+            const uint32_t b = __ballot_sync(0xffffffffu, le);
+            const int32_t j = 31 - __clz(b);    // lane 0 reads prefix[lo] <= it0, so b != 0
+            lo += j * step;
+            span = min(step, span - j * step);
+        }
+        set(pre, lo, it0, it1, s);
+    }
+    __device__ void set(const int32_t *pre, int32_t g0, int32_t it0, int32_t it1, int32_t s)
     {
         prefix = pre;
         it = it0;
         it_end = it1;
         stride = s;
-        // last group whose first item is <= it0 (prefix is non-decreasing)
-        int32_t lo = 0, hi = n_groups - 1;
-        while (lo < hi) {
-            int32_t mid = (lo + hi + 1) >> 1;
-            if (__ldg(prefix + mid) <= it0) lo = mid; else hi = mid - 1;
-        }
-        g = lo;
+        g = g0;
         g_first = __ldg(prefix + g);
         g_next = __ldg(prefix + g + 1);
     }
@@ -330,10 +359,20 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         // page-id round trip never sits in front of a TMA issue.
         constexpr int PREFETCH = 8;
         ItemCursor cur, ahead;
-        cur.init(prefix, n_groups, it0, it1, stride);
+        cur.init_warp(prefix, n_groups, it0, it1, stride, lane);
+        // the first group's queries are requested before the page ids: their
+        // load does not wait for the block-table round trip
+        cur.settle();
+        int32_t cur_g = cur.g, q_loads = 1, stage = 0;
+        Group gr = p.groups[cur_g];
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
+            tma_load_2d(q_s, &tmap_q, &c.q_full, 0, gr.row0 * H);
+            tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, gr.row0 * H);
+        }
         ahead = cur;
-        Group ga{};
-        int32_t ga_g = -1;                      // group held in ga (reloaded on a change only)
+        Group ga = gr;
+        int32_t ga_g = cur_g;                   // group held in ga (reloaded on a change only)
         auto page_id = [&](ItemCursor &a) -> int32_t {
             if (!a.valid()) return -1;
             a.settle();
@@ -353,9 +392,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             ring[d] = page_id(ahead);
             ahead.next();
         }
-        int32_t cur_g = -1, q_loads = 0, stage = 0;
         uint32_t phase = 0;
-        Group gr{};
         bool stop = false;
         // the ring slot read in an iteration is refilled in the same iteration
         // and read again PREFETCH iterations later (no move of a pending load)
