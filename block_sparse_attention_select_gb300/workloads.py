@@ -192,3 +192,91 @@ CONFIGS = {
     "ctx29k": bench_ctx29k,
     "bench_plus1": bench_plus_one,
 }
+
+
+# ------------------------------------------------------------------------
+# Inputs of the index-key producer (the step before the indexer): the raw
+# per-token index keys of each request's new tokens, optional pooling logits,
+# the RMSNorm weight and a paged cache to store into.  Random draws only.
+
+@dataclass
+class ProducerInputs:
+    name: str
+    x: np.ndarray              # float16 [T, D] raw index keys, request after request
+    pool_logit: np.ndarray | None   # float32 [T] or None (equal weights)
+    seq_start: np.ndarray      # int32 [num_reqs + 1] row offsets into x
+    pos_start: np.ndarray      # int32 [num_reqs] position of each request's first new token
+    norm_weight: np.ndarray    # float32 [D]
+    k_cache: np.ndarray        # float16 [num_pages, PAGE_POSITIONS, D] cache before the call
+    block_table: np.ndarray    # int32 [num_reqs, max_pages]
+    window: int                # pooling window in tokens (4 or 8)
+    rope_dim: int = 64
+    theta: float = 10000.0
+    eps: float = 1e-6
+
+    @property
+    def tokens(self) -> int:
+        return int(self.x.shape[0])
+
+    @property
+    def max_tokens(self) -> int:
+        return int(np.max(np.diff(self.seq_start))) if len(self.pos_start) else 0
+
+
+def make_producer_inputs(name: str, *, seed: int, new_tokens, pos_start, window: int = 4,
+                         logits: bool = False, rope_dim: int = 64, spare_pages: int = 3) -> ProducerInputs:
+    """new_tokens[b] tokens for request b starting at position pos_start[b];
+    each request's block table covers its last position, pages shuffled over
+    a cache with a few spare pages (filled with random keys, never written)."""
+    rng = np.random.default_rng(seed)
+    new_tokens = np.asarray(new_tokens, dtype=np.int64)
+    pos_start = np.asarray(pos_start, dtype=np.int64)
+    nreq = len(new_tokens)
+    seq_start = np.zeros(nreq + 1, dtype=np.int32)
+    seq_start[1:] = np.cumsum(new_tokens)
+    T = int(seq_start[-1])
+    x = (rng.standard_normal((T, HEAD_DIM)) * 0.5).astype(np.float16)
+    pool_logit = (rng.standard_normal(T) * 1.5).astype(np.float32) if logits else None
+    norm_weight = (1.0 + 0.1 * rng.standard_normal(HEAD_DIM)).astype(np.float32)
+    blocks_end = (pos_start + new_tokens + COMPRESS_RATIO - 1) // COMPRESS_RATIO
+    pages_per_req = np.maximum(1, (blocks_end + PAGE_POSITIONS - 1) // PAGE_POSITIONS)
+    max_pages = int(pages_per_req.max()) if nreq else 1
+    num_pages = int(pages_per_req.sum()) + spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    block_table = np.full((max(nreq, 1), max_pages), -1, dtype=np.int32)
+    at = 0
+    for b in range(nreq):
+        n = int(pages_per_req[b])
+        block_table[b, :n] = perm[at:at + n]
+        at += n
+    k_cache = (rng.standard_normal((num_pages, PAGE_POSITIONS, HEAD_DIM)) * 0.25).astype(np.float16)
+    return ProducerInputs(name, x, pool_logit, seq_start, pos_start.astype(np.int32), norm_weight,
+                          k_cache, block_table, window, rope_dim)
+
+
+def producer_small(seed: int = 11, window: int = 4, logits: bool = False) -> ProducerInputs:
+    """Ragged requests: from position 0, mid-context chunks (aligned and not), a
+    decode step that completes a block (passing the block's four tokens), a
+    decode token that completes none, an empty request."""
+    return make_producer_inputs("producer_small", seed=seed, window=window, logits=logits,
+                                new_tokens=[37, 64, 23, 4, 1, 0, 300],
+                                pos_start=[0, 128, 70, 12, 17, 40, 1000])
+
+
+def producer_context(seed: int = 12, window: int = 4, logits: bool = False) -> ProducerInputs:
+    """One request's whole 184,320-token context (46,080 index keys)."""
+    return make_producer_inputs("producer_ctx184320", seed=seed, window=window, logits=logits,
+                                new_tokens=[184_320], pos_start=[0])
+
+
+def producer_chunk(seed: int = 13, window: int = 4, logits: bool = False) -> ProducerInputs:
+    """The new tokens of a 1,616-token prefill chunk at the end of a 184,320-token context."""
+    return make_producer_inputs("producer_chunk1616", seed=seed, window=window, logits=logits,
+                                new_tokens=[1616], pos_start=[184_320 - 1616])
+
+
+PRODUCER_CONFIGS = {
+    "small": producer_small,
+    "context": producer_context,
+    "chunk": producer_chunk,
+}
