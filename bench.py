@@ -399,6 +399,133 @@ def measure_e2e(args, wl, qsa, keys_dev, stream, dev):
             "d2h_bytes_per_step": d2h, "ms_per_step": dt * 1e3}
 
 
+PRODUCE_METRIC = "index-key producer keys/s (pool + RMSNorm + RoPE + paged store) on 1 GB300"
+
+
+def produce_bytes(inp):
+    """Algorithmic bytes of one producer call: every token key (and pooling
+    logit) read once, per stored key its RoPE table row, its block-table entry
+    and the 256-byte FP16 key written."""
+    from oracle import producer as P  # noqa: F401  (block count only)
+    nkeys = sum(len(P.produced_blocks(int(inp.pos_start[b]), int(inp.seq_start[b + 1] - inp.seq_start[b]),
+                                      inp.window)) for b in range(len(inp.pos_start)))
+    read = inp.tokens * 256 + (inp.tokens * 4 if inp.pool_logit is not None else 0)
+    per_key = inp.rope_dim * 4 + 4 + 256
+    return nkeys, read + nkeys * per_key
+
+
+def run_produce(args, ws, rank, local):
+    import torch
+
+    from block_sparse_attention_select_gb300 import qsa
+
+    qsa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.PRODUCER_CONFIGS[args.producer_workload](window=args.window, logits=args.window == 8)
+    nkeys, alg_bytes = produce_bytes(inp)
+    peaks = load_peaks()
+    x = torch.from_numpy(inp.x).to(dev)
+    pl = torch.from_numpy(inp.pool_logit).to(dev) if inp.pool_logit is not None else None
+    ss = torch.from_numpy(inp.seq_start).to(dev)
+    ps = torch.from_numpy(inp.pos_start).to(dev)
+    g = torch.from_numpy(inp.norm_weight).to(dev)
+    kc = torch.from_numpy(inp.k_cache).to(dev)
+    keys = qsa.PagedKeys(kc, torch.from_numpy(inp.block_table).to(dev))
+    nb = int(((inp.pos_start.astype(np.int64) + np.diff(inp.seq_start)) // 4).max()) + 1
+    tab = qsa.rope_table(nb, inp.rope_dim, inp.theta)       # built once per model, not per step
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qsa.index_key_produce(x, ss, ps, inp.max_tokens, g, tab, keys, pool_logit=pl, eps=inp.eps,
+                              rope_dim=inp.rope_dim, window=inp.window, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()                                     # inputs fit in L2: flush between steps
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), ws)
+    achieved = alg_bytes / (ms / 1e3) / 1e9              # one launch per step
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(inp.x).pin_memory()
+        hl = torch.from_numpy(inp.pool_logit).pin_memory() if inp.pool_logit is not None else None
+        hout = torch.empty(kc.shape, dtype=kc.dtype).pin_memory()
+        n_e = max(3, min(args.steps, 50))
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(n_e):
+            x.copy_(hx, non_blocking=True)
+            if hl is not None:
+                pl.copy_(hl, non_blocking=True)
+            step()
+            hout.copy_(kc, non_blocking=True)
+            torch.cuda.synchronize()
+        el = (time.perf_counter() - t) / n_e
+        h2d = hx.numel() * 2 + (hl.numel() * 4 if hl is not None else 0)
+        e2e = {"value": nkeys / el, "unit": "keys/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": hout.numel() * 2, "ms_per_step": el * 1e3}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        from oracle import producer as P
+        t = time.perf_counter()
+        _, done = P.produce(inp.x, inp.pool_logit, inp.seq_start, inp.pos_start, inp.norm_weight, inp.eps,
+                            inp.rope_dim, inp.theta, inp.window, inp.k_cache, inp.block_table)
+        el = time.perf_counter() - t
+        cpu = {"value": len(done) / el, "unit": "keys/s", "cores": 1, "kind": "oracle",
+               "sample": f"all {len(done)} keys of {inp.name} (numpy float64, one thread), {el:.1f} s"}
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        try:
+            ent = json.load(open(tr_path)).get(f"{inp.name}_w{inp.window}", {}).get("produce")
+            if ent and ent.get("kernel_rev") == kernel_revision():
+                traffic = ent["bytes_per_launch"]
+        except Exception:
+            traffic = None
+    line = {
+        "metric": PRODUCE_METRIC, "value": nkeys * ws / (ms / 1e3), "unit": "keys/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in / f32 math / f16 out", "data": "synthetic",
+        "config": {"workload": f"{inp.name}_w{inp.window}", "tokens": inp.tokens, "keys": nkeys,
+                   "window": inp.window, "pool_logits": inp.pool_logit is not None, "rope_dim": inp.rope_dim,
+                   "page_positions": int(inp.k_cache.shape[1]), "l2": "flushed between steps (512 MiB write)",
+                   "median_ms": statistics.median(step_ms)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": "produce",
+                     "kernel_ms": ms, "algorithmic_bytes": alg_bytes, "peak_source": peaks["source"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,10 +536,21 @@ def main():
     ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--op", choices=["select", "produce"], default="select",
+                    help="select: the indexer step (default); produce: the index-key producer")
+    ap.add_argument("--producer-workload", choices=sorted(W.PRODUCER_CONFIGS), default="context")
+    ap.add_argument("--window", type=int, choices=[4, 8], default=4)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_setup()
-    if args.impl == "reference":
+    if args.op == "produce":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the producer's reference arm is the "
+                                  "oracle, reported as cpu_baseline in the produce line"}), flush=True)
+        else:
+            run_produce(args, ws, rank, local)
+    elif args.impl == "reference":
         run_reference(args, ws, rank)
     else:
         run_ours(args, ws, rank, local)

@@ -368,6 +368,63 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
 
 int32_t qsa_last_launch_count(void) { return g_launches; }
 
+qsa_status qsa_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream)
+{
+    g_launches = 0;
+    if (n_blocks < 0 || rope_dim < 0 || rope_dim > HEAD_DIM || (rope_dim & 7)) return QSA_ERR_INVALID_ARG;
+    if (!(theta > 0.0) || !std::isfinite(theta)) return QSA_ERR_INVALID_ARG;
+    if (n_blocks == 0 || rope_dim == 0) return QSA_OK;
+    if (!table || !aligned(table, 16)) return QSA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(n_blocks) * rope_dim >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+    DeviceInfo *d = nullptr;
+    qsa_status st = device_info(&d);
+    if (st != QSA_OK) return st;
+    return launch_rc(launch_rope_table(table, n_blocks, rope_dim, theta, stream));
+}
+
+qsa_status qsa_index_key_produce(const void *x, const float *pool_logit, int32_t n_reqs,
+                                 const int32_t *seq_start, const int32_t *pos_start, int32_t max_tokens,
+                                 const float *norm_weight, float eps, const float *rope_table,
+                                 int32_t rope_blocks, int32_t rope_dim, int32_t window,
+                                 const qsa_paged_keys *keys, void *stream)
+{
+    g_launches = 0;
+    if (n_reqs < 0 || max_tokens < 0 || rope_blocks < 0) return QSA_ERR_INVALID_ARG;
+    if (window != 4 && window != 8) return QSA_ERR_UNSUPPORTED;
+    if (rope_dim < 0 || rope_dim > HEAD_DIM || (rope_dim & 7)) return QSA_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return QSA_ERR_INVALID_ARG;
+    qsa_status st = check_keys(keys);
+    if (st != QSA_OK) return st;
+    if (n_reqs == 0 || max_tokens == 0) return QSA_OK;
+    if (n_reqs > keys->num_reqs || n_reqs > 65535) return QSA_ERR_UNSUPPORTED;
+    if (!x || !seq_start || !pos_start || !norm_weight) return QSA_ERR_INVALID_ARG;
+    if (!aligned(x, 8) || !aligned(norm_weight, 16)) return QSA_ERR_INVALID_ARG;
+    if (rope_dim > 0 && (!rope_table || !aligned(rope_table, 16))) return QSA_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != QSA_OK) return st;
+    ProduceParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = x;
+    p.pool_logit = pool_logit;
+    p.seq_start = seq_start;
+    p.pos_start = pos_start;
+    p.norm_weight = norm_weight;
+    p.rope_table = rope_table;
+    p.k_cache = const_cast<void *>(keys->k_cache);
+    p.block_table = keys->block_table;
+    p.n_reqs = n_reqs;
+    p.num_pages = keys->num_pages;
+    p.page_positions = keys->page_positions;
+    p.page_shift = log2_exact(keys->page_positions);
+    p.max_pages = keys->max_pages_per_req;
+    p.rope_dim = rope_dim;
+    p.rope_blocks = rope_dim > 0 ? rope_blocks : INT32_MAX;
+    p.window = window;
+    p.eps = eps;
+    p.status = d->status;
+    return launch_rc(launch_produce(p, max_tokens, stream));
+}
+
 qsa_status qsa_kernel_times(double *ms, int32_t *launches, int32_t n)
 {
     std::lock_guard<std::mutex> lk(g_mu);

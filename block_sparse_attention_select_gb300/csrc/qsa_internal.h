@@ -132,6 +132,22 @@ struct SelectParams {
     uint32_t *status;
 };
 
+// Index-key producer (the step before the indexer): see qsa_produce.cu.
+struct ProduceParams {
+    const void *x;              // FP16 [T, 128] token keys, request after request
+    const float *pool_logit;    // [T] or nullptr (equal weights)
+    const int32_t *seq_start;   // [n_reqs + 1] row offsets into x
+    const int32_t *pos_start;   // [n_reqs] position of each request's first new token
+    const float *norm_weight;   // [128], 16-byte aligned
+    const float *rope_table;    // [rope_blocks, rope_dim], 16-byte aligned
+    void *k_cache;              // FP16 [num_pages, page_positions, 128]
+    const int32_t *block_table; // [>= n_reqs, max_pages]
+    int32_t n_reqs, num_pages, page_positions, page_shift, max_pages;
+    int32_t rope_dim, rope_blocks, window;
+    float eps;
+    uint32_t *status;
+};
+
 // Launchers (one translation unit each); return cudaError_t as int.  With
 // `overlap` the launch carries programmatic stream serialization: the kernel
 // may be scheduled while the previous kernel of the stream is still running
@@ -148,5 +164,7 @@ int launch_select(const SelectParams &p, int grid, bool overlap, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
+int launch_produce(const ProduceParams &p, int32_t max_tokens, void *stream);
+int launch_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream);
 
 }  // namespace qsa

@@ -95,6 +95,11 @@ def load(path: str = LIB_PATH):
     lib.qsa_select_paged_tokens_noalloc.argtypes = [vp, vp, i32, i32, kp, vp, vp, i32, vp, vp, vp]
     lib.qsa_kernel_times.restype = ctypes.c_int
     lib.qsa_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), i32]
+    lib.qsa_rope_table.restype = ctypes.c_int
+    lib.qsa_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
+    lib.qsa_index_key_produce.restype = ctypes.c_int
+    lib.qsa_index_key_produce.argtypes = [vp, vp, i32, vp, vp, i32, vp, ctypes.c_float, vp, i32, i32, i32,
+                                          kp, vp]
     _lib = lib
     return lib
 
@@ -216,6 +221,34 @@ def select_paged_tokens_noalloc(q, w, keys: PagedKeys, row_req, row_visible, k: 
                                                 _ptr(out_idx), _ptr(out_val), _stream(stream))
     _check(st, "qsa_select_paged_tokens_noalloc")
     return out_idx, out_val
+
+
+def rope_table(n_blocks: int, rope_dim: int = 64, theta: float = 10000.0, device=None, stream=None):
+    """cos / sin rows of the block-start positions 4i, i < n_blocks: FP32 [n_blocks, rope_dim]."""
+    t = torch.empty((max(int(n_blocks), 1), max(int(rope_dim), 8)), dtype=torch.float32,
+                    device=device or "cuda")
+    _check(load().qsa_rope_table(_ptr(t), int(n_blocks), int(rope_dim), float(theta), _stream(stream)),
+           "qsa_rope_table")
+    return t
+
+
+def index_key_produce(x, seq_start, pos_start, max_tokens: int, norm_weight, rope_tab, keys: PagedKeys,
+                      pool_logit=None, eps: float = 1e-6, rope_dim: int = 64, window: int = 4, stream=None):
+    """Pool, RMS-normalise, rotate and store the index key of every block the new
+    tokens complete (x FP16 [T, 128]; seq_start int32 [B + 1]; pos_start int32
+    [B]) into keys.k_cache, in place."""
+    _need(x, torch.float16, "x"), _need(seq_start, torch.int32, "seq_start")
+    _need(pos_start, torch.int32, "pos_start"), _need(norm_weight, torch.float32, "norm_weight")
+    if pool_logit is not None:
+        _need(pool_logit, torch.float32, "pool_logit")
+    if rope_tab is not None:
+        _need(rope_tab, torch.float32, "rope_tab")
+    rope_blocks = int(rope_tab.shape[0]) if rope_tab is not None else 0
+    st = load().qsa_index_key_produce(_ptr(x), _ptr(pool_logit), int(pos_start.shape[0]), _ptr(seq_start),
+                                      _ptr(pos_start), int(max_tokens), _ptr(norm_weight), float(eps),
+                                      _ptr(rope_tab), rope_blocks, int(rope_dim), int(window),
+                                      ctypes.byref(keys.c), _stream(stream))
+    _check(st, "qsa_index_key_produce")
 
 
 def get_device_status(stream=None) -> int:

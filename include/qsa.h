@@ -115,6 +115,50 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
  * current device (QSA_OK when no kernel recorded an error). */
 qsa_status qsa_get_device_status(void *stream);
 
+/* ---- Index-key producer: the step before the indexer ----------------------
+ * ("spec(MODEL-MM-QWEN4-EXP) ...", section "The component deep-dives": one
+ * stored index-key state per four tokens, emitted at the token with
+ * (position + 1) % 4 == 0, RMSNorm on the pooled key, RoPE at the block-start
+ * position; the DSv4 compress kernel pools with a learned softmax over an
+ * overlapping window of eight tokens.)  The pages fix neither the pooling
+ * weights nor the RoPE layout; this library's reading:
+ *   key_i = RoPE_{4i}( RMSNorm( sum_t a_t * x_t ) )  over the window's tokens t,
+ *   a = softmax(pool_logit over the window), or equal weights (the mean) when
+ *   pool_logit is NULL; window 4 (the block) or 8 (the block and the four
+ *   tokens before it), clipped at position 0; RMSNorm(v) = v / sqrt(mean(v^2)
+ *   + eps) * norm_weight; RoPE rotates the pairs (j, j + rope_dim/2),
+ *   j < rope_dim/2, by 4i * theta^(-2j/rope_dim) and passes dims >= rope_dim;
+ *   the key is rounded to FP16 and stored in keys->k_cache at page
+ *   block_table[b][i / P], slot i % P (the cache is written through the
+ *   k_cache pointer, which must point to writable device memory).
+ *
+ * qsa_rope_table: fills table[i * rope_dim + j] = cos(4i * theta^(-2j/rope_dim))
+ * and table[i * rope_dim + rope_dim/2 + j] = the sine, for i < n_blocks and
+ * j < rope_dim/2, angles in FP64, stored as FP32.  Built once per model; the
+ * producer reads row i for block i.  table: device, 16-byte aligned, n_blocks
+ * * rope_dim floats.  rope_dim a multiple of 8 in [0, 128]; theta > 0. */
+qsa_status qsa_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream);
+
+/* qsa_index_key_produce: request b's new tokens are rows seq_start[b] ..
+ * seq_start[b+1]-1 of x (FP16 [T, 128], 8-byte aligned), at positions
+ * pos_start[b] ..; pool_logit: FP32 [T] or NULL.  Block i of request b is
+ * produced when it is complete among the new tokens and every position of its
+ * window (from max(0, 4i + 4 - window)) is among them: a decode step that
+ * completes a block passes that block's (window's) tokens.  max_tokens: an
+ * upper bound of seq_start[b+1] - seq_start[b] (host value; a request with
+ * more is flagged and its extra blocks are skipped).  norm_weight: FP32 [128],
+ * 16-byte aligned.  rope_table: rope_blocks rows from qsa_rope_table (unused,
+ * may be NULL, when rope_dim is 0).  window: 4 or 8 (else
+ * QSA_ERR_UNSUPPORTED).  n_reqs <= keys->num_reqs and <= 65535.  Device-side
+ * problems (a negative position, a block past the block table or the rope
+ * table, a page id outside the cache) skip that block and are reported by
+ * qsa_get_device_status(). */
+qsa_status qsa_index_key_produce(const void *x, const float *pool_logit, int32_t n_reqs,
+                                 const int32_t *seq_start, const int32_t *pos_start, int32_t max_tokens,
+                                 const float *norm_weight, float eps, const float *rope_table,
+                                 int32_t rope_blocks, int32_t rope_dim, int32_t window,
+                                 const qsa_paged_keys *keys, void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *qsa_status_string(qsa_status status);
 

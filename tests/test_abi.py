@@ -100,3 +100,40 @@ def test_topk_host_checks(lib):
     assert f(None, 10, 4, vp(16), 4, vp(16), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
     assert f(vp(16), 10, 4, vp(16), qsa.QSA_MAX_K + 1, vp(16), None, None, 0,
              None) == qsa.QSA_ERR_UNSUPPORTED
+
+
+def test_producer_host_checks(lib):
+    vp = ctypes.c_void_p
+    keys = qsa.PagedKeysC(16, 4, 16, 128, 16, 1, 4)
+    f = lib.qsa_index_key_produce
+
+    def call(**kw):
+        a = dict(x=vp(16), pl=None, n=1, ss=vp(16), ps=vp(16), mt=8, g=vp(16), eps=1e-6, rt=vp(16),
+                 rb=4, rd=64, win=4, keys=ctypes.byref(keys))
+        a.update(kw)
+        return f(a["x"], a["pl"], a["n"], a["ss"], a["ps"], a["mt"], a["g"], a["eps"], a["rt"], a["rb"],
+                 a["rd"], a["win"], a["keys"], None)
+
+    assert call(win=6) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(rd=60) == qsa.QSA_ERR_INVALID_ARG           # not a multiple of 8
+    assert call(rd=136) == qsa.QSA_ERR_INVALID_ARG
+    assert call(eps=-1.0) == qsa.QSA_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == qsa.QSA_ERR_INVALID_ARG
+    assert call(n=-1) == qsa.QSA_ERR_INVALID_ARG
+    assert call(n=0) == qsa.QSA_OK                           # nothing to do
+    assert call(mt=0) == qsa.QSA_OK
+    assert call(n=2) == qsa.QSA_ERR_UNSUPPORTED             # more requests than the block table has
+    assert call(x=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(x=vp(12)) == qsa.QSA_ERR_INVALID_ARG        # 8-byte alignment
+    assert call(g=vp(24)) == qsa.QSA_ERR_INVALID_ARG        # 16-byte alignment
+    assert call(rt=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(keys=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call() in (qsa.QSA_ERR_NO_DEVICE,)               # every host check passed, no GPU here
+    assert call(rd=0, rt=None) in (qsa.QSA_ERR_NO_DEVICE,)  # no table needed without rotation
+    r = lib.qsa_rope_table
+    assert r(vp(16), 4, 60, 10000.0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert r(vp(16), 4, 64, 0.0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert r(vp(16), -1, 64, 10000.0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert r(None, 0, 64, 10000.0, None) == qsa.QSA_OK
+    assert r(vp(20), 4, 64, 10000.0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert r(vp(16), 4, 64, 10000.0, None) == qsa.QSA_ERR_NO_DEVICE
