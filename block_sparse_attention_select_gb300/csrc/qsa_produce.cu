@@ -4,9 +4,10 @@
 // pooled key, RoPE at the block-start position; the DSv4 compress kernel pools
 // with a learned softmax over an overlapping window of eight tokens).
 //
-// One warp per produced block i of request b, lane l holding dimensions
-// [4l, 4l + 4): the window's token keys are loaded at once (one 256-byte line
-// per token per warp), pooled with softmax weights of the pooling logits (the
+// Two produced blocks i per warp (one with the 8-token window), lane l
+// holding dimensions [4l, 4l + 4):
+// the windows' token keys are loaded at once (one 256-byte line per token per
+// warp), pooled with softmax weights of the pooling logits (the
 // mean without them), RMS-normalised with a warp reduction, rotated with the
 // cos / sin row of the block from a table built once (qsa_rope_table, FP64
 // angles), and stored as FP16 into slot i % P of page block_table[b][i / P].
@@ -20,8 +21,12 @@
 namespace qsa {
 namespace {
 
-constexpr int PROD_WARPS = 8;      // blocks per CTA
-constexpr int MAX_WINDOW = 8;
+constexpr int PROD_WARPS = 8;      // warps per CTA
+// keys per warp: two for window 4; window 8 already holds eight token lines
+// per key (two keys per warp there cost spills and one CTA per SM, measured
+// slower)
+template <int W>
+__host__ __device__ constexpr int keys_per_warp() { return W == 4 ? 2 : 1; }
 
 // four FP16 values held as raw bits (two registers) until they are used
 __device__ __forceinline__ float4 half4_to_float4(uint2 u)
@@ -31,9 +36,15 @@ __device__ __forceinline__ float4 half4_to_float4(uint2 u)
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// W: the pooling window (4 or 8 tokens).  Each warp takes KPW keys, i_base
+// and i_base + PROD_WARPS * k, and requests every load of all of them before
+// it computes any: the bytes a warp keeps in flight, not the HBM rate, bound
+// this kernel.
+template <int W>
 __global__ void __launch_bounds__(PROD_WARPS * 32, 4)
 produce_kernel(const ProduceParams p)
 {
+    constexpr int KPW = keys_per_warp<W>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t b = blockIdx.y;
     wait_prior_grid();
@@ -49,105 +60,122 @@ produce_kernel(const ProduceParams p)
     // blocks [i_lo, i_hi): complete within the new tokens, and every existing
     // position of the window among them (window start max(0, 4i + 4 - W) >= p0)
     const int32_t i_hi = (p0 + n) >> 2;
-    const int32_t i_lo = p0 == 0 ? 0 : (p0 + p.window - 1) >> 2;
-    if (threadIdx.x == 0 && blockIdx.x == 0 && i_hi - i_lo > static_cast<int32_t>(gridDim.x) * PROD_WARPS)
+    const int32_t i_lo = p0 == 0 ? 0 : (p0 + W - 1) >> 2;
+    if (threadIdx.x == 0 && blockIdx.x == 0 && i_hi - i_lo > static_cast<int32_t>(gridDim.x) * PROD_WARPS * KPW)
         record_error(p.status, ST_BAD_ROW);            // more new tokens than max_tokens promised
-    const int32_t i = i_lo + static_cast<int32_t>(blockIdx.x) * PROD_WARPS + warp;
-    if (i >= i_hi) return;
+    const int32_t i_base = i_lo + static_cast<int32_t>(blockIdx.x) * PROD_WARPS * KPW + warp;
+    if (i_base >= i_hi) return;                         // warp-uniform
 
-    // ---- the window's tokens, all requested before any is used
-    const int32_t first = max(0, 4 * i + 4 - p.window);
-    const int32_t nw = 4 * i + 4 - first;               // 4 .. MAX_WINDOW
-    const __half *xw = static_cast<const __half *>(p.x) + (static_cast<int64_t>(t0) + first - p0) * HEAD_DIM +
-                       4 * lane;
-    uint2 xr[MAX_WINDOW];
-    float lg[MAX_WINDOW];
-#pragma unroll
-    for (int w = 0; w < MAX_WINDOW; ++w) {
-        if (w < nw) {
-            xr[w] = __ldg(reinterpret_cast<const uint2 *>(xw + w * HEAD_DIM));
-            lg[w] = p.pool_logit ? __ldg(p.pool_logit + t0 + first - p0 + w) : 0.0f;
-        }
-    }
-    const float4 g = __ldg(reinterpret_cast<const float4 *>(p.norm_weight) + lane);
-    // the block's RoPE row and page id do not depend on the arithmetic below:
-    // requested now, so the warp waits for one round trip to memory, not three
     const int32_t h = p.rope_dim >> 1;                  // a multiple of 4
     const int32_t d0 = 4 * lane;
     const bool lo_half = d0 < h, hi_half = !lo_half && d0 < p.rope_dim;
-    const bool table_ok = i < p.rope_blocks;
-    float4 cs = make_float4(1.0f, 1.0f, 1.0f, 1.0f), sn = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if ((lo_half || hi_half) && table_ok) {
-        const int32_t j0 = lo_half ? d0 : d0 - h;
-        const float *row = p.rope_table + static_cast<int64_t>(i) * p.rope_dim;
-        cs = __ldg(reinterpret_cast<const float4 *>(row + j0));
-        sn = __ldg(reinterpret_cast<const float4 *>(row + h + j0));
-    }
-    const int32_t pi = i >> p.page_shift;
-    const int32_t page = pi < p.max_pages ? __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pi) : -1;
+    const int32_t j0 = lo_half ? d0 : d0 - h;
 
-    // ---- pool: softmax of the logits over the window (equal logits = mean)
-    float m = lg[0];
+    // ---- every load of every key of this warp, before any arithmetic: the
+    //      window's token lines, pooling logits, RoPE row and page id
+    uint2 xr[KPW][W];
+    float lg[KPW][W];
+    float4 cs[KPW], sn[KPW];
+    int32_t page[KPW], nw[KPW];
 #pragma unroll
-    for (int w = 1; w < MAX_WINDOW; ++w)
-        if (w < nw) m = fmaxf(m, lg[w]);
-    float e[MAX_WINDOW], sum = 0.0f;
+    for (int k = 0; k < KPW; ++k) {
+        const int32_t i = i_base + k * PROD_WARPS;
+        cs[k] = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+        sn[k] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        page[k] = -1;
+        nw[k] = 0;
+        if (i < i_hi) {                                 // warp-uniform
+            const int32_t first = max(0, 4 * i + 4 - W);
+            nw[k] = 4 * i + 4 - first;                  // W, or less at block 0 when W = 8
+            const int64_t r0 = static_cast<int64_t>(t0) + first - p0;
+            const __half *xw = static_cast<const __half *>(p.x) + r0 * HEAD_DIM + 4 * lane;
 #pragma unroll
-    for (int w = 0; w < MAX_WINDOW; ++w) {
-        e[w] = 0.0f;
-        if (w < nw) {
-            e[w] = expf(lg[w] - m);
-            sum += e[w];
+            for (int w = 0; w < W; ++w) {
+                if (w < nw[k]) {
+                    xr[k][w] = __ldg(reinterpret_cast<const uint2 *>(xw + w * HEAD_DIM));
+                    lg[k][w] = p.pool_logit ? __ldg(p.pool_logit + r0 + w) : 0.0f;
+                }
+            }
+            if ((lo_half || hi_half) && i < p.rope_blocks) {
+                const float *row = p.rope_table + static_cast<int64_t>(i) * p.rope_dim;
+                cs[k] = __ldg(reinterpret_cast<const float4 *>(row + j0));
+                sn[k] = __ldg(reinterpret_cast<const float4 *>(row + h + j0));
+            }
+            const int32_t pi = i >> p.page_shift;
+            if (pi < p.max_pages) page[k] = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_pages + pi);
         }
     }
-    const float inv_sum = 1.0f / sum;
-    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int w = 0; w < MAX_WINDOW; ++w) {
-        if (w < nw) {
-            const float a = e[w] * inv_sum;
-            const float4 xv = half4_to_float4(xr[w]);
-            v[0] = fmaf(a, xv.x, v[0]);
-            v[1] = fmaf(a, xv.y, v[1]);
-            v[2] = fmaf(a, xv.z, v[2]);
-            v[3] = fmaf(a, xv.w, v[3]);
-        }
-    }
-
-    // ---- RMSNorm over the 128 dimensions
-    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss * (1.0f / HEAD_DIM) + p.eps);
-    float y[4] = {v[0] * r * g.x, v[1] * r * g.y, v[2] * r * g.z, v[3] * r * g.w};
-
-    // ---- RoPE at position 4i: pairs (j, j + h) of the first rope_dim dims
+    const float4 g = __ldg(reinterpret_cast<const float4 *>(p.norm_weight) + lane);
     const int src = lo_half ? lane + (h >> 2) : (hi_half ? lane - (h >> 2) : lane);
-    float yp[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) yp[c] = __shfl_sync(0xffffffffu, y[c], src);
-    if (lo_half || hi_half) {
-        const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, sc[4] = {sn.x, sn.y, sn.z, sn.w};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            y[c] = lo_half ? y[c] * cc[c] - yp[c] * sc[c] : yp[c] * sc[c] + y[c] * cc[c];
-    }
 
-    // ---- store into the block's page slot
-    if (!table_ok || pi >= p.max_pages) {
-        if (lane == 0) record_error(p.status, ST_BAD_ROW);
-        return;
+#pragma unroll
+    for (int k = 0; k < KPW; ++k) {
+        const int32_t i = i_base + k * PROD_WARPS;
+        if (i >= i_hi) break;                           // warp-uniform (keys in order)
+
+        // ---- pool: softmax of the logits over the window (equal logits = mean)
+        float m = lg[k][0];
+#pragma unroll
+        for (int w = 1; w < W; ++w)
+            if (w < nw[k]) m = fmaxf(m, lg[k][w]);
+        float e[W], sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            e[w] = 0.0f;
+            if (w < nw[k]) {
+                e[w] = expf(lg[k][w] - m);
+                sum += e[w];
+            }
+        }
+        const float inv_sum = 1.0f / sum;
+        float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            if (w < nw[k]) {
+                const float a = e[w] * inv_sum;
+                const float4 xv = half4_to_float4(xr[k][w]);
+                v[0] = fmaf(a, xv.x, v[0]);
+                v[1] = fmaf(a, xv.y, v[1]);
+                v[2] = fmaf(a, xv.z, v[2]);
+                v[3] = fmaf(a, xv.w, v[3]);
+            }
+        }
+
+        // ---- RMSNorm over the 128 dimensions
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = rsqrtf(ss * (1.0f / HEAD_DIM) + p.eps);
+        float y[4] = {v[0] * r * g.x, v[1] * r * g.y, v[2] * r * g.z, v[3] * r * g.w};
+
+        // ---- RoPE at position 4i: pairs (j, j + h) of the first rope_dim dims
+        float yp[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) yp[c] = __shfl_sync(0xffffffffu, y[c], src);
+        if (lo_half || hi_half) {
+            const float cc[4] = {cs[k].x, cs[k].y, cs[k].z, cs[k].w};
+            const float sc[4] = {sn[k].x, sn[k].y, sn[k].z, sn[k].w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                y[c] = lo_half ? y[c] * cc[c] - yp[c] * sc[c] : yp[c] * sc[c] + y[c] * cc[c];
+        }
+
+        // ---- store into the block's page slot
+        if (i >= p.rope_blocks || (i >> p.page_shift) >= p.max_pages) {
+            if (lane == 0) record_error(p.status, ST_BAD_ROW);
+            continue;
+        }
+        if (page[k] < 0 || page[k] >= p.num_pages) {
+            if (lane == 0) record_error(p.status, ST_BAD_PAGE);
+            continue;
+        }
+        const int64_t slot = static_cast<int64_t>(page[k]) * p.page_positions + (i & (p.page_positions - 1));
+        __half2 o0 = __floats2half2_rn(y[0], y[1]), o1 = __floats2half2_rn(y[2], y[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&o0);
+        u.y = *reinterpret_cast<uint32_t *>(&o1);
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(p.k_cache) + slot * HEAD_DIM + 4 * lane) = u;
     }
-    if (page < 0 || page >= p.num_pages) {
-        if (lane == 0) record_error(p.status, ST_BAD_PAGE);
-        return;
-    }
-    const int64_t slot = static_cast<int64_t>(page) * p.page_positions + (i & (p.page_positions - 1));
-    __half2 o0 = __floats2half2_rn(y[0], y[1]), o1 = __floats2half2_rn(y[2], y[3]);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t *>(&o0);
-    u.y = *reinterpret_cast<uint32_t *>(&o1);
-    *reinterpret_cast<uint2 *>(static_cast<__half *>(p.k_cache) + slot * HEAD_DIM + 4 * lane) = u;
 }
 
 // Row i: cos(4i * theta^(-2j / rope_dim)) for j < rope_dim / 2, then the sines;
@@ -170,10 +198,12 @@ __global__ void rope_table_kernel(float *__restrict__ table, int32_t n_blocks, i
 int launch_produce(const ProduceParams &p, int32_t max_tokens, void *stream)
 {
     const int32_t blocks_per_req = max_tokens / 4 + 2;
-    const dim3 grid((blocks_per_req + PROD_WARPS - 1) / PROD_WARPS, p.n_reqs);
+    const int kpw = p.window == 8 ? keys_per_warp<8>() : keys_per_warp<4>();
+    const dim3 grid((blocks_per_req + PROD_WARPS * kpw - 1) / (PROD_WARPS * kpw), p.n_reqs);
     void *args[] = {const_cast<ProduceParams *>(&p)};
-    return launch_kernel(reinterpret_cast<const void *>(&produce_kernel), grid, dim3(PROD_WARPS * 32), 0,
-                         static_cast<cudaStream_t>(stream), false, args);
+    const void *k = p.window == 8 ? reinterpret_cast<const void *>(&produce_kernel<8>)
+                                  : reinterpret_cast<const void *>(&produce_kernel<4>);
+    return launch_kernel(k, grid, dim3(PROD_WARPS * 32), 0, static_cast<cudaStream_t>(stream), false, args);
 }
 
 int launch_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream)
