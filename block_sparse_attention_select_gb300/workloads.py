@@ -280,3 +280,69 @@ PRODUCER_CONFIGS = {
     "context": producer_context,
     "chunk": producer_chunk,
 }
+
+
+# ------------------------------------------------------------------------
+# Inputs of the sparse-attention consumer (the step after the indexer): query
+# heads, raw K / V caches paged 64 tokens to a page through the index cache's
+# block table, and each row's selected index positions.  Random draws only.
+
+CONSUMER_Q_HEADS = 24
+CONSUMER_KV_HEADS = 2
+CONSUMER_HEAD_DIM = 256
+PAGE_TOKENS = PAGE_POSITIONS * COMPRESS_RATIO      # 64
+
+
+@dataclass
+class ConsumerInputs:
+    name: str
+    q: np.ndarray            # float16 [R, 24, 256]
+    k_cache: np.ndarray      # float16 [num_pages, 64, 2, 256]
+    v_cache: np.ndarray      # float16 [num_pages, 64, 2, 256]
+    block_table: np.ndarray  # int32 [num_reqs, max_pages]
+    row_req: np.ndarray      # int32 [R]
+    row_token: np.ndarray    # int32 [R] token position of each query row
+    sel: np.ndarray          # int32 [R, k] selected index positions (-1 = none)
+
+
+def make_consumer_inputs(name: str, *, seed: int, ctx_tokens, rows_per_req, k: int,
+                         all_selected_rows: int = 0) -> ConsumerInputs:
+    """Request b holds ctx_tokens[b] tokens; its last rows_per_req[b] tokens are
+    query rows.  Each row's selection is k distinct visible positions drawn at
+    random (all of them when fewer are visible); the first all_selected_rows
+    rows of request 0 select every visible position."""
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx_tokens, dtype=np.int64)
+    nreq = len(ctx)
+    pages_per_req = (ctx + PAGE_TOKENS - 1) // PAGE_TOKENS
+    max_pages = int(pages_per_req.max())
+    num_pages = int(pages_per_req.sum()) + 2
+    perm = rng.permutation(num_pages).astype(np.int32)
+    block_table = np.full((nreq, max_pages), -1, dtype=np.int32)
+    at = 0
+    for b in range(nreq):
+        n = int(pages_per_req[b])
+        block_table[b, :n] = perm[at:at + n]
+        at += n
+    shape = (num_pages, PAGE_TOKENS, CONSUMER_KV_HEADS, CONSUMER_HEAD_DIM)
+    k_cache = (rng.standard_normal(shape) * 0.5).astype(np.float16)
+    v_cache = rng.standard_normal(shape).astype(np.float16)
+    rows_req, rows_tok, sels = [], [], []
+    for b in range(nreq):
+        for t in range(int(ctx[b]) - int(rows_per_req[b]), int(ctx[b])):
+            v = (t + 1) // COMPRESS_RATIO
+            if b == 0 and len(rows_tok) < all_selected_rows or v <= k:
+                if v > k:
+                    raise ValueError("a row selecting every visible position needs k >= its visible count")
+                s = np.arange(v)
+            else:
+                s = np.sort(rng.choice(v, size=k, replace=False))
+            row = np.full(k, -1, dtype=np.int32)
+            row[:len(s)] = s[:k]
+            rows_req.append(b)
+            rows_tok.append(t)
+            sels.append(row)
+    R = len(rows_tok)
+    q = (rng.standard_normal((R, CONSUMER_Q_HEADS, CONSUMER_HEAD_DIM)) * 0.5).astype(np.float16)
+    return ConsumerInputs(name, q, k_cache, v_cache, block_table, np.array(rows_req, np.int32),
+                          np.array(rows_tok, np.int32), np.array(sels, np.int32).reshape(R, k))
