@@ -526,6 +526,98 @@ def run_produce(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+ATTEND_METRIC = "sparse-attention consumer rows/s (raw tokens of the selected positions, GQA 24/2 x 256) on 1 GB300"
+# FP32 FMA peak from the unit counts and the maximum SM clock: 152 SMs x 128
+# FP32 lanes x 2 FLOP x 2.07 GHz
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_attend(args, ws, rank, local):
+    import torch
+
+    from block_sparse_attention_select_gb300 import qsa
+
+    qsa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    # the prefill chunk of the indexer bench: 1,616 query rows at the end of a
+    # 184,320-token context, each attending its top-2,048 positions' raw tokens
+    inp = W.make_consumer_inputs("consumer_1616rows_ctx184320_k2048", seed=31, ctx_tokens=[184_320],
+                                 rows_per_req=[1616], k=2048)
+    R, hq, D = inp.q.shape
+    hkv = inp.k_cache.shape[2]
+    toks = sum(4 * int((row >= 0).sum()) + (int(t) + 1 - 4 * ((int(t) + 1) // 4))
+               for row, t in zip(inp.sel, inp.row_token))
+    flops = 4.0 * hq * D * toks                          # QK and PV, 2 FLOP per multiply-add
+    gathered = 2.0 * toks * hkv * D * 2                  # K and V lines read through the block table
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, kc, vc, bt = t(inp.q), t(inp.k_cache), t(inp.v_cache), t(inp.block_table)
+    rr, rt, sel = t(inp.row_req), t(inp.row_token), t(inp.sel)
+    out = torch.empty((R, hq, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qsa.sparse_attention(q, kc, vc, bt, rr, rt, sel, out=out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), ws)
+    achieved = flops / (ms / 1e3) / 1e12
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        from oracle import consumer as C
+        n_s = 4
+        t0 = time.perf_counter()
+        C.sparse_attention(inp.q[:n_s], inp.k_cache, inp.v_cache, inp.block_table, inp.row_req[:n_s],
+                           inp.row_token[:n_s], inp.sel[:n_s])
+        el = time.perf_counter() - t0
+        cpu = {"value": n_s / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"the first {n_s} rows of {R} (numpy float64, one thread), {el:.1f} s"}
+    line = {
+        "metric": ATTEND_METRIC, "value": R * ws / (ms / 1e3), "unit": "rows/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 in / f32 math / f32 out", "data": "synthetic",
+        "config": {"workload": inp.name, "rows": R, "q_heads": hq, "kv_heads": hkv, "head_dim": D, "k": 2048,
+                   "tokens_attended": toks, "gathered_gb": gathered / 1e9,
+                   "l2": "flushed between steps (512 MiB write)", "median_ms": statistics.median(step_ms)},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": ALU_FP32_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / ALU_FP32_TFLOPS, "traffic": None, "kernel": "attend", "kernel_ms": ms,
+                     "gathered_gb_per_s": gathered / (ms / 1e3) / 1e9,
+                     "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz"},
+        "cpu_baseline": cpu,
+        "e2e": None,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -536,14 +628,22 @@ def main():
     ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--op", choices=["select", "produce"], default="select",
-                    help="select: the indexer step (default); produce: the index-key producer")
+    ap.add_argument("--op", choices=["select", "produce", "attend"], default="select",
+                    help="select: the indexer step (default); produce: the index-key producer; "
+                         "attend: the sparse-attention consumer")
     ap.add_argument("--producer-workload", choices=sorted(W.PRODUCER_CONFIGS), default="context")
     ap.add_argument("--window", type=int, choices=[4, 8], default=4)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_setup()
-    if args.op == "produce":
+    if args.op == "attend":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the consumer's reference arm is the "
+                                  "oracle, reported as cpu_baseline in the attend line"}), flush=True)
+        else:
+            run_attend(args, ws, rank, local)
+    elif args.op == "produce":
         if args.impl == "reference":
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the producer's reference arm is the "

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqsa.so")
-SOURCES = ["qsa_api.cu", "qsa_plan.cu", "qsa_produce.cu", "qsa_score.cu", "qsa_select.cu"]
+SOURCES = ["qsa_api.cu", "qsa_attend.cu", "qsa_plan.cu", "qsa_produce.cu", "qsa_score.cu", "qsa_select.cu"]
 HEADERS = ["qsa_device.cuh", "qsa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

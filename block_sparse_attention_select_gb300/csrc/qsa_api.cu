@@ -368,6 +368,53 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
 
 int32_t qsa_last_launch_count(void) { return g_launches; }
 
+qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const void *k_cache, const void *v_cache,
+                                int32_t num_pages, int32_t page_tokens, int32_t hkv, int32_t head_dim,
+                                const int32_t *block_table, int32_t num_reqs, int32_t max_pages,
+                                const int32_t *row_req, const int32_t *row_token, const int32_t *sel, int32_t k,
+                                float scale, float *out, void *stream)
+{
+    g_launches = 0;
+    if (rows < 0 || k < 0 || hq < 1 || hkv < 1 || num_pages < 1 || num_reqs < 1 || max_pages < 1)
+        return QSA_ERR_INVALID_ARG;
+    if (head_dim != 256 || hq % hkv != 0 || hq / hkv > 16 || hkv > 65535) return QSA_ERR_UNSUPPORTED;
+    if (page_tokens < 8 || page_tokens > 256 || (page_tokens & (page_tokens - 1))) return QSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_pages) * page_tokens >= INT32_MAX ||
+        static_cast<int64_t>(num_pages) * page_tokens * hkv * 256 >= (int64_t{1} << 62))
+        return QSA_ERR_UNSUPPORTED;
+    if (!(scale > 0.0f) || !std::isfinite(scale)) return QSA_ERR_INVALID_ARG;
+    if (rows == 0) return QSA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !row_req || !row_token || !out || (k > 0 && !sel))
+        return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return QSA_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    qsa_status st = device_info(&d);
+    if (st != QSA_OK) return st;
+    AttendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.row_req = row_req;
+    p.row_token = row_token;
+    p.sel = sel;
+    p.out = out;
+    p.rows = rows;
+    p.hq = hq;
+    p.hkv = hkv;
+    p.k = k;
+    p.num_pages = num_pages;
+    p.page_tokens = page_tokens;
+    p.page_shift = log2_exact(page_tokens);
+    p.num_reqs = num_reqs;
+    p.max_pages = max_pages;
+    p.scale = scale;
+    p.status = d->status;
+    return launch_rc(launch_attend(p, stream));
+}
+
 qsa_status qsa_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream)
 {
     g_launches = 0;

@@ -148,6 +148,21 @@ struct ProduceParams {
     uint32_t *status;
 };
 
+// Sparse-attention consumer (the step after the indexer): see qsa_attend.cu.
+struct AttendParams {
+    const void *q;              // FP16 [rows, hq, 256]
+    const void *k_cache;        // FP16 [num_pages, page_tokens, hkv, 256]
+    const void *v_cache;        // same layout
+    const int32_t *block_table; // [num_reqs, max_pages]
+    const int32_t *row_req;     // [rows]
+    const int32_t *row_token;   // [rows]
+    const int32_t *sel;         // [rows, k] selected index positions, -1 = none
+    float *out;                 // FP32 [rows, hq, 256]
+    int32_t rows, hq, hkv, k, num_pages, page_tokens, page_shift, num_reqs, max_pages;
+    float scale;
+    uint32_t *status;
+};
+
 // Launchers (one translation unit each); return cudaError_t as int.  With
 // `overlap` the launch carries programmatic stream serialization: the kernel
 // may be scheduled while the previous kernel of the stream is still running
@@ -166,5 +181,6 @@ uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
 int launch_produce(const ProduceParams &p, int32_t max_tokens, void *stream);
 int launch_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream);
+int launch_attend(const AttendParams &p, void *stream);
 
 }  // namespace qsa

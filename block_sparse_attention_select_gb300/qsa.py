@@ -95,6 +95,9 @@ def load(path: str = LIB_PATH):
     lib.qsa_select_paged_tokens_noalloc.argtypes = [vp, vp, i32, i32, kp, vp, vp, i32, vp, vp, vp]
     lib.qsa_kernel_times.restype = ctypes.c_int
     lib.qsa_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i32), i32]
+    lib.qsa_sparse_attention.restype = ctypes.c_int
+    lib.qsa_sparse_attention.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, vp, i32, i32, vp, vp, vp, i32,
+                                         ctypes.c_float, vp, vp]
     lib.qsa_rope_table.restype = ctypes.c_int
     lib.qsa_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
     lib.qsa_index_key_produce.restype = ctypes.c_int
@@ -249,6 +252,29 @@ def index_key_produce(x, seq_start, pos_start, max_tokens: int, norm_weight, rop
                                       _ptr(rope_tab), rope_blocks, int(rope_dim), int(window),
                                       ctypes.byref(keys.c), _stream(stream))
     _check(st, "qsa_index_key_produce")
+
+
+def sparse_attention(q, k_cache, v_cache, block_table, row_req, row_token, sel, scale=None, out=None,
+                     stream=None):
+    """Each row attends the raw tokens of its selected index positions (and its
+    unfinished block): q FP16 [R, hq, 256]; caches FP16 [pages, page_tokens, hkv,
+    256]; block_table int32 [B, max_pages]; sel int32 [R, k].  Returns FP32
+    [R, hq, 256]."""
+    _need(q, torch.float16, "q"), _need(k_cache, torch.float16, "k_cache")
+    _need(v_cache, torch.float16, "v_cache"), _need(block_table, torch.int32, "block_table")
+    _need(row_req, torch.int32, "row_req"), _need(row_token, torch.int32, "row_token")
+    _need(sel, torch.int32, "sel")
+    R, hq, D = (int(x) for x in q.shape)
+    npg, pt, hkv = (int(x) for x in k_cache.shape[:3])
+    if out is None:
+        out = torch.empty((R, hq, D), dtype=torch.float32, device=q.device)
+    scale = 1.0 / (D ** 0.5) if scale is None else float(scale)
+    st = load().qsa_sparse_attention(_ptr(q), R, hq, _ptr(k_cache), _ptr(v_cache), npg, pt, hkv, D,
+                                     _ptr(block_table), int(block_table.shape[0]), int(block_table.shape[1]),
+                                     _ptr(row_req), _ptr(row_token), _ptr(sel), int(sel.shape[1]), scale,
+                                     _ptr(out), _stream(stream))
+    _check(st, "qsa_sparse_attention")
+    return out
 
 
 def get_device_status(stream=None) -> int:

@@ -159,6 +159,29 @@ qsa_status qsa_index_key_produce(const void *x, const float *pool_logit, int32_t
                                  int32_t rope_blocks, int32_t rope_dim, int32_t window,
                                  const qsa_paged_keys *keys, void *stream);
 
+/* ---- Sparse-attention consumer: the step after the indexer ----------------
+ * ("spec(MODEL-MM-QWEN4-EXP) ...", section "The component deep-dives": QSA
+ * attends raw tokens selected at ratio-4 granularity; plain GQA, 24 query
+ * heads over 2 KV heads, head_dim 256.)  This library's reading: row r, a
+ * query at token t of request b = row_req[r], attends the tokens 4j .. 4j+3 of
+ * every selected index position j = sel[r, 0..k) (as qsa_select_paged_tokens
+ * returns them: distinct, below V = (t+1)/4, -1 for none) and the tokens
+ * 4V .. t of its unfinished block; query head h reads KV head h / (hq / hkv);
+ *   out[r, h, :] = sum_s softmax_s(scale * q[r,h,:] . K[s]) * V[s]
+ * q: FP16 [rows, hq, 256]; k_cache, v_cache: FP16 [num_pages, page_tokens,
+ * hkv, 256], token p of request b at page block_table[b * max_pages + p /
+ * page_tokens], slot p % page_tokens; out: FP32 [rows, hq, 256]; q, the caches
+ * and out 16-byte aligned.  head_dim must be 256, hq / hkv <= 16, page_tokens a
+ * power of two in [8, 256].  Device-side problems (row_req out of range, a
+ * token past the block table, a selected position at or past V, a page id
+ * outside the cache) skip the token or the row and are reported by
+ * qsa_get_device_status(). */
+qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const void *k_cache, const void *v_cache,
+                                int32_t num_pages, int32_t page_tokens, int32_t hkv, int32_t head_dim,
+                                const int32_t *block_table, int32_t num_reqs, int32_t max_pages,
+                                const int32_t *row_req, const int32_t *row_token, const int32_t *sel, int32_t k,
+                                float scale, float *out, void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *qsa_status_string(qsa_status status);
 

@@ -137,3 +137,28 @@ def test_producer_host_checks(lib):
     assert r(None, 0, 64, 10000.0, None) == qsa.QSA_OK
     assert r(vp(20), 4, 64, 10000.0, None) == qsa.QSA_ERR_INVALID_ARG
     assert r(vp(16), 4, 64, 10000.0, None) == qsa.QSA_ERR_NO_DEVICE
+
+
+def test_consumer_host_checks(lib):
+    vp = ctypes.c_void_p
+    f = lib.qsa_sparse_attention
+
+    def call(**kw):
+        a = dict(q=vp(16), rows=2, hq=24, kc=vp(16), vc=vp(16), npg=4, pt=64, hkv=2, d=256, bt=vp(16), nr=1,
+                 mp=4, rr=vp(16), rt=vp(16), sel=vp(16), k=16, scale=0.0625, out=vp(16))
+        a.update(kw)
+        return f(a["q"], a["rows"], a["hq"], a["kc"], a["vc"], a["npg"], a["pt"], a["hkv"], a["d"], a["bt"],
+                 a["nr"], a["mp"], a["rr"], a["rt"], a["sel"], a["k"], a["scale"], a["out"], None)
+
+    assert call(d=128) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(hq=25) == qsa.QSA_ERR_UNSUPPORTED          # not a multiple of hkv
+    assert call(hq=34) == qsa.QSA_ERR_UNSUPPORTED          # 17 query heads per KV head
+    assert call(pt=48) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(scale=0.0) == qsa.QSA_ERR_INVALID_ARG
+    assert call(rows=-1) == qsa.QSA_ERR_INVALID_ARG
+    assert call(rows=0) == qsa.QSA_OK
+    assert call(q=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(sel=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(sel=None, k=0) == qsa.QSA_ERR_NO_DEVICE    # k = 0: only the unfinished block
+    assert call(out=vp(24)) == qsa.QSA_ERR_INVALID_ARG      # 16-byte alignment
+    assert call() == qsa.QSA_ERR_NO_DEVICE
