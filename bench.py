@@ -318,7 +318,7 @@ def run_ours(args, ws, rank, local):
         try:
             tr = json.load(open(tr_path))
             ent = tr.get(wl.name, {}).get(dom_name)
-            if ent and ent.get("kernel_rev") == kernel_revision():
+            if ent and ent.get("kernel_rev") == kernel_revision(dom_name):
                 roof_traffic = ent["bytes_per_launch"]
         except Exception:
             roof_traffic = None
@@ -359,11 +359,22 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def kernel_revision():
+# the sources each measured kernel is compiled from: its own file and the
+# shared headers (a change anywhere else leaves its recorded traffic valid)
+KERNEL_SOURCES = {
+    "score": ("qsa_score.cu", "qsa_device.cuh", "qsa_internal.h"),
+    "select": ("qsa_select.cu", "qsa_device.cuh", "qsa_internal.h"),
+    "produce": ("qsa_produce.cu", "qsa_device.cuh", "qsa_internal.h"),
+}
+
+
+def kernel_revision(kernel: str) -> str:
+    """Hash of the sources of `kernel` (a kernel-times name such as
+    score_filter or select_cand, or produce)."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "block_sparse_attention_select_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel.split("_")[0]]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -501,7 +512,7 @@ def run_produce(args, ws, rank, local):
     if os.path.exists(tr_path):
         try:
             ent = json.load(open(tr_path)).get(f"{inp.name}_w{inp.window}", {}).get("produce")
-            if ent and ent.get("kernel_rev") == kernel_revision():
+            if ent and ent.get("kernel_rev") == kernel_revision("produce"):
                 traffic = ent["bytes_per_launch"]
         except Exception:
             traffic = None
