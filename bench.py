@@ -372,9 +372,12 @@ def kernel_revision(kernel: str) -> str:
     """Hash of the sources of `kernel` (a kernel-times name such as
     score_filter or select_cand, or produce)."""
     import hashlib
+    files = KERNEL_SOURCES.get(kernel.split("_")[0])
+    if files is None:
+        return ""                                         # no recorded traffic for this kernel
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "block_sparse_attention_select_gb300", "csrc")
-    for f in KERNEL_SOURCES[kernel.split("_")[0]]:
+    for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:12]
 
