@@ -346,3 +346,55 @@ def make_consumer_inputs(name: str, *, seed: int, ctx_tokens, rows_per_req, k: i
     q = (rng.standard_normal((R, CONSUMER_Q_HEADS, CONSUMER_HEAD_DIM)) * 0.5).astype(np.float16)
     return ConsumerInputs(name, q, k_cache, v_cache, block_table, np.array(rows_req, np.int32),
                           np.array(rows_tok, np.int32), np.array(sels, np.int32).reshape(R, k))
+
+
+# ------------------------------------------------------------------------
+# Inputs of the second workload, the M3-style block scorer: per-head index
+# queries and per-token, per-head index keys paged 128 tokens to a page.
+# Random draws only.
+
+SCORER_BLOCK = 128
+
+
+@dataclass
+class BlockScorerInputs:
+    name: str
+    q: np.ndarray            # float16 [R, H, 128]
+    k_cache: np.ndarray      # float16 [num_pages, 128, H, 128]
+    block_table: np.ndarray  # int32 [num_reqs, max_pages]
+    row_req: np.ndarray      # int32 [R]
+    row_token: np.ndarray    # int32 [R]
+    k: int
+
+
+def make_block_scorer_inputs(name: str, *, seed: int, ctx_tokens, rows_per_req, k: int, heads: int = 2,
+                             dist: str = "gauss") -> BlockScorerInputs:
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx_tokens, dtype=np.int64)
+    nreq = len(ctx)
+    pages_per_req = (ctx + SCORER_BLOCK - 1) // SCORER_BLOCK
+    num_pages = int(pages_per_req.sum()) + 2
+    perm = rng.permutation(num_pages).astype(np.int32)
+    block_table = np.full((nreq, int(pages_per_req.max())), -1, dtype=np.int32)
+    at = 0
+    for b in range(nreq):
+        n = int(pages_per_req[b])
+        block_table[b, :n] = perm[at:at + n]
+        at += n
+    shape = (num_pages, SCORER_BLOCK, heads, HEAD_DIM)
+    if dist == "int":
+        k_cache = rng.integers(-2, 3, size=shape).astype(np.float16)
+    else:
+        k_cache = (rng.standard_normal(shape) / np.sqrt(HEAD_DIM)).astype(np.float16)
+    rows_req, rows_tok = [], []
+    for b in range(nreq):
+        for t in range(int(ctx[b]) - int(rows_per_req[b]), int(ctx[b])):
+            rows_req.append(b)
+            rows_tok.append(t)
+    R = len(rows_tok)
+    if dist == "int":
+        q = rng.integers(-2, 3, size=(R, heads, HEAD_DIM)).astype(np.float16)
+    else:
+        q = rng.standard_normal((R, heads, HEAD_DIM)).astype(np.float16)
+    return BlockScorerInputs(name, q, k_cache, block_table, np.array(rows_req, np.int32),
+                             np.array(rows_tok, np.int32), k)
