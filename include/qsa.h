@@ -28,9 +28,10 @@
  *    out of time) never trap: the kernels record them in a per-device status
  *    word and carry on with safe values.  qsa_get_device_status() reads and
  *    clears that word.
- *  - Supported shapes: head_dim == 128, H in {1, 2, 4, 8}, page_positions a
- *    power of two in [8, 256], 0 <= k <= QSA_MAX_K.  k may exceed V_r.  Others
- *    return QSA_ERR_UNSUPPORTED.  q and k_cache must be 16-byte aligned.
+ *  - Supported shapes of the indexer calls: head_dim == 128, H in {1, 2, 4,
+ *    8}, page_positions a power of two in [8, 256], 0 <= k <= QSA_MAX_K.  k may
+ *    exceed V_r.  Others return QSA_ERR_UNSUPPORTED.  q and k_cache must be
+ *    16-byte aligned.  The producer and the consumer (below) state their own.
  *  - Output of the top-k: out_idx[r, 0:min(k, V_r)] holds positions in
  *    (score desc, position asc) order and -1 after that; out_val (optional,
  *    may be NULL) holds the matching logits and -inf after that.
