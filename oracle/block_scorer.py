@@ -13,7 +13,7 @@ ReLU and no reduction over heads; index heads equal KV heads, so each query
 token gets one block set per KV head; the block is 128 tokens, the KV page
 size; a bitonic top-k picks the blocks.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings taken where the pages are silent:
   * a query at token t sees the tokens 0 .. t; a block counts when it holds at
     least one of them, and its score is the maximum over those only;
   * the top-k is ordered by score descending, the lower block index first on

@@ -13,7 +13,7 @@ pooled key and value, and not whole pages); and, where the same page sets QSA
 beside MiniMax-M3 in its op survey, its attention is plain GQA, 24 query heads
 over 2 KV heads, head_dim 256.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings taken where the pages are silent:
   * row r, a query at token t_r of request b, attends the tokens 4j .. 4j + 3
     of every selected position j (the indexer's output, -1 entries ignored,
     duplicates counted once) and the tokens 4 V_r .. t_r of its current,

@@ -17,7 +17,7 @@ block-start position; the same section notes that the DSv4 compress kernel is
 not a mean pool but a learned softmax pool over an overlapping window of eight
 tokens, driven by a score channel the QSA checkpoint does not have.
 
-Readings where the pages are silent (each listed in the design notes):
+Readings taken where the pages are silent:
   * pool: weights softmax(pool_logit) over the window's tokens, or equal
     weights (the mean) when no logits are given; window W = 4 (the block) or 8
     (the block and the four tokens before it), clipped at position 0;
