@@ -225,7 +225,7 @@ qsa_status check_keys(const qsa_paged_keys *keys)
     if (P < 8 || P > 256 || (P & (P - 1)) != 0) return QSA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(keys->num_pages) * P >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(keys->max_pages_per_req) * P >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
-    if (!aligned(keys->k_cache, 16)) return QSA_ERR_INVALID_ARG;
+    if (!aligned(keys->k_cache, 16) || !aligned(keys->block_table, 4)) return QSA_ERR_INVALID_ARG;
     return QSA_OK;
 }
 
@@ -309,6 +309,8 @@ qsa_status check_common(const void *q, const float *w, int32_t rows, int32_t H,
     if (!supported_heads(H)) return QSA_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(rows) * H >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
     if (!aligned(q, 16)) return QSA_ERR_INVALID_ARG;
+    // every int32 / float array is read element by element: 4-byte aligned
+    if (!aligned(w, 4) || !aligned(row_req, 4) || !aligned(row_visible, 4)) return QSA_ERR_INVALID_ARG;
     return check_keys(keys);
 }
 
@@ -388,6 +390,8 @@ qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const v
         return QSA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
         return QSA_ERR_INVALID_ARG;
+    if (!aligned(block_table, 4) || !aligned(row_req, 4) || !aligned(row_token, 4) || !aligned(sel, 4))
+        return QSA_ERR_INVALID_ARG;
     DeviceInfo *d = nullptr;
     qsa_status st = device_info(&d);
     if (st != QSA_OK) return st;
@@ -446,6 +450,7 @@ qsa_status qsa_index_key_produce(const void *x, const float *pool_logit, int32_t
     if (n_reqs > keys->num_reqs || n_reqs > 65535) return QSA_ERR_UNSUPPORTED;
     if (!x || !seq_start || !pos_start || !norm_weight) return QSA_ERR_INVALID_ARG;
     if (!aligned(x, 8) || !aligned(norm_weight, 16)) return QSA_ERR_INVALID_ARG;
+    if (!aligned(pool_logit, 4) || !aligned(seq_start, 4) || !aligned(pos_start, 4)) return QSA_ERR_INVALID_ARG;
     if (rope_dim > 0 && (!rope_table || !aligned(rope_table, 16))) return QSA_ERR_INVALID_ARG;
     DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != QSA_OK) return st;
@@ -519,7 +524,7 @@ qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t 
     g_launches = 0;
     qsa_status st = check_common(q, w, rows, H, keys, row_req, row_visible);
     if (st != QSA_OK) return st;
-    if (!logits || ld_logits < 1) return QSA_ERR_INVALID_ARG;
+    if (!logits || ld_logits < 1 || !aligned(logits, 4)) return QSA_ERR_INVALID_ARG;
     if (rows == 0) return QSA_OK;
     DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != QSA_OK) return st;
@@ -553,6 +558,8 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
     if (k > QSA_MAX_K) return QSA_ERR_UNSUPPORTED;
     if (rows == 0 || k == 0) return QSA_OK;
     if (!logits || !row_visible || !out_idx) return QSA_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(row_visible, 4) || !aligned(out_idx, 4) || !aligned(out_val, 4))
+        return QSA_ERR_INVALID_ARG;
     if (ld_logits > INT32_MAX) return QSA_ERR_UNSUPPORTED;
     DeviceInfo *d = nullptr;
     qsa_status st = device_info(&d);
@@ -585,6 +592,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     if (k < 0) return QSA_ERR_INVALID_ARG;
     if (k > QSA_MAX_K) return QSA_ERR_UNSUPPORTED;
     if (!out_idx) return QSA_ERR_INVALID_ARG;
+    if (!aligned(out_idx, 4) || !aligned(out_val, 4)) return QSA_ERR_INVALID_ARG;
     if (rows == 0 || k == 0) return QSA_OK;
     DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != QSA_OK) return st;

@@ -23,6 +23,8 @@
  *    stream).  Every call is asynchronous on that stream.
  *  - Host-side argument checks run before any launch and return a status;
  *    nothing is launched when a check fails.  No C++ exception crosses the ABI.
+ *    Every int32 / FP32 array must be 4-byte aligned (QSA_ERR_INVALID_ARG
+ *    otherwise); stricter alignments are stated where they apply.
  *  - Errors found on the device (bad page id, row_req out of range, a row
  *    longer than the block table or the logit row, a pipeline wait that ran
  *    out of time) never trap: the kernels record them in a per-device status

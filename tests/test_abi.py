@@ -162,3 +162,26 @@ def test_consumer_host_checks(lib):
     assert call(sel=None, k=0) == qsa.QSA_ERR_NO_DEVICE    # k = 0: only the unfinished block
     assert call(out=vp(24)) == qsa.QSA_ERR_INVALID_ARG      # 16-byte alignment
     assert call() == qsa.QSA_ERR_NO_DEVICE
+
+
+def test_misaligned_arrays_are_rejected_on_the_host(lib):
+    """Every int32 / float array is read element by element on the device; a
+    pointer that is not 4-byte aligned is refused before any launch."""
+    for name in ("w", "row_req", "row_visible", "out_idx"):
+        assert _call_select(lib, **{name: 18}) == qsa.QSA_ERR_INVALID_ARG, name
+    assert _call_select(lib, out_val=18) == qsa.QSA_ERR_INVALID_ARG
+    bad_table = qsa.PagedKeysC(16, 4, 16, 128, 18, 1, 4)
+    assert _call_select(lib, keys=ctypes.byref(bad_table)) == qsa.QSA_ERR_INVALID_ARG
+    vp = ctypes.c_void_p
+    f = lib.qsa_topk_exact
+    assert f(vp(18), 10, 4, vp(16), 4, vp(16), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
+    assert f(vp(16), 10, 4, vp(16), 4, vp(18), None, None, 0, None) == qsa.QSA_ERR_INVALID_ARG
+    keys = qsa.PagedKeysC(16, 4, 16, 128, 16, 1, 4)
+    p = lib.qsa_index_key_produce
+    for pl, ss, ps in ((vp(18), vp(16), vp(16)), (None, vp(18), vp(16)), (None, vp(16), vp(18))):
+        assert p(vp(16), pl, 1, ss, ps, 8, vp(16), 1e-6, vp(16), 4, 64, 4, ctypes.byref(keys), None) \
+            == qsa.QSA_ERR_INVALID_ARG
+    a = lib.qsa_sparse_attention
+    for bt, rr, rt, sel in ((18, 16, 16, 16), (16, 18, 16, 16), (16, 16, 18, 16), (16, 16, 16, 18)):
+        assert a(vp(16), 2, 24, vp(16), vp(16), 4, 64, 2, 256, vp(bt), 1, 4, vp(rr), vp(rt), vp(sel), 16,
+                 0.0625, vp(16), None) == qsa.QSA_ERR_INVALID_ARG
