@@ -74,17 +74,65 @@ def algorithmic(wl):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """SM clock and throttle-reason samples taken while the timed region runs.
+
+    Reads NVML through ctypes every ~0.5 ms from a background thread (the
+    timed region of a short run lasts a few milliseconds); falls back to
+    nvidia-smi at 200 ms where libnvidia-ml cannot be loaded.  Read-only:
+    no clock or other GPU setting is changed."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clocks-event-reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index):
         self.index = index
         self.proc = None
         self.lines = []
+        self.nvml = None
+        self.samples = []
+        self.stop_flag = threading.Event()
+
+    def _nvml_open(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return None
+        return lib, h
+
+    def _poll(self):
+        import ctypes
+        lib, h = self.nvml
+        mhz, mx, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_flag.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0            # NVML_CLOCK_SM
+            ok = ok and lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
+            ok = ok and get_reasons(h, ctypes.byref(reasons)) == 0
+            if ok:
+                self.samples.append((mhz.value, mx.value, reasons.value))
+            time.sleep(0.0005)
 
     def start(self):
+        try:
+            self.nvml = self._nvml_open()
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
@@ -100,6 +148,19 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag.set()
+            self.t.join(timeout=2)
+            if not self.samples:
+                return None
+            reasons = set()
+            for _, _, bits in self.samples:
+                for bit, name in self.REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                    "sm_max_mhz": max(s[1] for s in self.samples), "reasons": sorted(reasons),
+                    "samples": len(self.samples), "source": "nvml, every ~0.5 ms"}
         if not self.proc:
             return None
         self.proc.terminate()
@@ -124,7 +185,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi, every 200 ms"}
 
 
 def dist_setup():
@@ -416,13 +477,25 @@ def measure_e2e(args, wl, qsa, keys_dev, stream, dev):
 PRODUCE_METRIC = "index-key producer keys/s (pool + RMSNorm + RoPE + paged store) on 1 GB300"
 
 
+def keys_written(pos_start: int, n_tokens: int, window: int) -> int:
+    """Index keys one request's call stores: the blocks of four tokens that end
+    among the new tokens [pos_start, pos_start + n_tokens) and whose pooling
+    window, clipped at position 0, starts at or after pos_start."""
+    first = (pos_start + 3) // 4                  # first block ending at or after pos_start
+    last = (pos_start + n_tokens) // 4 - 1        # last block ending before the end
+    n = 0
+    for i in range(first, last + 1):
+        if max(0, 4 * i + 4 - window) >= pos_start:
+            n += 1
+    return n
+
+
 def produce_bytes(inp):
     """Algorithmic bytes of one producer call: every token key (and pooling
     logit) read once, per stored key its RoPE table row, its block-table entry
     and the 256-byte FP16 key written."""
-    from oracle import producer as P  # noqa: F401  (block count only)
-    nkeys = sum(len(P.produced_blocks(int(inp.pos_start[b]), int(inp.seq_start[b + 1] - inp.seq_start[b]),
-                                      inp.window)) for b in range(len(inp.pos_start)))
+    nkeys = sum(keys_written(int(inp.pos_start[b]), int(inp.seq_start[b + 1] - inp.seq_start[b]), inp.window)
+                for b in range(len(inp.pos_start)))
     read = inp.tokens * 256 + (inp.tokens * 4 if inp.pool_logit is not None else 0)
     per_key = inp.rope_dim * 4 + 4 + 256
     return nkeys, read + nkeys * per_key

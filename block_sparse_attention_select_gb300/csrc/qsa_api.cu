@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -31,16 +32,18 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-int64_t g_cfg_path = 0;
-bool g_overlap = true;          // dependent launches inside a call (QSA_CFG_OVERLAP)
-uint64_t g_wait_ns = 2000000000ull;
+// process-wide switches (qsa_set_config); atomics, so that a switch set on one
+// host thread is read whole on another
+std::atomic<int64_t> g_cfg_path{0};
+std::atomic<bool> g_overlap{true};          // dependent launches inside a call (QSA_CFG_OVERLAP)
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
 thread_local int32_t g_launches = 0;
 
 // Optional per-launch CUDA-event timing (test / benchmark instrument).
 enum Kind { K_PLAN = 0, K_SCORE_LOGITS, K_SCORE_SAMPLE, K_SCORE_FILTER, K_SCORE_FALLBACK,
             K_SEL_DENSE, K_SEL_THRESH, K_SEL_CAND, K_SEL_FLAGGED, K_PAD, K_KINDS };
 struct Pending { cudaEvent_t a, b; int kind; };
-bool g_timing = false;
+std::atomic<bool> g_timing{false};
 std::vector<Pending> g_pending;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -146,7 +149,8 @@ FilterShape filter_shape(int64_t max_len, int32_t k)
     f.stride = std::max(1, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
     // candidates the selector holds (~1.5 k expected); a multiple of 4 so that
     // the selector's arrays after the cap-sized one stay 16-byte aligned
-    f.cap = (std::max(2 * k + 256, k + 512) + 3) / 4 * 4;
+    const int64_t k64 = k;
+    f.cap = static_cast<int32_t>((std::max<int64_t>(2 * k64 + 256, k64 + 512) + 3) / 4 * 4);
     const int64_t tiles = (max_len + TILE_M - 1) / TILE_M;
     f.sample_ld = std::max<int64_t>(TILE_M, (tiles + f.stride - 1) / f.stride * TILE_M);
     return f;
@@ -318,11 +322,11 @@ qsa_status check_common(const void *q, const float *w, int32_t rows, int32_t H,
 
 extern "C" {
 
-size_t qsa_workspace_bytes(int32_t rows, int32_t max_visible, int32_t k, int32_t flags)
+size_t qsa_workspace_bytes(int32_t rows, int32_t row_capacity, int32_t k, int32_t flags)
 {
     (void)flags;
     if (rows <= 0) return 256;
-    const int64_t ld = std::max<int64_t>(8, (static_cast<int64_t>(std::max(max_visible, 0)) + 7) / 8 * 8);
+    const int64_t ld = std::max<int64_t>(8, (static_cast<int64_t>(std::max(row_capacity, 0)) + 7) / 8 * 8);
     return layout(rows, ld, std::max(k, 1)).total;
 }
 
@@ -712,10 +716,15 @@ extern "C" qsa_status qsa_select_paged_tokens_noalloc(const void *q, const float
     g_launches = 0;
     if (!keys || keys->max_pages_per_req < 1 || keys->page_positions < 1 || rows < 0 || k < 0)
         return QSA_ERR_INVALID_ARG;
+    if (k > QSA_MAX_K) return QSA_ERR_UNSUPPORTED;
     const int64_t ld = static_cast<int64_t>(keys->max_pages_per_req) * keys->page_positions;
     if (ld > INT32_MAX) return QSA_ERR_UNSUPPORTED;
     const size_t need = qsa_workspace_bytes(rows, static_cast<int32_t>(ld), k, 0);
     if (need > QSA_STATIC_SCRATCH_BYTES) return QSA_ERR_STATIC_LIMIT;
+    // the same device check as every other entry point, before the symbol lookup
+    DeviceInfo *info = nullptr;
+    qsa_status dst = device_info(&info);
+    if (dst != QSA_OK) return dst;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
         cudaGetLastError();

@@ -14,6 +14,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -566,15 +568,20 @@ template <int H>
 int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *tk128, int grid, bool overlap,
              cudaStream_t s)
 {
+    // once per device (calls from several host threads may race here)
+    static std::mutex mu;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
-    if (!attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(score_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(SMEM_BYTES));
-        if (e != cudaSuccess) return static_cast<int>(e);
-        attr_done[dev] = true;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(score_kernel<H>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(SMEM_BYTES));
+            if (e != cudaSuccess) return static_cast<int>(e);
+            attr_done[dev] = true;
+        }
     }
     void *args[] = {const_cast<void *>(tq), const_cast<void *>(tk), const_cast<void *>(tk128),
                     const_cast<ScoreParams *>(&p)};

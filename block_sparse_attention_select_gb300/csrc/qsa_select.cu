@@ -12,6 +12,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -1097,12 +1099,17 @@ size_t select_smem_bytes(int32_t smem_cap)
 
 namespace {
 
+// serialises the attribute updates of the kernels below (callers on several
+// host threads)
+std::mutex g_attr_mu;
+
 template <typename K>
 int set_smem(K kernel, size_t smem, size_t (&done)[64])
 {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
     if (smem > done[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));

@@ -153,12 +153,12 @@ class PagedKeys:
         return int(self.block_table.shape[1]) * int(self.k_cache.shape[1])
 
 
-def workspace_bytes(rows: int, max_visible: int, k: int, flags: int = 0) -> int:
-    return int(load().qsa_workspace_bytes(int(rows), int(max_visible), int(k), int(flags)))
+def workspace_bytes(rows: int, row_capacity: int, k: int, flags: int = 0) -> int:
+    return int(load().qsa_workspace_bytes(int(rows), int(row_capacity), int(k), int(flags)))
 
 
-def alloc_workspace(rows: int, max_visible: int, k: int, device=None) -> torch.Tensor:
-    n = workspace_bytes(rows, max_visible, k)
+def alloc_workspace(rows: int, row_capacity: int, k: int, device=None) -> torch.Tensor:
+    n = workspace_bytes(rows, row_capacity, k)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 

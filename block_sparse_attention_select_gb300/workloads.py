@@ -74,6 +74,12 @@ def _weights(rng: np.random.Generator, shape, dist: str) -> np.ndarray:
         return rng.random(size=shape, dtype=np.float32)
     if dist == "zero":
         return np.zeros(shape, dtype=np.float32)
+    if dist == "int4_signed":
+        # dyadic magnitudes with either sign: integer-valued scores stay exact
+        mag = rng.choice(np.array([0.25, 0.5, 1.0, 2.0], dtype=np.float32), size=shape)
+        return np.where(rng.random(size=shape) < 0.5, -mag, mag).astype(np.float32)
+    if dist == "gauss_signed":
+        return (2.0 * rng.random(size=shape, dtype=np.float32) - 1.0).astype(np.float32)
     raise ValueError(dist)
 
 

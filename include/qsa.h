@@ -30,6 +30,10 @@
  *    out of time) never trap: the kernels record them in a per-device status
  *    word and carry on with safe values.  qsa_get_device_status() reads and
  *    clears that word.
+ *  - The library keeps per-device state for the life of the process (the
+ *    device address of its status word and of its static scratch buffer,
+ *    kernel attributes).  A device reset (cudaDeviceReset) invalidates it: do
+ *    not call the library on a device after resetting it.
  *  - Supported shapes of the indexer calls: head_dim == 128, H in {1, 2, 4,
  *    8}, page_positions a power of two in [8, 256], 0 <= k <= QSA_MAX_K.  k may
  *    exceed V_r.  Others return QSA_ERR_UNSUPPORTED.  q and k_cache must be
@@ -75,11 +79,14 @@ typedef struct {
     int32_t        max_pages_per_req;  /* row stride of block_table; V_r <= max_pages_per_req * page_positions */
 } qsa_paged_keys;
 
-/* Bytes of device workspace the calls below need for `rows` query rows whose
- * visible lengths are at most `max_visible` and a top-k of `k`.  For
- * qsa_select_paged_tokens pass max_visible = max_pages_per_req * page_positions.
- * `flags` is reserved (pass 0).  Host only; no device is touched. */
-size_t qsa_workspace_bytes(int32_t rows, int32_t max_visible, int32_t k, int32_t flags);
+/* Bytes of device workspace the calls below need for `rows` query rows, a
+ * top-k of `k` and rows of up to `row_capacity` positions.  row_capacity is
+ * the longest row the block table can address, max_pages_per_req *
+ * page_positions, NOT the longest visible length of the batch: the workspace
+ * is laid out by the block table's capacity.  qsa_index_score needs the size
+ * for (rows, 1, 1); qsa_topk_exact needs none.  `flags` is reserved (pass 0).
+ * Host only; no device is touched. */
+size_t qsa_workspace_bytes(int32_t rows, int32_t row_capacity, int32_t k, int32_t flags);
 
 /* Index scores only: logits[r * ld_logits + j] for 0 <= j < ld_logits, FP32,
  * row-major; -inf for j >= V_r.  q: FP16 [rows, H, 128]; w: FP32 [rows, H];

@@ -16,10 +16,13 @@
  *    section "Purpose": FP16 operands with FP32 accumulation, and an *exact*
  *    lexicographic top-k with a deterministic tie rule (a non-exact selector
  *    "can pick a different block set when scores tie at the cutoff").
- *  - The per-head weighting logit = sum_h w[r,h] * ReLU(q[r,h] . k[j]) and the
- *    tie order (higher score first, lower position index on equal scores) are
- *    the plainest reading of the above; see the readings list in the design
- *    notes.
+ *  - The pages do not spell out how the heads are weighted or which of two
+ *    equal scores wins.  Readings taken: ReLU per head first, then the
+ *    per-row head weight, then the sum over the heads in order h = 0 .. H-1
+ *    (logit = sum_h w[r,h] * ReLU(q[r,h] . k[j]); w may be any finite value,
+ *    1/sqrt(head_dim) folded into it by the caller); the higher score first
+ *    and, on equal scores, the lower position index; -0 and +0 are equal
+ *    scores; positions j >= V_r are never candidates (their logits are -inf).
  *
  * Arithmetic: IEEE binary32, multiply then add in a fixed order, no fused
  * multiply-add (the build passes -ffp-contract=off).  Products of two binary16

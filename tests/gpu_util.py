@@ -70,6 +70,16 @@ def check_sorted_valid(idx, val, vis, k):
         assert np.all(np.diff(sel.astype(np.int64))[ties] > 0), r
 
 
+def assert_values_at_selection(g_idx, g_val, o_logits_rows):
+    """Each returned value is the oracle's logit at the returned position,
+    within the logit tolerance (padding excluded)."""
+    sel = g_idx >= 0
+    o = np.take_along_axis(o_logits_rows, np.where(sel, g_idx, 0).astype(np.int64), axis=1)
+    o, g = o.astype(np.float64), g_val.astype(np.float64)
+    bad = sel & (np.abs(g - o) > RTOL * np.abs(o) + ATOL)
+    assert not np.any(bad), (np.argwhere(bad)[:5], g[bad][:5], o[bad][:5])
+
+
 def near_tie_disagreement(g_idx, o_idx, o_logits_rows, vis, k):
     """Rows compared as sets; every position in the symmetric difference must
     score within tolerance of the oracle's k-th score.  Returns the

@@ -16,7 +16,7 @@ import torch
 from block_sparse_attention_select_gb300 import qsa
 from block_sparse_attention_select_gb300 import workloads as W
 
-from gpu_util import ATOL, RTOL, to_device
+from gpu_util import to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -41,23 +41,56 @@ def _noalloc(lib, d, wl, k):
     return oi.cpu().numpy(), ov.cpu().numpy()
 
 
-@pytest.mark.parametrize("which", ["tiny", "gauss"])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, which):
-    if which == "tiny":
-        wl = W.tiny()
-    else:
-        wl = W.make_workload("noalloc", seed=31, ctx_tokens=[20000, 9000], rows_per_req=[40, 24],
-                             k=256)
+def _workspace_call(d, wl, path):
+    qsa.set_config(qsa.QSA_CFG_PATH, path)
+    try:
+        ri, rv = qsa.select_paged_tokens(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"], wl.k)
+    finally:
+        qsa.set_config(qsa.QSA_CFG_PATH, qsa.PATH_AUTO)
+    return ri.cpu().numpy(), rv.cpu().numpy()
+
+
+def _noalloc_on_path(lib, d, wl, path):
+    qsa.set_config(qsa.QSA_CFG_PATH, path)
+    try:
+        return _noalloc(lib, d, wl, wl.k)
+    finally:
+        qsa.set_config(qsa.QSA_CFG_PATH, qsa.PATH_AUTO)
+
+
+def test_noalloc_tiny_matches_oracle(lib):
+    import oracle
+    wl = W.tiny()
     d = to_device(wl)
-    ri, rv = qsa.select_paged_tokens(d["q"], d["w"], d["keys"], d["row_req"], d["row_visible"],
-                                     wl.k)
-    ri, rv = ri.cpu().numpy(), rv.cpu().numpy()
-    for _ in range(2):
-        gi, gv = _noalloc(lib, d, wl, wl.k)
-        np.testing.assert_array_equal(gi, ri)
-        fin = np.isfinite(rv)
-        np.testing.assert_array_equal(np.isfinite(gv), fin)
-        np.testing.assert_allclose(gv[fin], rv[fin], rtol=RTOL, atol=ATOL)
+    oi, ov, _ = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                           wl.row_visible, wl.k, ld=wl.ld)
+    for path in (qsa.PATH_AUTO, qsa.PATH_FILTER):
+        for _ in range(2):
+            gi, gv = _noalloc_on_path(lib, d, wl, path)
+            np.testing.assert_array_equal(gi, oi)
+            np.testing.assert_array_equal(gv, ov)
+    assert qsa.get_device_status() == qsa.QSA_OK
+
+
+# Two different batches in turn, each twice: the shared buffer then holds the
+# other batch's (or the same batch's) leftovers when a call starts.  "long"
+# takes the sampled-threshold filter path on its own (7,500 positions, k 512);
+# "short" (fewer rows and positions) is run on both paths.
+_BATCHES = {
+    "long": dict(seed=31, ctx_tokens=[30000], rows_per_req=[100], k=512),
+    "short": dict(seed=32, ctx_tokens=[20000, 9000], rows_per_req=[40, 24], k=256),
+}
+
+
+@pytest.mark.parametrize("path", [qsa.PATH_AUTO, qsa.PATH_FILTER, qsa.PATH_DENSE])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(lib, path):
+    wls = {n: W.make_workload(f"noalloc_{n}", **kw) for n, kw in _BATCHES.items()}
+    devs = {n: to_device(wl) for n, wl in wls.items()}
+    want = {n: _workspace_call(devs[n], wl, path) for n, wl in wls.items()}
+    for n in ("long", "short", "long", "short", "short"):
+        gi, gv = _noalloc_on_path(lib, devs[n], wls[n], path)
+        np.testing.assert_array_equal(gi, want[n][0])        # same kernels, same inputs: bit for bit
+        np.testing.assert_array_equal(gv, want[n][1])
     assert qsa.get_device_status() == qsa.QSA_OK
 
 
