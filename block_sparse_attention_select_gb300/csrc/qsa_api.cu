@@ -162,9 +162,7 @@ int64_t cand_tiles_ld(int64_t ld) { return ((ld + TILE_M - 1) / TILE_M + 7) / 8 
 
 bool use_filter(int32_t rows, int64_t max_len, int32_t k)
 {
-    // the filter scorer addresses the candidate slots (4 planes) with 32-bit
-    // offsets from a group's plane-0 run
-    if (static_cast<int64_t>(rows) * cand_tiles_ld(max_len) * 4 * CAND_SLOTS >= (int64_t{1} << 32)) return false;
+    (void)rows;
     if (g_cfg_path == 1) return false;
     if (g_cfg_path == 2) return true;
     const FilterShape f = filter_shape(max_len, k);
@@ -172,11 +170,15 @@ bool use_filter(int32_t rows, int64_t max_len, int32_t k)
 }
 
 struct Layout {
-    size_t plan, row_vis, groups, item_prefix, sample_prefix, logits, sample, tau, flag, cand_mask, cand_score;
+    size_t plan, row_vis, groups, item_prefix, sample_prefix, scores, sample, tau, flag, cand_mask;
     size_t total;
 };
 
-Layout layout(int32_t R, int64_t ld, int32_t k)
+// Workspace regions (256-byte aligned).  `scores` holds either the dense
+// logits [R, ld] (dense path) or the candidate slots [tiles_ld, R, 128] of the
+// filter path (a call uses one of the two), sized for the larger; the
+// score-only call needs none of it.
+Layout layout(int32_t R, int64_t ld, int32_t k, bool with_scores = true)
 {
     Layout L{};
     size_t o = 0;
@@ -186,14 +188,15 @@ Layout layout(int32_t R, int64_t ld, int32_t k)
     L.groups = take(sizeof(Group) * R);
     L.item_prefix = take(sizeof(int32_t) * (static_cast<size_t>(R) + 1));
     L.sample_prefix = take(sizeof(int32_t) * (static_cast<size_t>(R) + 1));
-    L.logits = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(ld));
+    const size_t tiles = static_cast<size_t>(cand_tiles_ld(ld));
+    const size_t dense = sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(ld);
+    const size_t slots = sizeof(float) * tiles * static_cast<size_t>(R) * TILE_M;
+    L.scores = take(with_scores ? std::max(dense, slots) : 0);
     const FilterShape f = filter_shape(ld, std::max(k, 1));
     L.sample = take(sizeof(float) * static_cast<size_t>(R) * static_cast<size_t>(f.sample_ld));
     L.tau = take(sizeof(float) * R);
     L.flag = take(sizeof(int32_t) * R);
-    const size_t tiles = static_cast<size_t>(cand_tiles_ld(ld));
     L.cand_mask = take(sizeof(uint32_t) * static_cast<size_t>(R) * tiles * 4);
-    L.cand_score = take(sizeof(float) * static_cast<size_t>(R) * tiles * 4 * CAND_SLOTS);   // 4 planes
     L.total = o;
     return L;
 }
@@ -251,9 +254,9 @@ int launch_scorer(const ScoreSetup &s, int grid, void *stream)
 qsa_status setup_score(ScoreSetup &s, const void *q, const float *w, int32_t rows, int32_t H,
                        const qsa_paged_keys *keys, const int32_t *row_req, const int32_t *row_visible,
                        int64_t ld, int64_t max_len, int32_t k, int32_t sample_stride, void *ws,
-                       size_t ws_bytes, DeviceInfo *d, void *stream)
+                       size_t ws_bytes, DeviceInfo *d, void *stream, bool with_scores = true)
 {
-    s.L = layout(rows, ld, k);
+    s.L = layout(rows, ld, k, with_scores);
     if (!ws || ws_bytes < s.L.total) return QSA_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return QSA_ERR_INVALID_ARG;
     s.ws = static_cast<uint8_t *>(ws);
@@ -327,7 +330,7 @@ size_t qsa_workspace_bytes(int32_t rows, int32_t row_capacity, int32_t k, int32_
     (void)flags;
     if (rows <= 0) return 256;
     const int64_t ld = std::max<int64_t>(8, (static_cast<int64_t>(std::max(row_capacity, 0)) + 7) / 8 * 8);
-    return layout(rows, ld, std::max(k, 1)).total;
+    return layout(rows, ld, std::max(k, 1), row_capacity > 1 || k > 1).total;
 }
 
 const char *qsa_status_string(qsa_status s)
@@ -537,7 +540,7 @@ qsa_status qsa_index_score(const void *q, const float *w, int32_t rows, int32_t 
     ScoreSetup s;
     // the score-only call needs no logits scratch: size the layout for one column
     st = setup_score(s, q, w, rows, H, keys, row_req, row_visible, 1, max_len, 1, 1, ws,
-                     ws_bytes, d, stream);
+                     ws_bytes, d, stream, false);
     if (st != QSA_OK) return st;
     s.sp.mode = SCORE_LOGITS;
     s.sp.out = logits;
@@ -608,7 +611,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
                      filter ? f.stride : 1, ws, ws_bytes, d, stream);
     if (st != QSA_OK) return st;
     auto at = [&](size_t off) { return s.ws + off; };
-    float *logits = reinterpret_cast<float *>(at(s.L.logits));
+    float *logits = reinterpret_cast<float *>(at(s.L.scores));
 
     SelectParams sel;
     std::memset(&sel, 0, sizeof(sel));
@@ -637,7 +640,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     float *sample = reinterpret_cast<float *>(at(s.L.sample));
     float *tau = reinterpret_cast<float *>(at(s.L.tau));
     uint32_t *cand_mask = reinterpret_cast<uint32_t *>(at(s.L.cand_mask));
-    float *cand_score = reinterpret_cast<float *>(at(s.L.cand_score));
+    float *cand_score = logits;                     // the same region, laid out by (tile, row)
     const int32_t tiles_ld = static_cast<int32_t>(cand_tiles_ld(ld));
 
     // 1. scores of every stride-th key tile
@@ -660,7 +663,6 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.mode = SCORE_FILTER;
     s.sp.tau = tau;
     s.sp.cand_score = cand_score;
-    s.sp.cand_plane = static_cast<uint32_t>(static_cast<int64_t>(rows) * tiles_ld * 4 * 8);
     s.sp.cand_mask = cand_mask;
     s.sp.tiles_ld = tiles_ld;
     if ((st = launch_rc(timed(K_SCORE_FILTER, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
@@ -671,7 +673,6 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     SelectParams cs = sel;
     cs.mode = SEL_CAND;
     cs.cand_score = cand_score;
-    cs.cand_plane = s.sp.cand_plane;
     cs.cand_mask = cand_mask;
     cs.tiles_ld = tiles_ld;
     cs.cap = f.cap;
@@ -686,7 +687,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     cs.max_pages = keys->max_pages_per_req;
     cs.num_pages = keys->num_pages;
     cs.page_pos = keys->page_positions;
-    cs.fb_logits = logits;
+    cs.fb_scores = cand_score;
     return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, g_overlap, stream); }));
 }
 

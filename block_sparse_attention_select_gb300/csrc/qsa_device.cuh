@@ -144,6 +144,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait that ignores any abort flag: for copies still in flight into
+// a CTA's shared memory after another wait gave up.  Returns whether the
+// phase completed within about limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    const long long t0 = clock64();
+    const long long limit = static_cast<long long>(limit_ns) * 2;
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+
 // -------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, uint64_t *bar,
@@ -153,6 +165,28 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, ui
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst_smem)),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+// 3-D tiled TMA load (coordinates innermost first).
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const void *tmap, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// Plain bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 

@@ -20,20 +20,19 @@ constexpr int EPI_WARPS = 16;    // 4 per TMEM lane quarter, each owning 64 accu
 constexpr int SCORE_THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA, then epilogue
 
 // Candidate lists of the filter pass.  Key tile t of row r has four quarters
-// q of 32 positions (t*128 + q*32 + i, i < 32); quarter e = 4*t + q of row r:
-//   cand_mask[r*tiles_ld*4 + e], bit i: position t*128 + q*32 + i passed;
-//   the j-th passing position of the quarter (ascending i) has twice its
-//   score (an exact scaling) at
-//   cand_score[(j / 8) * plane + (r*tiles_ld*4 + e)*8 + j % 8],
-//   plane = R * tiles_ld * 4 * 8 floats.
-// Plane 0 holds every quarter's first eight slots, one contiguous run per
-// row that the selector streams like a dense array; a quarter rarely has
-// more than eight candidates (the filter keeps a few percent of the
-// positions), and those go to planes 1..3 at the same offset.  The scorer
-// addresses slot j as j + (j / 8) * (plane - 8) from the plane-0 run, one
-// store per row with no test for the rare case.  tiles_ld is a multiple of
-// 8, which keeps each row's mask words in lines of their own.
-constexpr int CAND_SLOTS = 32;   // score slots per quarter (4 planes of 8)
+// q of 32 positions (t*128 + q*32 + i, i < 32):
+//   cand_mask[r*tiles_ld*4 + 4t + q], bit i: position t*128 + q*32 + i passed;
+//   the j-th passing position of quarter q (ascending i) has its score at
+//   cand_score[(t*R + r)*128 + 4j + q].
+// Each (tile, row) owns one 512-byte region whose "slot row" j holds the j-th
+// candidate of each of the four quarters, so the few candidates of a tile
+// (the filter keeps a few percent of the positions) share the region's first
+// sectors and the four quarter warps of a tile fill those sectors together.
+// Rows of one tile are 512 bytes apart, a compile-time stride: the scorer
+// addresses a row's slot with an immediate offset.  The region is as large as
+// the dense logits of the same rows, which it replaces on the filter path (a
+// row the selector re-scores reuses it).  tiles_ld is a multiple of 8, which
+// keeps each row's mask words in 128-byte lines of their own.
 constexpr int TH_STAGE = 16384;  // sampled scores of one row the threshold kernel holds in shared memory
 
 // A group: consecutive query rows of one request that share every key tile.
@@ -83,8 +82,7 @@ struct ScoreParams {
     int64_t ld;
     int32_t pad_inf;            // LOGITS: write -inf for V_r <= j < tile end (j < ld)
     const float *tau;           // FILTER: per-row threshold
-    float *cand_score;          // FILTER: [4, R, tiles_ld * 4, 8] candidate scores (layout above)
-    uint32_t cand_plane;        // floats per plane of cand_score (host keeps 4 planes below 2^32)
+    float *cand_score;          // FILTER: [tiles_ld, R, 128] candidate scores (layout above)
     uint32_t *cand_mask;        // FILTER: [R, tiles_ld * 4] passing positions of each quarter
     int32_t tiles_ld;           // key tiles per row in the candidate arrays (multiple of 8)
     uint32_t *status;
@@ -106,21 +104,22 @@ struct SelectParams {
     int64_t max_len;            // largest valid V_r (longer rows are clamped and flagged)
     const int32_t *row_vis;     // V_r
     const float *cand_score;    // CAND: lists written by the filter scorer
-    uint32_t cand_plane;
     const uint32_t *cand_mask;
     int32_t tiles_ld;
     int32_t cap;                // THRESH: rows up to this length keep every position; CAND: list capacity
     int32_t *row_flag;          // CAND: 1 for rows that took the in-kernel fallback, else 0
     Plan *plan;
     // CAND fallback: a row whose list cannot be trusted is re-scored (plain
-    // FP32 arithmetic) into fb_logits[r * max_len ...] and selected densely
+    // FP32 arithmetic) into its own regions of the candidate array (fb_scores
+    // = cand_score, position j of row r at ((j / 128) * R + r) * 128 + j % 128)
+    // and selected densely
     const uint16_t *q;          // FP16 bits [R, H, 128]
     const float *w;             // [R, H]
     const uint16_t *k_cache;    // FP16 bits [num_pages, page_pos, 128]
     const int32_t *block_table;
     const int32_t *row_req;
     int32_t H, max_pages, num_pages, page_pos;
-    float *fb_logits;
+    float *fb_scores;
     // THRESH
     int32_t sample_stride;
     float *tau;
@@ -177,6 +176,7 @@ int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, c
                  int grid, bool overlap, void *stream);
 int launch_select(const SelectParams &p, int grid, bool overlap, void *stream);
 size_t select_smem_bytes(int32_t smem_cap);
+size_t cand_smem_bytes(int32_t k, int32_t cap);
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
 int launch_produce(const ProduceParams &p, int32_t max_tokens, void *stream);

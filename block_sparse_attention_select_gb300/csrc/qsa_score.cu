@@ -44,7 +44,7 @@ struct __align__(8) Ctrl {
 // Group data of one epilogue warp: the rows of its 64 accumulator columns,
 // private to the warp so that a group change needs no barrier across warps.
 struct EpiRows {
-    __align__(16) float w[64];   // w[(row - first row of the warp) * H + h]
+    __align__(16) float w[64];   // weights by row pair: w[(r / 2) * 2H + 2h + r % 2], r = row - first row of the warp
     __align__(16) int32_t vis[64];   // V of each row
     __align__(16) float tau[64];     // FILTER threshold of each row
     uint32_t masks[32];              // FILTER: mask words of the chunk being drained
@@ -132,59 +132,31 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
     return d;
 }
 
-// sum_h w[h] * max(acc[h], 0) for one (row, position).  Heads are paired
-// into packed FMAs; the accumulation starts from +0 so the result is never -0.
+__device__ __forceinline__ float relu_f(uint32_t acc) { return fmaxf(__uint_as_float(acc), 0.0f); }
+
+// Scores of two query rows (a, b) at one key position:
+//   s = sum_h w[row, h] * max(acc[row, h], 0),  heads in order h = 0 .. H-1,
+// each head one fused multiply-add onto an accumulator that starts at +0 (so
+// no score is -0), the two rows side by side in one packed FMA per head.
+// wp: the pair's weights interleaved by head, (w[a,h], w[b,h]) for h = 0 ...
+// Every mode of the scorer (logits, sampled tiles, filter) uses this same
+// arithmetic, so a score is the same bit pattern whichever pass computed it.
 template <int H>
-__device__ __forceinline__ float weighted_relu_sum(const float *w, const uint32_t *acc)
+__device__ __forceinline__ float2 relu_pair_sum(const float *wp, const uint32_t *acc_a, const uint32_t *acc_b)
 {
+    float2 s = make_float2(0.0f, 0.0f);
     if constexpr (H == 1) {
-        return fmaf(w[0], fmaxf(__uint_as_float(acc[0]), 0.0f), 0.0f);
+        const float2 ww = *reinterpret_cast<const float2 *>(wp);
+        s = ffma2(ww, make_float2(relu_f(acc_a[0]), relu_f(acc_b[0])), s);
     } else {
-        float2 s = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int h = 0; h < H; h += 2) {
-            const float2 a = make_float2(fmaxf(__uint_as_float(acc[h]), 0.0f),
-                                         fmaxf(__uint_as_float(acc[h + 1]), 0.0f));
-            s = ffma2(make_float2(w[h], w[h + 1]), a, s);
-        }
-        return s.x + s.y;
-    }
-}
-
-// 2 * sum_h w[h] * max(acc[h], 0), the filter pass's form: d + |d| is
-// exactly 2 * max(d, 0) (+0 for d <= 0) and is an add on the FMA pipe rather
-// than a max on the integer pipe; scaling by 2 commutes with every rounding
-// (short of overflow or subnormal results), so the value is exactly twice
-// weighted_relu_sum's.
-template <int H>
-__device__ __forceinline__ float weighted_relu_sum2(const float *w, const uint32_t *acc)
-{
-    auto t = [&](int h) { const float d = __uint_as_float(acc[h]); return d + fabsf(d); };
-    if constexpr (H == 1) {
-        return fmaf(w[0], t(0), 0.0f);
-    } else {
-        float2 s = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int h = 0; h < H; h += 2) s = ffma2(make_float2(w[h], w[h + 1]), make_float2(t(h), t(h + 1)), s);
-        return s.x + s.y;
-    }
-}
-
-template <int H>
-__device__ __forceinline__ void load_w(const float *w, int el, float (&out)[H])
-{
-    if constexpr (H == 1) {
-        out[0] = w[el];
-    } else if constexpr (H == 2) {
-        const float2 a = reinterpret_cast<const float2 *>(w)[el];
-        out[0] = a.x; out[1] = a.y;
-    } else {
-#pragma unroll
-        for (int q = 0; q < H / 4; ++q) {
-            const float4 a = reinterpret_cast<const float4 *>(w)[el * (H / 4) + q];
-            out[4 * q] = a.x; out[4 * q + 1] = a.y; out[4 * q + 2] = a.z; out[4 * q + 3] = a.w;
+            const float4 ww = *reinterpret_cast<const float4 *>(wp + 2 * h);
+            s = ffma2(make_float2(ww.x, ww.y), make_float2(relu_f(acc_a[h]), relu_f(acc_b[h])), s);
+            s = ffma2(make_float2(ww.z, ww.w), make_float2(relu_f(acc_a[h + 1]), relu_f(acc_b[h + 1])), s);
         }
     }
+    return s;
 }
 
 // Drains this warp's 64 accumulator columns (64 / H query rows) of one tile.
@@ -198,29 +170,24 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, 
     constexpr int RPC = 32 / H;          // rows per 32-column chunk
     constexpr int RPW = 64 / H;          // rows per warp
     constexpr int B = RPC < 8 ? RPC : 8; // rows scored together: independent chains, no branches
+    static_assert(B % 4 == 0, "row pairs, thresholds read four rows at a time");
     const int32_t p_in_tile = quarter * 32 + lane;
     const int32_t j = tile * TILE_M + p_in_tile;
     const int64_t r0 = static_cast<int64_t>(gr.row0) + cq * RPW;     // first row of this warp
-    // FILTER: quarter e0 of row r0 (score slots and mask word); a row further
-    // is tiles_ld * 4 quarters further
-    const int64_t e0 = (r0 * p.tiles_ld + tile) * 4 + quarter;
-    const int64_t q_stride = static_cast<int64_t>(p.tiles_ld) * 4;
-    // score slots from one row to the next, as a 32-bit offset: the host uses
-    // the filter path only while 64 rows of slots span less than 2^32 floats
-    const uint32_t slot_row = static_cast<uint32_t>(q_stride * 8);   // plane-0 floats per row
-    const uint32_t plane_step = p.cand_plane - 8u;                        // slot 8 -> plane 1, ...
-    const uint32_t mask_row = static_cast<uint32_t>(q_stride);
-    float *score0 = nullptr;
+    float *slot0 = nullptr;
     uint32_t *mask0 = nullptr;
     float *out0 = nullptr;
     if constexpr (MODE == SCORE_FILTER) {
-        score0 = p.cand_score + e0 * 8;
-        mask0 = p.cand_mask + e0;
+        // this quarter's slot column in the (tile, r0) region: a row further is
+        // TILE_M floats further (an immediate offset), a slot row 4 floats
+        slot0 = p.cand_score + (static_cast<int64_t>(tile) * p.R + r0) * TILE_M + quarter;
+        mask0 = p.cand_mask + (r0 * p.tiles_ld + tile) * 4 + quarter;
     } else if constexpr (MODE == SCORE_SAMPLE) {
         out0 = p.out + r0 * p.ld + static_cast<int64_t>(tile >> p.sample_shift) * TILE_M + p_in_tile;
     } else {
         out0 = p.out + r0 * p.ld + j;
     }
+    const uint32_t mask_row = static_cast<uint32_t>(p.tiles_ld) * 4u;   // mask words from one row to the next
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
         const int32_t c0 = ch * RPC;
@@ -233,11 +200,18 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, 
             if (!ALLROWS && c0 + b0 >= nmine) break;         // warp-uniform
             float s[B];
 #pragma unroll
-            for (int i = 0; i < B; ++i) {
-                float wv[H];
-                load_w<H>(e.w, c0 + b0 + i, wv);
-                if constexpr (MODE == SCORE_FILTER) s[i] = weighted_relu_sum2<H>(wv, v + (b0 + i) * H);
-                else s[i] = weighted_relu_sum<H>(wv, v + (b0 + i) * H);
+            for (int i = 0; i < B; i += 2) {
+                const float2 sp = relu_pair_sum<H>(e.w + (c0 + b0 + i) * H, v + (b0 + i) * H, v + (b0 + i + 1) * H);
+                s[i] = sp.x;
+                s[i + 1] = sp.y;
+            }
+            float tau[B];
+            if constexpr (MODE == SCORE_FILTER) {
+#pragma unroll
+                for (int i = 0; i < B; i += 4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(e.tau + c0 + b0 + i);
+                    tau[i] = t4.x; tau[i + 1] = t4.y; tau[i + 2] = t4.z; tau[i + 3] = t4.w;
+                }
             }
 #pragma unroll
             for (int i = 0; i < B; ++i) {
@@ -245,16 +219,12 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, 
                 const bool live = ALLROWS || el < nmine;      // warp-uniform
                 const bool ok = live && (FULL || j < e.vis[el]);
                 if constexpr (MODE == SCORE_FILTER) {
-                    // s and tau are both doubled here; the stored slot value
-                    // is 2 * score (halved exactly by the selector)
-                    const bool take = ok && s[i] >= e.tau[el];
+                    const bool take = ok && s[i] >= tau[i];
                     const uint32_t m = __ballot_sync(0xffffffffu, take);
                     if (lane == 0) e.masks[b0 + i] = m;
-                    // a passing lane's slot: the passing lanes below it
-                    const int rk = __popc(m & lt_mask);
-                    if (take)
-                        score0[static_cast<uint32_t>(el) * slot_row + static_cast<uint32_t>(rk) +
-                               (static_cast<uint32_t>(rk) >> 3) * plane_step] = s[i];
+                    // a passing lane's slot row: the passing lanes below it
+                    const uint32_t rk = static_cast<uint32_t>(__popc(m & lt_mask));
+                    if (take) (slot0 + rk * 4u)[el * TILE_M] = s[i];
                 } else if constexpr (MODE == SCORE_SAMPLE) {
                     if (ok) out0[el * p.ld] = s[i];
                 } else {
@@ -526,12 +496,15 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 const int32_t first = cq * RPW;
                 const int32_t nmine = max(0, min(RPW, gr.nrows - first));
                 __syncwarp();
-                for (int32_t i = lane; i < nmine * H; i += 32)
-                    er.w[i] = __ldg(p.w + static_cast<int64_t>(gr.row0 + first) * H + i);
+                for (int32_t i = lane; i < RPW * H; i += 32) {
+                    const int32_t rr = i / H, h = i % H;          // rows past the group weigh 0
+                    er.w[(rr >> 1) * 2 * H + 2 * h + (rr & 1)] =
+                        rr < nmine ? __ldg(p.w + static_cast<int64_t>(gr.row0 + first + rr) * H + h) : 0.0f;
+                }
                 for (int32_t i = lane; i < nmine; i += 32) {
                     const int32_t r = gr.row0 + first + i;
                     er.vis[i] = __ldg(p.row_vis + r);
-                    er.tau[i] = p.mode == SCORE_FILTER ? 2.0f * __ldg(p.tau + r) : 0.0f;   // see weighted_relu_sum2
+                    er.tau[i] = p.mode == SCORE_FILTER ? __ldg(p.tau + r) : 0.0f;
                 }
                 __syncwarp();
             }

@@ -412,6 +412,17 @@ __device__ void write_row(const SelectParams &p, int32_t r, const uint64_t *buf,
     }
 }
 
+// A row of scores in global memory: element i at base[(i >> 7) * tile_stride
+// + (i & 127)].  Dense logits are one contiguous run (tile_stride = TILE_M); a
+// row the candidate selector re-scores lives in its own 128-float regions of
+// the candidate array, TILE_M * R floats apart.
+struct RowView {
+    float *base;
+    int64_t tile_stride;
+    __device__ __forceinline__ float *at(int32_t i) const { return base + (i >> 7) * tile_stride + (i & 127); }
+    __device__ __forceinline__ float ld(int32_t i) const { return __ldcg(at(i)); }
+};
+
 // Streaming narrowing over a long row in global memory (fixed 11/11/10-bit
 // digits of key32): stops as soon as every element at or above the current
 // cut digit fits in shared memory (gathers them and returns their count), or
@@ -419,7 +430,7 @@ __device__ void write_row(const SelectParams &p, int32_t r, const uint64_t *buf,
 __device__ __forceinline__ int level_shift(int lv) { return lv == 0 ? 21 : (lv == 1 ? 10 : 0); }
 __device__ __forceinline__ uint32_t level_mask(int lv) { return lv < 2 ? 0x7FFu : 0x3FFu; }
 
-__device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, int32_t n, uint32_t k,
+__device__ int32_t stream_narrow(SelShared &sh, const RowView row, int32_t n, uint32_t k,
                                  int32_t cap, uint32_t *keys, uint32_t *inv, uint32_t &T_out,
                                  uint32_t &k_rem_out, bool gather)
 {
@@ -427,7 +438,7 @@ __device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, i
     for (int lv = 0; lv < 3; ++lv) {
         clear_hist(sh);
         for (int32_t i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = score_key(__ldcg(row + i));
+            const uint32_t key = score_key(row.ld(i));
             if ((key & pmask) == prefix) atomicAdd(&sh.hist[(key >> level_shift(lv)) & level_mask(lv)], 1u);
         }
         __syncthreads();
@@ -443,7 +454,7 @@ __device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, i
             if (threadIdx.x == 0) sh.count = 0;
             __syncthreads();
             for (int32_t i = threadIdx.x; i < n; i += NT) {
-                const uint32_t key = score_key(__ldcg(row + i));
+                const uint32_t key = score_key(row.ld(i));
                 if ((key & pmask) >= prefix) {
                     const uint32_t slot = atomicAdd(&sh.count, 1u);
                     keys[slot] = key;
@@ -461,14 +472,14 @@ __device__ int32_t stream_narrow(SelShared &sh, const float *__restrict__ row, i
 
 // Everything above the exact cut key T, then the k_rem lowest positions that
 // hold T, in position order.
-__device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ row, int32_t n,
+__device__ int32_t gather_cut_in_order(SelShared &sh, const RowView row, int32_t n,
                                        uint32_t T, uint32_t k_rem, uint32_t *keys, uint32_t *inv)
 {
     if (threadIdx.x == 0) { sh.count = 0; sh.taken = 0; }
     __syncthreads();
     for (int32_t base = 0; base < n; base += NT) {
         const int32_t i = base + threadIdx.x;
-        const uint32_t key = i < n ? score_key(__ldcg(row + i)) : 0u;
+        const uint32_t key = i < n ? score_key(row.ld(i)) : 0u;
         if (i < n && key > T) {
             const uint32_t slot = atomicAdd(&sh.count, 1u);
             keys[slot] = key;
@@ -487,7 +498,7 @@ __device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ 
         __syncthreads();
         if (sh.taken >= k_rem) {
             for (int32_t j = base + NT + threadIdx.x; j < n; j += NT) {
-                const uint32_t kj = score_key(__ldcg(row + j));
+                const uint32_t kj = score_key(row.ld(j));
                 if (kj > T) {
                     const uint32_t slot = atomicAdd(&sh.count, 1u);
                     keys[slot] = kj;
@@ -504,7 +515,7 @@ __device__ int32_t gather_cut_in_order(SelShared &sh, const float *__restrict__ 
 // Plain FP32 scores of row r, written to `row` (multiply then add, head by
 // head, in the order of the definition).  Used only for rows whose candidate
 // list the filter could not certify; qf is shared scratch for H * 128 floats.
-__device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, float *row, float *qf)
+__device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, const RowView row, float *qf)
 {
     const int32_t H = p.H;
     for (int32_t i = threadIdx.x; i < H * HEAD_DIM; i += NT)
@@ -532,7 +543,7 @@ __device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, floa
         } else {
             record_error(p.status, ST_BAD_PAGE);   // as on the tensor path: the page reads as zeros
         }
-        row[j] = s + 0.0f;
+        *row.at(j) = s + 0.0f;
     }
     __syncthreads();
 }
@@ -542,7 +553,8 @@ __device__ void simt_score_row(const SelectParams &p, int32_t r, int32_t V, floa
 __host__ __device__ __forceinline__ int32_t out_capacity(const SelectParams &p) { return p.k + SLACK; }
 
 // One row of the dense selection: logits[r, 0:V_r] from HBM or, with
-// `rescore`, the row re-scored here first (plain FP32) into fb_logits.
+// `rescore`, the row re-scored here first (plain FP32) into its own regions
+// of the candidate array.
 // Shared memory: sh, then out64[k + SLACK], keys[smem_cap], inv[smem_cap].
 __device__ __forceinline__ void select_row(const SelectParams &p, int32_t r, bool rescore, SelShared &sh,
                            uint64_t *out64, uint32_t *keys, uint32_t *inv, int32_t smem_cap)
@@ -553,16 +565,16 @@ __device__ __forceinline__ void select_row(const SelectParams &p, int32_t r, boo
         V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
     }
     const int32_t kk_target = min(p.k, V);
-    const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+    RowView row{const_cast<float *>(p.logits) + static_cast<int64_t>(r) * p.ld, TILE_M};
     if (rescore) {
-        float *fb = p.fb_logits + static_cast<int64_t>(r) * p.max_len;
-        simt_score_row(p, r, V, fb, reinterpret_cast<float *>(keys));
-        row = fb;
+        // the row's own candidate regions, dead once the selector gives up on them
+        row = RowView{p.fb_scores + static_cast<int64_t>(r) * TILE_M, static_cast<int64_t>(p.R) * TILE_M};
+        simt_score_row(p, r, V, row, reinterpret_cast<float *>(keys));
     }
     int32_t n;
     if (V <= smem_cap) {
         for (int32_t i = threadIdx.x; i < V; i += NT) {
-            keys[i] = score_key(__ldcg(row + i));
+            keys[i] = score_key(row.ld(i));
             inv[i] = ~static_cast<uint32_t>(i);
         }
         __syncthreads();
@@ -611,20 +623,22 @@ select_kernel(const SelectParams p)
 
 // ------------------------------------------------------------ candidates --
 //
-// One CTA per row.  The row's mask words and the first score line of every
-// quarter are loaded together (one round trip), each thread appends its
-// quarters' candidates as full keys (key32 << 32 | ~position) at its
-// exclusive-scan offset, and the top kk are ordered by one counting pass on
-// the top 11 bits of (key32 - smallest key) plus rank counting inside the
-// buckets; each element's rank is its output index, so the result goes
-// straight to HBM.  A row whose list cannot be trusted (fewer than min(k, V)
-// candidates, more than cap, or a cut bucket too large to order here) is
-// re-scored in plain FP32 and selected densely by the same CTA (row_flag
-// records it).
+// One CTA per row.  The row's candidates (layout in qsa_internal.h) are read
+// exactly: the mask words first (one coalesced load per thread and quarter),
+// then, after one block scan for the offsets, one 4-byte cp.async per
+// candidate from its slot straight into the compact score array, so only
+// slots the filter pass wrote this call are touched (every read is an L2 hit
+// of that pass's output).  The candidates become full keys (key32 << 32 |
+// ~position); the top kk are then ordered by one counting pass on the top 11
+// bits of (key32 - smallest key) plus rank counting inside the buckets, and
+// each element's rank is its output index, so the result goes straight to
+// HBM.  A row whose list cannot be trusted (fewer than min(k, V) candidates,
+// more than cap, or a cut bucket too large to order here) is re-scored in
+// plain FP32 and selected densely by the same CTA (row_flag records it).
 constexpr int CT = 256;               // threads per row
 static_assert(CT == NT, "the in-kernel fallback runs the dense selection with the same block");
-constexpr int QPT = 8;                // half quarters per thread and gather round
 constexpr int BIG_MAX = 320;          // > (QSA_MAX_K + SLACK) / (RANK_MAX + 1)
+constexpr int QPR = 8;                // quarters per thread whose mask words are loaded together
 
 struct CandShared {
     uint32_t hist[NBINS];
@@ -660,38 +674,30 @@ __device__ __forceinline__ uint32_t cand_scan(uint32_t v, uint32_t *wt, uint32_t
     return before + x - v;
 }
 
-// Loads kept where they are written: all of a thread's loads are in flight
-// before the first of them is used (the compiler would otherwise move each
-// load next to its first use, inside the per-candidate loop).
-__device__ __forceinline__ uint32_t ld_issue_u32(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float4 ld_issue_f4(const float *p)
-{
-    float4 v;
-    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
-    return v;
-}
-
 __device__ __forceinline__ void discard_l2_line(const void *p)
 {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
+
+// 4-byte asynchronous copy global -> shared (completed by cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __global__ void __launch_bounds__(CT, 3)
 cand_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     CandShared &sh = *reinterpret_cast<CandShared *>(smem_raw);
-    uint64_t *a = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD);             // cap entries
-    uint64_t *bq = a + p.cap;                                                     // k + SLACK entries
+    uint64_t *bq = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD);          // k + SLACK entries
+    uint32_t *a_key = reinterpret_cast<uint32_t *>(bq + p.k + SLACK);            // cap entries: scores, then keys
+    uint32_t *a_pos = a_key + p.cap;                                             // cap entries: ~position
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int32_t r = blockIdx.x;
+    for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
+    if (t == 0) sh.nbig = 0;
     wait_prior_grid();                      // last kernel of its call: nothing to allow
     if (r >= p.R) return;
     // a row whose list cannot be trusted is re-scored and selected densely
@@ -702,8 +708,7 @@ cand_kernel(const SelectParams p)
             atomicExch(&p.plan->any_fallback, 1);
         }
         __syncthreads();
-        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), bq,
-                        reinterpret_cast<uint32_t *>(a), reinterpret_cast<uint32_t *>(a) + p.cap, p.cap);
+        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), bq, a_key, a_pos, p.cap);
     };
     int32_t V = p.row_vis[r];
     if (V < 0 || V > p.max_len) {
@@ -712,107 +717,67 @@ cand_kernel(const SelectParams p)
     }
     const int32_t kk_target = min(p.k, V);
     const int32_t ntile = (V + TILE_M - 1) / TILE_M;
-    const int32_t nh = ntile * 8;                  // half quarters: 4 slots each
-    const int64_t q_row = static_cast<int64_t>(r) * p.tiles_ld * 4;
-    const uint32_t *mrow = p.cand_mask + q_row;
-    const float *srow = p.cand_score + q_row * 8;          // plane 0: slots 0..7 of each quarter
-    for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
-    if (t == 0) sh.nbig = 0;
+    const int32_t nq = ntile * 4;
+    const uint32_t *mrow = p.cand_mask + static_cast<int64_t>(r) * p.tiles_ld * 4;
+    const float *srow = p.cand_score + static_cast<int64_t>(r) * TILE_M;    // tile t at + t * R * TILE_M
 
-    // ---- gather.  Thread pair (2i, 2i+1) takes quarter e: the even thread
-    //      its candidates 0..3, the odd one 4..7 and any further ones (rare);
-    //      a warp's load covers 512 contiguous bytes of the row's plane 0.
-    const uint32_t par = static_cast<uint32_t>(t & 1);
-    uint32_t kmin = 0xffffffffu, kmax = 0u, done = 0;
+    // ---- gather.  Thread t takes quarters e = t, t + CT, ... in rounds of
+    //      QPR: their mask words are loaded together, one block scan gives
+    //      the thread's offset, and each candidate's score is copied
+    //      asynchronously from its slot (row j of quarter q at float 4j + q
+    //      of the (tile, row) region) to its place in a_key.
+    uint32_t done = 0;
     bool overflow = false;
     int sbuf = 0;
-    for (int32_t h0 = 0; h0 < nh; h0 += QPT * CT) {
-        uint32_t m[QPT];
-        float4 f[QPT];
+    for (int32_t e0 = 0; e0 < nq; e0 += QPR * CT) {
+        uint32_t m[QPR], cnt = 0;
 #pragma unroll
-        for (int u = 0; u < QPT; ++u) {
-            const int32_t h = h0 + t + u * CT;
-            m[u] = 0u;
-            if (h < nh) {
-                m[u] = ld_issue_u32(mrow + (h >> 1));
-                f[u] = ld_issue_f4(srow + 4 * h);
-            }
+        for (int u = 0; u < QPR; ++u) {
+            const int32_t e = e0 + t + u * CT;
+            m[u] = e < nq ? __ldcg(mrow + e) : 0u;
         }
-        uint32_t cnt = 0;
 #pragma unroll
-        for (int u = 0; u < QPT; ++u) {
-            const uint32_t c = __popc(m[u]);
-            cnt += par ? (c > 4u ? c - 4u : 0u) : min(c, 4u);
-        }
+        for (int u = 0; u < QPR; ++u) cnt += __popc(m[u]);
         uint32_t ctot;
-        const uint32_t base = cand_scan(cnt, sh.wtot[sbuf], ctot);
+        const uint32_t before = cand_scan(cnt, sh.wtot[sbuf], ctot);
         sbuf ^= 1;
         if (done + ctot > static_cast<uint32_t>(p.cap)) { overflow = true; break; }   // uniform
-        // per half quarter: candidates held in registers (up to 4) and, for
-        // odd threads, overflow ones; their offsets in this thread's run
-        uint32_t off[QPT], nreg[QPT];
-        uint32_t run = done + base;
+        uint32_t o = done + before;
 #pragma unroll
-        for (int u = 0; u < QPT; ++u) {
-            const uint32_t c = __popc(m[u]);
-            nreg[u] = par ? min(c > 4u ? c - 4u : 0u, 4u) : min(c, 4u);
-            off[u] = run;
-            run += par ? (c > 4u ? c - 4u : 0u) : nreg[u];
-            if (par) {
-#pragma unroll
-                for (int z = 0; z < 4; ++z) m[u] &= m[u] - 1u;   // skip the even thread's four
-            }
-        }
-        // slot jj of every half quarter at once: independent chains
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-#pragma unroll
-            for (int u = 0; u < QPT; ++u) {
-                if (static_cast<uint32_t>(jj) < nreg[u]) {
-                    const float sc = 0.5f * (jj == 0 ? f[u].x : (jj == 1 ? f[u].y : (jj == 2 ? f[u].z : f[u].w)));
-                    const uint32_t bit = static_cast<uint32_t>(__ffs(m[u]) - 1);
-                    m[u] &= m[u] - 1u;
-                    const uint32_t key = score_key(sc);
-                    kmin = min(kmin, key);
-                    kmax = max(kmax, key);
-                    const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
-                    a[off[u] + jj] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
-                }
-            }
-        }
-        if (par) {
-#pragma unroll
-            for (int u = 0; u < QPT; ++u) {
-                uint32_t mm = m[u];
-                if (mm == 0u) continue;
-                // more than eight candidates in this quarter (rare): slots
-                // 8.., kept out of the loops above so that their iterations
-                // carry no global load
-                const uint32_t e = static_cast<uint32_t>(h0 + t + u * CT) >> 1;
-                const float *ov_q = srow + static_cast<int64_t>(e) * 8;
-                uint32_t o = off[u] + 4u;
-                // one plane of eight slots (two 16-byte loads) per step
-#pragma unroll 1
-                for (uint32_t g = 1; mm != 0u; ++g) {
-                    const float4 *pl = reinterpret_cast<const float4 *>(ov_q + g * static_cast<int64_t>(p.cand_plane));
-                    const float4 lo4 = __ldcg(pl), hi4 = __ldcg(pl + 1);
-                    const float v[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (mm == 0u) break;
-                        const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
-                        mm &= mm - 1u;
-                        const uint32_t key = score_key(0.5f * v[j]);
-                        kmin = min(kmin, key);
-                        kmax = max(kmax, key);
-                        a[o++] = (static_cast<uint64_t>(key) << 32) | ~(e * 32u + bit);
-                    }
-                }
+        for (int u = 0; u < QPR; ++u) {
+            const int32_t e = e0 + t + u * CT;
+            uint32_t mm = m[u];
+            const int32_t tile = e >> 2, q = e & 3;
+            const float *slot = srow + static_cast<int64_t>(tile) * p.R * TILE_M + q;
+            const uint32_t pos0 = static_cast<uint32_t>(tile * TILE_M + q * 32);
+            for (uint32_t j = 0; mm != 0u; ++j) {
+                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                mm &= mm - 1u;
+                cp_async4(a_key + o, slot + 4 * j);
+                a_pos[o] = ~(pos0 + bit);
+                ++o;
             }
         }
         done += ctot;
     }
-    // block min / max of the keys; the barrier also publishes a[]
+    cp_async_wait_all();
+    __syncthreads();
+    // every mask word of the row has been read: drop its lines from L2 unwritten
+    for (int32_t l = t; l < (ntile * 16 + 127) / 128; l += CT) discard_l2_line(mrow + l * 32);
+    const uint32_t n = done;
+    if (overflow || n < static_cast<uint32_t>(kk_target)) {   // uniform
+        fallback();
+        return;
+    }
+    // ---- scores -> order-preserving keys, and their range
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    for (uint32_t i = t; i < n; i += CT) {
+        const uint32_t key = score_key(__uint_as_float(a_key[i]));
+        a_key[i] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+    }
+    // block min / max of the keys; the barrier also publishes a_key[]
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
@@ -822,15 +787,6 @@ cand_kernel(const SelectParams p)
     __syncthreads();
 #pragma unroll
     for (int w = 0; w < CT / 32; ++w) { kmin = min(kmin, sh.red_min[w]); kmax = max(kmax, sh.red_max[w]); }
-    // every candidate line of the row has been read: drop it from L2 unwritten
-    for (int32_t tl = t; tl < ntile; tl += CT) discard_l2_line(srow + static_cast<int64_t>(tl) * 32);
-    for (int32_t l = t; l < (ntile * 16 + 127) / 128; l += CT) discard_l2_line(mrow + l * 32);
-
-    const uint32_t n = done;
-    if (overflow || n < static_cast<uint32_t>(kk_target)) {   // uniform
-        fallback();
-        return;
-    }
     const uint32_t kk = min(static_cast<uint32_t>(p.k), n);
     int32_t *oi = p.out_idx + static_cast<int64_t>(r) * p.k;
     float *ov = p.out_val ? p.out_val + static_cast<int64_t>(r) * p.k : nullptr;
@@ -838,7 +794,7 @@ cand_kernel(const SelectParams p)
         // ---- counting pass: bucket 0 holds the largest keys
         const int shift = span_shift(kmax - kmin);
         for (uint32_t i = t; i < n; i += CT)
-            atomicAdd(&sh.hist[NBINS - 1 - ((static_cast<uint32_t>(a[i] >> 32) - kmin) >> shift)], 1u);
+            atomicAdd(&sh.hist[NBINS - 1 - ((a_key[i] - kmin) >> shift)], 1u);
         __syncthreads();
         uint32_t c[BPT], sum = 0;
 #pragma unroll
@@ -859,19 +815,20 @@ cand_kernel(const SelectParams p)
         }
         // ---- scatter the buckets down to the cut
         for (uint32_t i = t; i < n; i += CT) {
-            const uint64_t x = a[i];
-            const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - kmin) >> shift);
-            if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = x;
+            const uint32_t key = a_key[i];
+            const uint32_t b = NBINS - 1 - ((key - kmin) >> shift);
+            if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = (static_cast<uint64_t>(key) << 32) | a_pos[i];
         }
         __syncthreads();
         // ---- rank inside the bucket = place in the output (hist[b] is now
         //      the end of bucket b, hence the start of bucket b + 1)
-        // two positions per iteration: two independent chains
-        for (uint32_t p0 = t; p0 < need; p0 += 2 * CT) {
-            uint64_t x[2];
-            uint32_t s0[2], m[2], rk[2];
+        // four positions per iteration: four independent chains
+        constexpr int NP = 4;
+        for (uint32_t p0 = t; p0 < need; p0 += NP * CT) {
+            uint64_t x[NP];
+            uint32_t s0[NP], m[NP], rk[NP];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NP; ++h) {
                 const uint32_t pos = p0 + h * CT;
                 m[h] = 0u;
                 s0[h] = 0xffffffffu;                              // no output unless ranked below
@@ -890,14 +847,14 @@ cand_kernel(const SelectParams p)
                 }
                 rk[h] = s0[h];
             }
-            const uint32_t mx = max(m[0], m[1]);
+            const uint32_t mx = max(max(m[0], m[1]), max(m[2], m[3]));
             for (uint32_t q = 0; q < mx; ++q) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < NP; ++h)
                     if (q < m[h]) rk[h] += bq[s0[h] + q] > x[h];
             }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NP; ++h) {
                 if (rk[h] < kk) {
                     oi[rk[h]] = static_cast<int32_t>(~static_cast<uint32_t>(x[h]));
                     if (ov) ov[rk[h]] = key_score(static_cast<uint32_t>(x[h] >> 32));
@@ -1126,6 +1083,11 @@ int set_smem(K kernel, size_t smem, size_t (&done)[64])
 
 }  // namespace
 
+size_t cand_smem_bytes(int32_t k, int32_t cap)
+{
+    return CAND_HEAD + static_cast<size_t>(k + SLACK) * 8 + static_cast<size_t>(cap) * 8;
+}
+
 int launch_select(const SelectParams &p, int grid, bool overlap, void *stream)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1151,7 +1113,7 @@ int launch_select(const SelectParams &p, int grid, bool overlap, void *stream)
     }
     if (p.mode == SEL_CAND) {
         static size_t done[64] = {};
-        const size_t smem = CAND_HEAD + (static_cast<size_t>(p.cap) + p.k + SLACK) * 8;
+        const size_t smem = cand_smem_bytes(p.k, p.cap);
         if (int rc = set_smem(cand_kernel, smem, done)) return rc;
         return launch_kernel(reinterpret_cast<const void *>(&cand_kernel), dim3(p.R), dim3(CT), smem, st, overlap,
                              args);
