@@ -705,6 +705,119 @@ def run_attend(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+BLOCKS_METRIC = "block-scorer rows/s (per-head 128-token block max + exact top-k) on 1 GB300"
+
+
+def run_blocks(args, ws, rank, local):
+    import torch
+
+    from block_sparse_attention_select_gb300 import qsa
+
+    qsa.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.block_scorer_bench()
+    R, H, D = inp.q.shape
+    tokens = int(np.sum(inp.row_token.astype(np.int64) + 1))
+    flops = 2.0 * D * H * tokens                       # every visible token's dot product per head
+    peaks = load_peaks()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q, kc, bt, rr, rt = t(inp.q), t(inp.k_cache), t(inp.block_table), t(inp.row_req), t(inp.row_token)
+    oi = torch.empty((R, H, inp.k), dtype=torch.int32, device=dev)
+    ov = torch.empty((R, H, inp.k), dtype=torch.float32, device=dev)
+    wsb = torch.empty(int(qsa.load().qsa_block_select_workspace_bytes(R, H, int(bt.shape[1]), inp.k)),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qsa.block_select(q, kc, bt, rr, rt, inp.k, oi, ov, wsb, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    launches = qsa.last_launch_count()
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    st = qsa.get_device_status()
+    assert st == qsa.QSA_OK, qsa.status_string(st)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), ws)
+    # per-kernel times (a separate pass with events around every launch)
+    qsa.set_config(qsa.QSA_CFG_KERNEL_TIMING, 1)
+    qsa.kernel_times()
+    n_kt = max(1, min(args.steps, 100))
+    for _ in range(n_kt):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    kt = qsa.kernel_times()
+    qsa.set_config(qsa.QSA_CFG_KERNEL_TIMING, 0)
+    score_ms = kt.get("score_logits", (ms * n_kt, n_kt))[0] / n_kt
+    achieved = flops / (score_ms / 1e3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        hq, hk = torch.from_numpy(inp.q).pin_memory(), torch.from_numpy(inp.k_cache).pin_memory()
+        hout = torch.empty((R, H, inp.k), dtype=torch.int32).pin_memory()
+        n_e = max(3, min(args.steps, 50))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e):
+            q.copy_(hq, non_blocking=True)
+            kc.copy_(hk, non_blocking=True)
+            qsa.block_select(q, kc, bt, rr, rt, inp.k, oi, None, wsb, stream, with_values=False)
+            hout.copy_(oi, non_blocking=True)
+            torch.cuda.synchronize()
+        el = (time.perf_counter() - t0) / n_e
+        e2e = {"value": R * ws / el, "unit": "rows/s", "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2,
+               "d2h_bytes_per_step": hout.numel() * 4, "ms_per_step": el * 1e3}
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        from oracle import block_scorer as BS
+        n_s = 4
+        rows = np.linspace(0, R - 1, n_s).astype(np.int64)
+        t0 = time.perf_counter()
+        BS.select_blocks(inp.q[rows], inp.k_cache, inp.block_table, inp.row_req[rows], inp.row_token[rows], inp.k)
+        el = time.perf_counter() - t0
+        cpu = {"value": n_s / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n_s} evenly spaced rows of {R} (numpy float64, one thread), {el:.1f} s"}
+    line = {
+        "metric": BLOCKS_METRIC, "value": R * ws / (ms / 1e3), "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": inp.name, "rows": R, "kv_heads": H, "head_dim": D, "k_blocks": inp.k,
+                   "block_tokens": 128, "visible_tokens": tokens, "l2": "flushed between steps (512 MiB write)",
+                   "accumulate": "f32", "median_ms": statistics.median(step_ms)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "score_blockmax",
+                     "kernel_ms": score_ms, "gflop": flops / 1e9, "peak_source": peaks["source"]},
+        "kernels_ms_per_step": {k: v[0] / n_kt for k, v in kt.items()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -715,15 +828,22 @@ def main():
     ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--op", choices=["select", "produce", "attend"], default="select",
+    ap.add_argument("--op", choices=["select", "produce", "attend", "blocks"], default="select",
                     help="select: the indexer step (default); produce: the index-key producer; "
-                         "attend: the sparse-attention consumer")
+                         "attend: the sparse-attention consumer; blocks: the M3-style block scorer")
     ap.add_argument("--producer-workload", choices=sorted(W.PRODUCER_CONFIGS), default="context")
     ap.add_argument("--window", type=int, choices=[4, 8], default=4)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     ws, rank, local = dist_setup()
-    if args.op == "attend":
+    if args.op == "blocks":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the block scorer's reference arm is the "
+                                  "oracle, reported as cpu_baseline in the blocks line"}), flush=True)
+        else:
+            run_blocks(args, ws, rank, local)
+    elif args.op == "attend":
         if args.impl == "reference":
             if rank == 0:
                 print(json.dumps({"impl": "reference", "unavailable": "the consumer's reference arm is the "

@@ -220,7 +220,46 @@ qsa_status make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint32_t 
     return r == CUDA_SUCCESS ? QSA_OK : QSA_ERR_INVALID_ARG;
 }
 
+// 3-D FP16 map with 128-byte swizzle: dims (innermost first) and byte strides
+// of dims 1 and 2; boxes of {64, box1, box2}.
+qsa_status make_tmap3(CUtensorMap *tm, const void *base, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+                      uint32_t box1, uint32_t box2)
+{
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(HEAD_DIM), static_cast<cuuint64_t>(d1), static_cast<cuuint64_t>(d2)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(s1), static_cast<cuuint64_t>(s2)};
+    cuuint32_t box[3] = {64, box1, box2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QSA_OK : QSA_ERR_INVALID_ARG;
+}
+
 bool supported_heads(int32_t H) { return H == 1 || H == 2 || H == 4 || H == 8; }
+
+// Workspace of the block scorer: plan over the H * rows virtual rows, their
+// request / token / block counts, and the block-score matrix [H * rows, max_blocks].
+struct BlockLayout {
+    size_t plan, vreq, vtok, vblk, row_vis, groups, item_prefix, sample_prefix, scores, total;
+};
+
+BlockLayout block_layout(int64_t RV, int64_t max_blocks)
+{
+    BlockLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = up(o + bytes, 256); return at; };
+    L.plan = take(sizeof(Plan));
+    L.vreq = take(sizeof(int32_t) * RV);
+    L.vtok = take(sizeof(int32_t) * RV);
+    L.vblk = take(sizeof(int32_t) * RV);
+    L.row_vis = take(sizeof(int32_t) * RV);
+    L.groups = take(sizeof(Group) * RV);
+    L.item_prefix = take(sizeof(int32_t) * (RV + 1));
+    L.sample_prefix = take(sizeof(int32_t) * (RV + 1));
+    L.scores = take(sizeof(float) * RV * max_blocks);
+    L.total = o;
+    return L;
+}
 
 qsa_status check_keys(const qsa_paged_keys *keys)
 {
@@ -689,6 +728,106 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     cs.page_pos = keys->page_positions;
     cs.fb_scores = cand_score;
     return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, g_overlap, stream); }));
+}
+
+size_t qsa_block_select_workspace_bytes(int32_t rows, int32_t H, int32_t max_blocks, int32_t k)
+{
+    (void)k;
+    if (rows <= 0 || H <= 0) return 256;
+    return block_layout(static_cast<int64_t>(rows) * H, std::max(max_blocks, 1)).total;
+}
+
+qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *k_cache, int32_t num_pages,
+                            const int32_t *block_table, int32_t num_reqs, int32_t max_blocks,
+                            const int32_t *row_req, const int32_t *row_token, int32_t k, int32_t *out_idx,
+                            float *out_val, void *ws, size_t ws_bytes, void *stream)
+{
+    g_launches = 0;
+    if (rows < 0 || k < 0 || H < 1 || num_pages < 1 || num_reqs < 1 || max_blocks < 1) return QSA_ERR_INVALID_ARG;
+    if (k > QSA_MAX_K || H > 16) return QSA_ERR_UNSUPPORTED;
+    const int64_t RV = static_cast<int64_t>(rows) * H;
+    if (RV >= INT32_MAX || static_cast<int64_t>(num_reqs) * H >= INT32_MAX ||
+        static_cast<int64_t>(max_blocks) * TILE_M >= INT32_MAX || static_cast<int64_t>(num_pages) * TILE_M >= INT32_MAX)
+        return QSA_ERR_UNSUPPORTED;
+    if (rows == 0 || k == 0) return QSA_OK;
+    if (!q || !k_cache || !block_table || !row_req || !row_token || !out_idx) return QSA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16)) return QSA_ERR_INVALID_ARG;
+    if (!aligned(block_table, 4) || !aligned(row_req, 4) || !aligned(row_token, 4) || !aligned(out_idx, 4) ||
+        !aligned(out_val, 4))
+        return QSA_ERR_INVALID_ARG;
+    DeviceInfo *d = nullptr;
+    qsa_status st = device_info(&d);
+    if (st != QSA_OK) return st;
+    const BlockLayout L = block_layout(RV, max_blocks);
+    if (!ws || ws_bytes < L.total) return QSA_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return QSA_ERR_INVALID_ARG;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    auto i32 = [&](size_t off) { return reinterpret_cast<int32_t *>(w8 + off); };
+    // queries [rows][H][128], boxes of one head x 256 rows; keys [pages * 128
+    // tokens][H][128], boxes of one head x 128 tokens (strides increase with the
+    // dimension in both maps)
+    CUtensorMap tq, tk;
+    if ((st = make_tmap3(&tq, q, static_cast<uint64_t>(H), static_cast<uint64_t>(rows), HEAD_DIM * 2,
+                         static_cast<uint64_t>(H) * HEAD_DIM * 2, 1, N_MAX)) != QSA_OK)
+        return st;
+    if ((st = make_tmap3(&tk, k_cache, static_cast<uint64_t>(H), static_cast<uint64_t>(num_pages) * TILE_M,
+                         HEAD_DIM * 2, static_cast<uint64_t>(H) * HEAD_DIM * 2, 1, TILE_M)) != QSA_OK)
+        return st;
+    const int32_t RVi = static_cast<int32_t>(RV);
+    if ((st = launch_rc(launch_block_rows(row_req, row_token, rows, H, num_reqs, i32(L.vreq), i32(L.vtok),
+                                          i32(L.vblk), d->status, stream))) != QSA_OK)
+        return st;
+    if ((st = launch_rc(timed(K_PLAN, stream, [&] {
+             return launch_plan(i32(L.vreq), i32(L.vtok), RVi, N_MAX, num_reqs * H,
+                                static_cast<int64_t>(max_blocks) * TILE_M, 1, i32(L.row_vis),
+                                reinterpret_cast<Group *>(w8 + L.groups), i32(L.item_prefix), i32(L.sample_prefix),
+                                reinterpret_cast<Plan *>(w8 + L.plan), d->status, stream);
+         }))) != QSA_OK)
+        return st;
+    ScoreParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.row_vis = i32(L.row_vis);
+    sp.groups = reinterpret_cast<const Group *>(w8 + L.groups);
+    sp.item_prefix = i32(L.item_prefix);
+    sp.sample_prefix = i32(L.sample_prefix);
+    sp.plan = reinterpret_cast<const Plan *>(w8 + L.plan);
+    sp.block_table = block_table;
+    sp.max_pages = max_blocks;
+    sp.num_pages = num_pages;
+    sp.page_pos = TILE_M;
+    sp.page_box = TILE_M;
+    sp.page_pos_shift = log2_exact(TILE_M);
+    sp.page_box_shift = sp.page_pos_shift;
+    sp.H = 1;
+    sp.R = RVi;
+    sp.mode = SCORE_BLOCKMAX;
+    sp.sample_stride = 1;
+    sp.out = reinterpret_cast<float *>(w8 + L.scores);
+    sp.ld = max_blocks;
+    sp.status = d->status;
+    sp.wait_limit_ns = g_wait_ns;
+    sp.blk_heads = H;
+    sp.blk_reqs = num_reqs;
+    sp.blk_rows = rows;
+    if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] {
+             return launch_score(sp, &tq, &tk, &tk, d->sms, g_overlap, stream);
+         }))) != QSA_OK)
+        return st;
+    SelectParams sel;
+    std::memset(&sel, 0, sizeof(sel));
+    sel.mode = SEL_DENSE;
+    sel.R = RVi;
+    sel.k = k;
+    sel.logits = reinterpret_cast<const float *>(w8 + L.scores);
+    sel.ld = max_blocks;
+    sel.max_len = max_blocks;
+    sel.row_vis = i32(L.vblk);
+    sel.out_idx = out_idx;
+    sel.out_val = out_val;
+    sel.smem_cap = std::max(8192, k);
+    sel.status = d->status;
+    sel.out_heads = H;
+    return launch_rc(timed(K_SEL_DENSE, stream, [&] { return launch_select(sel, RVi, g_overlap, stream); }));
 }
 
 }  // extern "C"

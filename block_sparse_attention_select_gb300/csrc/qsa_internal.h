@@ -56,6 +56,7 @@ enum ScoreMode : int32_t {
     SCORE_LOGITS = 0,      // logits for j < V_r (and -inf up to the tile end when pad_inf)
     SCORE_SAMPLE = 1,      // sampled tiles only, into the sample matrix
     SCORE_FILTER = 2,      // append (score, j) with score >= tau_r to the candidate lists
+    SCORE_BLOCKMAX = 3,    // block scorer: per (row, head) the max over each 128-token block
 };
 
 struct ScoreParams {
@@ -87,6 +88,13 @@ struct ScoreParams {
     int32_t tiles_ld;           // key tiles per row in the candidate arrays (multiple of 8)
     uint32_t *status;
     uint64_t wait_limit_ns;
+    // BLOCKMAX (the M3-style block scorer): rows are virtual rows v = h * blk_rows
+    // + r, one per (query row r, KV head h); a group's req is the virtual
+    // request h * blk_reqs + b.  Queries are read through a 3-D map [H][rows][128]
+    // and keys through [tokens][H][128] (one 128-token page per tile).
+    int32_t blk_heads;          // KV heads (0 outside BLOCKMAX)
+    int32_t blk_reqs;           // requests of the block table
+    int32_t blk_rows;           // query rows
 };
 
 enum SelectMode : int32_t {
@@ -129,6 +137,9 @@ struct SelectParams {
     float *out_val;
     int32_t smem_cap;           // elements the CTA can hold in shared memory
     uint32_t *status;
+    // DENSE: with out_heads > 1 the R = out_heads * n rows are virtual rows
+    // v = h * n + r and row v's output goes to row r * out_heads + h
+    int32_t out_heads;
 };
 
 // Index-key producer (the step before the indexer): see qsa_produce.cu.
@@ -179,6 +190,12 @@ size_t select_smem_bytes(int32_t smem_cap);
 size_t cand_smem_bytes(int32_t k, int32_t cap);
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
+// Block scorer rows: for v = h * R + r, vreq[v] = row_req[r] + h * num_reqs (or
+// -1 when row_req[r] is out of range), vtok[v] = row_token[r] + 1 visible
+// tokens (0 and flagged when negative), vblk[v] = visible 128-token blocks.
+int launch_block_rows(const int32_t *row_req, const int32_t *row_token, int32_t R, int32_t H,
+                      int32_t num_reqs, int32_t *vreq, int32_t *vtok, int32_t *vblk, uint32_t *status,
+                      void *stream);
 int launch_produce(const ProduceParams &p, int32_t max_tokens, void *stream);
 int launch_rope_table(float *table, int32_t n_blocks, int32_t rope_dim, double theta, void *stream);
 int launch_attend(const AttendParams &p, void *stream);

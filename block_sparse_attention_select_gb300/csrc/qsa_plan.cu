@@ -4,6 +4,8 @@
 // work items out for the persistent scorer.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
 
@@ -204,6 +206,44 @@ int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, boo
     void *args[] = {&logits, &ld, &R, const_cast<int32_t **>(&row_vis)};
     return launch_kernel(reinterpret_cast<const void *>(&pad_kernel), dim3(R), dim3(256), 0,
                          static_cast<cudaStream_t>(stream), overlap, args);
+}
+
+}  // namespace qsa
+
+namespace qsa {
+namespace {
+
+// Virtual rows of the block scorer (one per query row and KV head).
+__global__ void block_rows_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row_token,
+                                  int32_t R, int32_t H, int32_t num_reqs, int32_t *__restrict__ vreq,
+                                  int32_t *__restrict__ vtok, int32_t *__restrict__ vblk, uint32_t *status)
+{
+    const int64_t n = static_cast<int64_t>(R) * H;
+    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < n;
+         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t h = static_cast<int32_t>(v / R), r = static_cast<int32_t>(v % R);
+        const int32_t b = row_req[r];
+        const int32_t t = row_token[r];
+        const bool ok = b >= 0 && b < num_reqs && t >= 0;
+        if (!ok && h == 0) record_error(status, ST_BAD_ROW);
+        vreq[v] = ok ? b + h * num_reqs : -1;
+        const int32_t tok = ok ? t + 1 : 0;
+        vtok[v] = tok;
+        vblk[v] = (tok + TILE_M - 1) / TILE_M;
+    }
+}
+
+}  // namespace
+
+int launch_block_rows(const int32_t *row_req, const int32_t *row_token, int32_t R, int32_t H,
+                      int32_t num_reqs, int32_t *vreq, int32_t *vtok, int32_t *vblk, uint32_t *status,
+                      void *stream)
+{
+    const int64_t n = static_cast<int64_t>(R) * H;
+    const int grid = static_cast<int>(std::min<int64_t>((n + 255) / 256, 1024));
+    block_rows_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(row_req, row_token, R, H, num_reqs,
+                                                                          vreq, vtok, vblk, status);
+    return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace qsa

@@ -398,8 +398,13 @@ __device__ void select_and_sort(SelShared &sh, const uint32_t *keys, const uint3
 
 __device__ void write_row(const SelectParams &p, int32_t r, const uint64_t *buf, int32_t kk)
 {
-    int32_t *oi = p.out_idx + static_cast<int64_t>(r) * p.k;
-    float *ov = p.out_val ? p.out_val + static_cast<int64_t>(r) * p.k : nullptr;
+    int64_t ro = r;
+    if (p.out_heads > 1) {                  // virtual row r = h * n + row -> output row row * H + h
+        const int32_t n = p.R / p.out_heads;
+        ro = static_cast<int64_t>(r % n) * p.out_heads + r / n;
+    }
+    int32_t *oi = p.out_idx + ro * p.k;
+    float *ov = p.out_val ? p.out_val + ro * p.k : nullptr;
     for (int32_t i = threadIdx.x; i < p.k; i += NT) {
         if (i < kk) {
             const uint64_t e = buf[i];

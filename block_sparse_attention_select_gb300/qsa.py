@@ -100,6 +100,10 @@ def load(path: str = LIB_PATH):
                                          ctypes.c_float, vp, vp]
     lib.qsa_rope_table.restype = ctypes.c_int
     lib.qsa_rope_table.argtypes = [vp, i32, i32, ctypes.c_double, vp]
+    lib.qsa_block_select_workspace_bytes.restype = sz
+    lib.qsa_block_select_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.qsa_block_select.restype = ctypes.c_int
+    lib.qsa_block_select.argtypes = [vp, i32, i32, vp, i32, vp, i32, i32, vp, vp, i32, vp, vp, vp, sz, vp]
     lib.qsa_index_key_produce.restype = ctypes.c_int
     lib.qsa_index_key_produce.argtypes = [vp, vp, i32, vp, vp, i32, vp, ctypes.c_float, vp, i32, i32, i32,
                                           kp, vp]
@@ -275,6 +279,32 @@ def sparse_attention(q, k_cache, v_cache, block_table, row_req, row_token, sel, 
                                      _ptr(out), _stream(stream))
     _check(st, "qsa_sparse_attention")
     return out
+
+
+def block_select(q, k_cache, block_table, row_req, row_token, k: int, out_idx=None, out_val=None, ws=None,
+                 stream=None, with_values: bool = True):
+    """Block scorer (the M3-style second workload): top-k 128-token blocks per
+    (row, head) by the maximum query-key dot product over each block's visible
+    tokens.  q FP16 [R, H, 128]; k_cache FP16 [pages, 128, H, 128]; block_table
+    int32 [B, max_blocks]; row_req, row_token int32 [R].  Returns (int32 [R, H,
+    k], FP32 [R, H, k] or None)."""
+    _need(q, torch.float16, "q"), _need(k_cache, torch.float16, "k_cache")
+    _need(block_table, torch.int32, "block_table"), _need(row_req, torch.int32, "row_req")
+    _need(row_token, torch.int32, "row_token")
+    R, H = int(q.shape[0]), int(q.shape[1])
+    nb, mb = int(block_table.shape[0]), int(block_table.shape[1])
+    if out_idx is None:
+        out_idx = torch.empty((R, H, k), dtype=torch.int32, device=q.device)
+    if out_val is None and with_values:
+        out_val = torch.empty((R, H, k), dtype=torch.float32, device=q.device)
+    if ws is None:
+        n = int(load().qsa_block_select_workspace_bytes(R, H, mb, int(k)))
+        ws = torch.empty(n, dtype=torch.uint8, device=q.device)
+    st = load().qsa_block_select(_ptr(q), R, H, _ptr(k_cache), int(k_cache.shape[0]), _ptr(block_table), nb, mb,
+                                 _ptr(row_req), _ptr(row_token), int(k), _ptr(out_idx), _ptr(out_val), _ptr(ws),
+                                 ws.numel(), _stream(stream))
+    _check(st, "qsa_block_select")
+    return out_idx, out_val
 
 
 def get_device_status(stream=None) -> int:

@@ -404,3 +404,11 @@ def make_block_scorer_inputs(name: str, *, seed: int, ctx_tokens, rows_per_req, 
         q = rng.standard_normal((R, heads, HEAD_DIM)).astype(np.float16)
     return BlockScorerInputs(name, q, k_cache, block_table, np.array(rows_req, np.int32),
                              np.array(rows_tok, np.int32), k)
+
+
+def block_scorer_bench(seed: int = 41) -> BlockScorerInputs:
+    """The indexer bench's prefill chunk for the block scorer: 1,616 query rows at
+    the end of a 184,320-token context, 2 KV heads, the top 16 blocks of 128
+    tokens (a 2,048-token budget) per row and head."""
+    return make_block_scorer_inputs("blocks_1x1616rows_ctx184320_h2_k16", seed=seed, ctx_tokens=[184_320],
+                                    rows_per_req=[1616], k=16, heads=2)

@@ -192,6 +192,32 @@ qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const v
                                 const int32_t *row_req, const int32_t *row_token, const int32_t *sel, int32_t k,
                                 float scale, float *out, void *stream);
 
+/* ---- Second workload: the MiniMax-M3-style block scorer ------------------
+ * ("spec(MODEL-MM-QWEN4-EXP) ...", section "The component deep-dives", where
+ * M3 is set against QSA: a block's score is the maximum of the raw-token
+ * query-key dot products over the block, with no pooling, no ReLU and no
+ * reduction over heads; index heads equal KV heads, so each query token gets
+ * one block set per head; blocks of 128 tokens, the KV page size.)  This
+ * library's reading: row r is a query at token t = row_token[r] of request b
+ * = row_req[r]; for each head h,
+ *   score[r, h, c] = max over tokens p of block c with p <= t of q[r,h,:] . K[p,h,:]
+ *   (FP16 inputs, FP32 accumulation), block c holding tokens 128c .. 128c+127,
+ * for the blocks c <= t / 128 that hold a visible token; out_idx[r, h, :]
+ * holds the top-k blocks by (score desc, block index asc), -1 after them, and
+ * out_val (optional) their scores, -inf after them.
+ * q: FP16 [rows, H, 128]; k_cache: FP16 [num_pages, 128, H, 128] (one page
+ * per block), block c of request b at page block_table[b * max_blocks + c];
+ * out_idx int32 / out_val FP32 [rows, H, k].  q and k_cache 16-byte aligned;
+ * 1 <= H <= 16; 0 <= k <= QSA_MAX_K.  ws: qsa_block_select_workspace_bytes(rows,
+ * H, max_blocks, k) bytes, 256-byte aligned.  Device-side problems (row_req
+ * out of range, a negative token, a page id outside the cache) are reported
+ * by qsa_get_device_status() (a bad page reads as zeros). */
+size_t qsa_block_select_workspace_bytes(int32_t rows, int32_t H, int32_t max_blocks, int32_t k);
+qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *k_cache, int32_t num_pages,
+                            const int32_t *block_table, int32_t num_reqs, int32_t max_blocks,
+                            const int32_t *row_req, const int32_t *row_token, int32_t k, int32_t *out_idx,
+                            float *out_val, void *ws, size_t ws_bytes, void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *qsa_status_string(qsa_status status);
 

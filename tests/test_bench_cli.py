@@ -1,5 +1,5 @@
 """bench.py's command line on a machine without a GPU: the reference arms of
-the producer and consumer modes print one JSON line and exit 0 (their oracle
+the producer, consumer and block-scorer modes print one JSON line and exit 0 (their oracle
 timing lives in the GPU arm's cpu_baseline), and every mode is listed."""
 import json
 import os
@@ -16,7 +16,7 @@ def _run(*args):
 
 
 def test_reference_arms_of_the_neighbouring_steps():
-    for op in ("produce", "attend"):
+    for op in ("produce", "attend", "blocks"):
         rc, out = _run("--op", op, "--impl", "reference")
         assert rc == 0
         line = json.loads(out.strip().splitlines()[-1])
@@ -26,5 +26,5 @@ def test_reference_arms_of_the_neighbouring_steps():
 def test_help_lists_every_mode():
     rc, out = _run("--help")
     assert rc == 0
-    for word in ("select", "produce", "attend", "--producer-workload", "--window"):
+    for word in ("select", "produce", "attend", "blocks", "--producer-workload", "--window"):
         assert word in out

@@ -1,0 +1,106 @@
+"""GPU parity of the M3-style block scorer (qsa_block_select) against its
+oracle (oracle/block_scorer.py, numpy float64).
+
+A block's score is the maximum raw-token dot product over its visible tokens,
+per query row and KV head; the top-k blocks are ordered by score, then block
+index.  Integer-valued inputs make every FP32 dot product exact, so indices
+and values must match bit for bit; on Gaussian inputs the values must agree
+within |g - o| <= 1e-3 |o| + 1e-6 and the selected sets may differ only at
+near-ties of the cut.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import block_scorer as BS
+from block_sparse_attention_select_gb300 import qsa
+from block_sparse_attention_select_gb300 import workloads as W
+
+from gpu_util import ATOL, RTOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    qsa.load()
+    assert torch.cuda.is_available()
+    yield
+    assert qsa.get_device_status() == qsa.QSA_OK
+
+
+def _run(inp, k=None, block_table=None):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bt = inp.block_table if block_table is None else block_table
+    gi, gv = qsa.block_select(t(inp.q), t(inp.k_cache), t(bt), t(inp.row_req), t(inp.row_token),
+                              inp.k if k is None else k)
+    return gi.cpu().numpy(), gv.cpu().numpy()
+
+
+def _oracle_scores(inp, r, h):
+    b, tok = int(inp.row_req[r]), int(inp.row_token[r])
+    pages = inp.block_table[b, : tok // 128 + 1]
+    keys = inp.k_cache[pages].reshape(-1, inp.k_cache.shape[2], 128)
+    return BS.block_scores(inp.q[r, h], keys[:, h], tok)
+
+
+CASES = [
+    # (ctx tokens per request, rows per request, k, heads, dist)
+    ([3000, 700, 129], [300, 5, 2], 8, 1, "int"),
+    ([5000, 1000], [40, 300], 12, 2, "int"),
+    ([2000, 4100, 260], [70, 9, 3], 16, 4, "int"),
+    ([9000], [600], 20, 2, "int"),
+    ([6000, 3000], [100, 40], 16, 2, "gauss"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"c{i}" for i in range(len(CASES))])
+def test_block_scorer_against_oracle(case):
+    ctx, rows, k, heads, dist = case
+    inp = W.make_block_scorer_inputs("blk", seed=sum(ctx) % 997, ctx_tokens=ctx, rows_per_req=rows, k=k,
+                                     heads=heads, dist=dist)
+    gi, gv = _run(inp)
+    oi, ov = BS.select_blocks(inp.q, inp.k_cache, inp.block_table, inp.row_req, inp.row_token, k)
+    assert qsa.get_device_status() == qsa.QSA_OK
+    if dist == "int":
+        np.testing.assert_array_equal(gi, oi)
+        np.testing.assert_array_equal(gv, ov.astype(np.float32))
+        return
+    R, H, _ = gi.shape
+    for r in range(R):
+        for h in range(H):
+            sc = _oracle_scores(inp, r, h)
+            n = min(k, len(sc))
+            assert np.all(gi[r, h, n:] == -1) and np.all(np.isneginf(gv[r, h, n:]))
+            sel = gi[r, h, :n]
+            assert len(np.unique(sel)) == n and np.all((sel >= 0) & (sel < len(sc)))
+            o = sc[sel]
+            assert np.all(np.abs(gv[r, h, :n] - o) <= RTOL * np.abs(o) + ATOL), (r, h)
+            assert np.all(np.diff(gv[r, h, :n].astype(np.float64)) <= 0)
+            kth = sc[oi[r, h, n - 1]]
+            for c in set(sel.tolist()) ^ set(oi[r, h, :n].tolist()):
+                assert abs(sc[c] - kth) <= RTOL * abs(kth) + ATOL, (r, h, c)
+
+
+def test_block_scorer_k_above_visible_blocks_and_ties():
+    # every dot product 0 (q = 0): all visible blocks tie, in index order, and
+    # k exceeds the visible count of the short rows
+    inp = W.make_block_scorer_inputs("tie", seed=3, ctx_tokens=[1000, 200], rows_per_req=[20, 6], k=9, heads=2,
+                                     dist="int")
+    inp.q[:] = 0
+    gi, gv = _run(inp)
+    oi, ov = BS.select_blocks(inp.q, inp.k_cache, inp.block_table, inp.row_req, inp.row_token, inp.k)
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov.astype(np.float32))
+    assert np.any(gi == -1)
+
+
+def test_block_scorer_bad_page_is_reported():
+    inp = W.make_block_scorer_inputs("bp", seed=4, ctx_tokens=[2000], rows_per_req=[5], k=4, heads=2, dist="int")
+    bt = inp.block_table.copy()
+    bt[0, 2] = inp.k_cache.shape[0] + 50
+    _run(inp, block_table=bt)
+    assert qsa.get_device_status() == qsa.QSA_ERR_BAD_PAGE
+    assert qsa.get_device_status() == qsa.QSA_OK
