@@ -37,6 +37,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int64_t> g_cfg_path{0};
 std::atomic<bool> g_overlap{true};          // dependent launches inside a call (QSA_CFG_OVERLAP)
 std::atomic<uint64_t> g_wait_ns{2000000000ull};
+std::atomic<int> g_cluster{0};              // candidate selector CTAs per row (QSA_CFG_CLUSTER)
 thread_local int32_t g_launches = 0;
 
 // Optional per-launch CUDA-event timing (test / benchmark instrument).
@@ -406,6 +407,11 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
         g_overlap = value != 0;
         return QSA_OK;
     }
+    if (key == QSA_CFG_CLUSTER) {
+        if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8)) return QSA_ERR_INVALID_ARG;
+        g_cluster = static_cast<int>(value);
+        return QSA_OK;
+    }
     if (key == QSA_CFG_WAIT_LIMIT_NS) {
         if (value <= 0) return QSA_ERR_INVALID_ARG;
         g_wait_ns = static_cast<uint64_t>(value);
@@ -415,6 +421,8 @@ qsa_status qsa_set_config(int32_t key, int64_t value)
 }
 
 int32_t qsa_last_launch_count(void) { return g_launches; }
+
+int32_t qsa_last_cluster_size(void) { return qsa::last_cluster; }
 
 qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const void *k_cache, const void *v_cache,
                                 int32_t num_pages, int32_t page_tokens, int32_t hkv, int32_t head_dim,
@@ -727,7 +735,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     cs.num_pages = keys->num_pages;
     cs.page_pos = keys->page_positions;
     cs.fb_scores = cand_score;
-    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, g_overlap, stream); }));
+    return launch_rc(timed(K_SEL_CAND, stream, [&] { return launch_select(cs, rows, g_overlap, stream, g_cluster); }));
 }
 
 size_t qsa_block_select_workspace_bytes(int32_t rows, int32_t H, int32_t max_blocks, int32_t k)

@@ -185,9 +185,15 @@ int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, i
                 uint32_t *status, void *stream);
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
                  int grid, bool overlap, void *stream);
-int launch_select(const SelectParams &p, int grid, bool overlap, void *stream);
+// cluster_pref (SEL_CAND only): CTAs per row of the candidate selector, 0 =
+// automatic (a thread-block cluster per row when rows are fewer than SMs, its
+// size from the device's occupancy query), 1 = one CTA per row, 2 / 4 / 8 =
+// that cluster size (capped by the query)
+int launch_select(const SelectParams &p, int grid, bool overlap, void *stream, int cluster_pref = 0);
 size_t select_smem_bytes(int32_t smem_cap);
 size_t cand_smem_bytes(int32_t k, int32_t cap);
+size_t cand_cluster_smem_bytes(int32_t k, int32_t cap);
+extern int last_cluster;    // CTAs per row of the most recent candidate-selector launch
 uint32_t score_smem_bytes();
 int launch_pad(float *logits, int64_t ld, int32_t R, const int32_t *row_vis, bool overlap, void *stream);
 // Block scorer rows: for v = h * R + r, vreq[v] = row_req[r] + h * num_reqs (or

@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "qsa_device.cuh"
@@ -691,6 +692,109 @@ __device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Gathers the candidates of quarters [e_lo, e_hi) of row r (layout in
+// qsa_internal.h).  Thread t takes quarters e_lo + t, e_lo + t + CT, ... in
+// rounds of QPR: their mask words are loaded together, one block scan gives
+// the thread's offset, and each candidate's score is copied asynchronously
+// from its slot (slot row j of quarter q at float 4j + q of the (tile, row)
+// region) to a_key[done + ...], its ~position to a_pos.  Stops with overflow
+// set (the count past cap) instead of writing past cap.  The copies are
+// complete after cp_async_wait_all() and a barrier.
+__device__ __forceinline__ void gather_quarters(const SelectParams &p, int32_t r, int32_t e_lo, int32_t e_hi,
+                                                uint32_t *a_key, uint32_t *a_pos, CandShared &sh, int &sbuf,
+                                                uint32_t &done, bool &overflow)
+{
+    const int t = threadIdx.x;
+    const uint32_t *mrow = p.cand_mask + static_cast<int64_t>(r) * p.tiles_ld * 4;
+    const float *srow = p.cand_score + static_cast<int64_t>(r) * TILE_M;    // tile t at + t * R * TILE_M
+    for (int32_t e0 = e_lo; e0 < e_hi; e0 += QPR * CT) {
+        uint32_t m[QPR], cnt = 0;
+#pragma unroll
+        for (int u = 0; u < QPR; ++u) {
+            const int32_t e = e0 + t + u * CT;
+            m[u] = e < e_hi ? __ldcg(mrow + e) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < QPR; ++u) cnt += __popc(m[u]);
+        uint32_t ctot;
+        const uint32_t before = cand_scan(cnt, sh.wtot[sbuf], ctot);
+        sbuf ^= 1;
+        if (done + ctot > static_cast<uint32_t>(p.cap)) { overflow = true; return; }   // uniform
+        uint32_t o = done + before;
+#pragma unroll
+        for (int u = 0; u < QPR; ++u) {
+            const int32_t e = e0 + t + u * CT;
+            uint32_t mm = m[u];
+            const int32_t tile = e >> 2, q = e & 3;
+            const float *slot = srow + static_cast<int64_t>(tile) * p.R * TILE_M + q;
+            const uint32_t pos0 = static_cast<uint32_t>(tile * TILE_M + q * 32);
+            for (uint32_t j = 0; mm != 0u; ++j) {
+                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
+                mm &= mm - 1u;
+                cp_async4(a_key + o, slot + 4 * j);
+                a_pos[o] = ~(pos0 + bit);
+                ++o;
+            }
+        }
+        done += ctot;
+    }
+}
+
+// a_key[0, n): scores -> order-preserving keys; block-wide min and max (the
+// barrier inside also publishes a_key to the block).
+__device__ __forceinline__ void keys_and_range(uint32_t *a_key, uint32_t n, CandShared &sh, uint32_t &kmin,
+                                               uint32_t &kmax)
+{
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    kmin = 0xffffffffu;
+    kmax = 0u;
+    for (uint32_t i = t; i < n; i += CT) {
+        const uint32_t key = score_key(__uint_as_float(a_key[i]));
+        a_key[i] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    }
+    if (lane == 0) { sh.red_min[wid] = kmin; sh.red_max[wid] = kmax; }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < CT / 32; ++w) { kmin = min(kmin, sh.red_min[w]); kmax = max(kmax, sh.red_max[w]); }
+}
+
+// One counting pass over the keys >= lo of a_key[0, n) into 11-bit buckets of
+// width 2^shift (bucket 0 holds the largest keys), sh.hist zero on entry;
+// leaves in sh.hist each bucket's start (the scatter cursors) and returns the
+// bucket holding the kk-th largest key (bb) and the end of that bucket (need).
+__device__ __forceinline__ void count_and_cut(const uint32_t *a_key, uint32_t n, uint32_t lo, int shift, uint32_t kk,
+                                              CandShared &sh, int &sbuf, uint32_t &bb, uint32_t &need)
+{
+    const int t = threadIdx.x;
+    for (uint32_t i = t; i < n; i += CT) {
+        const uint32_t key = a_key[i];
+        if (key >= lo) atomicAdd(&sh.hist[NBINS - 1 - ((key - lo) >> shift)], 1u);
+    }
+    __syncthreads();
+    uint32_t c[BPT], sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) { c[i] = sh.hist[BPT * t + i]; sum += c[i]; }
+    uint32_t all;
+    uint32_t start = cand_scan(sum, sh.wtot[sbuf], all);
+    sbuf ^= 1;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+        if (start < kk && kk <= start + c[i]) { sh.cut = BPT * t + i; sh.need = start + c[i]; }
+        sh.hist[BPT * t + i] = start;        // scatter cursor
+        start += c[i];
+    }
+    __syncthreads();
+    bb = sh.cut;
+    need = sh.need;
+}
+
 __global__ void __launch_bounds__(CT, 3)
 cand_kernel(const SelectParams p)
 {
@@ -724,47 +828,11 @@ cand_kernel(const SelectParams p)
     const int32_t ntile = (V + TILE_M - 1) / TILE_M;
     const int32_t nq = ntile * 4;
     const uint32_t *mrow = p.cand_mask + static_cast<int64_t>(r) * p.tiles_ld * 4;
-    const float *srow = p.cand_score + static_cast<int64_t>(r) * TILE_M;    // tile t at + t * R * TILE_M
 
-    // ---- gather.  Thread t takes quarters e = t, t + CT, ... in rounds of
-    //      QPR: their mask words are loaded together, one block scan gives
-    //      the thread's offset, and each candidate's score is copied
-    //      asynchronously from its slot (row j of quarter q at float 4j + q
-    //      of the (tile, row) region) to its place in a_key.
     uint32_t done = 0;
     bool overflow = false;
     int sbuf = 0;
-    for (int32_t e0 = 0; e0 < nq; e0 += QPR * CT) {
-        uint32_t m[QPR], cnt = 0;
-#pragma unroll
-        for (int u = 0; u < QPR; ++u) {
-            const int32_t e = e0 + t + u * CT;
-            m[u] = e < nq ? __ldcg(mrow + e) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < QPR; ++u) cnt += __popc(m[u]);
-        uint32_t ctot;
-        const uint32_t before = cand_scan(cnt, sh.wtot[sbuf], ctot);
-        sbuf ^= 1;
-        if (done + ctot > static_cast<uint32_t>(p.cap)) { overflow = true; break; }   // uniform
-        uint32_t o = done + before;
-#pragma unroll
-        for (int u = 0; u < QPR; ++u) {
-            const int32_t e = e0 + t + u * CT;
-            uint32_t mm = m[u];
-            const int32_t tile = e >> 2, q = e & 3;
-            const float *slot = srow + static_cast<int64_t>(tile) * p.R * TILE_M + q;
-            const uint32_t pos0 = static_cast<uint32_t>(tile * TILE_M + q * 32);
-            for (uint32_t j = 0; mm != 0u; ++j) {
-                const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
-                mm &= mm - 1u;
-                cp_async4(a_key + o, slot + 4 * j);
-                a_pos[o] = ~(pos0 + bit);
-                ++o;
-            }
-        }
-        done += ctot;
-    }
+    gather_quarters(p, r, 0, nq, a_key, a_pos, sh, sbuf, done, overflow);
     cp_async_wait_all();
     __syncthreads();
     // every mask word of the row has been read: drop its lines from L2 unwritten
@@ -775,53 +843,41 @@ cand_kernel(const SelectParams p)
         return;
     }
     // ---- scores -> order-preserving keys, and their range
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    for (uint32_t i = t; i < n; i += CT) {
-        const uint32_t key = score_key(__uint_as_float(a_key[i]));
-        a_key[i] = key;
-        kmin = min(kmin, key);
-        kmax = max(kmax, key);
-    }
-    // block min / max of the keys; the barrier also publishes a_key[]
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    }
-    if (lane == 0) { sh.red_min[wid] = kmin; sh.red_max[wid] = kmax; }
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < CT / 32; ++w) { kmin = min(kmin, sh.red_min[w]); kmax = max(kmax, sh.red_max[w]); }
+    uint32_t kmin, kmax;
+    keys_and_range(a_key, n, sh, kmin, kmax);
     const uint32_t kk = min(static_cast<uint32_t>(p.k), n);
     int32_t *oi = p.out_idx + static_cast<int64_t>(r) * p.k;
     float *ov = p.out_val ? p.out_val + static_cast<int64_t>(r) * p.k : nullptr;
     if (kk > 0) {
-        // ---- counting pass: bucket 0 holds the largest keys
-        const int shift = span_shift(kmax - kmin);
-        for (uint32_t i = t; i < n; i += CT)
-            atomicAdd(&sh.hist[NBINS - 1 - ((a_key[i] - kmin) >> shift)], 1u);
-        __syncthreads();
-        uint32_t c[BPT], sum = 0;
-#pragma unroll
-        for (int i = 0; i < BPT; ++i) { c[i] = sh.hist[BPT * t + i]; sum += c[i]; }
-        uint32_t all;
-        uint32_t start = cand_scan(sum, sh.wtot[sbuf], all);
-#pragma unroll
-        for (int i = 0; i < BPT; ++i) {
-            if (start < kk && kk <= start + c[i]) { sh.cut = BPT * t + i; sh.need = start + c[i]; }
-            sh.hist[BPT * t + i] = start;        // scatter cursor
-            start += c[i];
+        // ---- counting pass: bucket 0 holds the largest keys; when the
+        //      buckets down to the cut span a much narrower key range than
+        //      all candidates (every position a candidate: scores down to the
+        //      spike of exact zeros), count once more over that range only, so
+        //      that the buckets to be ordered stay small
+        uint32_t lo = kmin;
+        int shift = span_shift(kmax - kmin);
+        uint32_t bb = 0, need = 0;
+        for (int level = 0; level < 2; ++level) {
+            count_and_cut(a_key, n, lo, shift, kk, sh, sbuf, bb, need);
+            if (level == 1 || shift == 0) break;
+            const uint32_t lo2 = lo + (static_cast<uint32_t>(NBINS - 1 - bb) << shift);
+            const int shift2 = span_shift(kmax - lo2);
+            if (shift2 + 3 > shift) break;                         // uniform
+            lo = lo2;
+            shift = shift2;
+            for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
+            __syncthreads();
         }
-        __syncthreads();
-        const uint32_t bb = sh.cut, need = sh.need;
         if (need > static_cast<uint32_t>(p.k + SLACK)) {           // uniform: huge tie bucket at the cut
             fallback();
             return;
         }
+        const uint32_t kmin_sel = lo;                              // every ordered key is >= lo
         // ---- scatter the buckets down to the cut
         for (uint32_t i = t; i < n; i += CT) {
             const uint32_t key = a_key[i];
-            const uint32_t b = NBINS - 1 - ((key - kmin) >> shift);
+            if (key < lo) continue;
+            const uint32_t b = NBINS - 1 - ((key - lo) >> shift);
             if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = (static_cast<uint64_t>(key) << 32) | a_pos[i];
         }
         __syncthreads();
@@ -840,7 +896,7 @@ cand_kernel(const SelectParams p)
                 x[h] = 0ull;
                 if (pos < need) {
                     x[h] = bq[pos];
-                    const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x[h] >> 32) - kmin) >> shift);
+                    const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x[h] >> 32) - kmin_sel) >> shift);
                     s0[h] = b ? sh.hist[b - 1] : 0u;
                     const uint32_t e = sh.hist[b];
                     if (e - s0[h] > RANK_MAX) {
@@ -883,6 +939,298 @@ cand_kernel(const SelectParams p)
         if (ov) ov[i] = -__int_as_float(0x7f800000);
     }
     if (t == 0) p.row_flag[r] = 0;
+}
+
+// ---------------------------------------------------- cluster candidates --
+//
+// The same selection for batches with fewer rows than the GPU has SMs (decode
+// batches): the C CTAs of a thread-block cluster share one row, and their
+// shared memories are joined through distributed shared memory.
+//  1. CTA c gathers quarters [c nq / C, (c + 1) nq / C) of the row, makes
+//     keys and takes their range;
+//  2. every CTA reads the C counts and ranges (the row's key range is then
+//     known to all), counts its keys into the row's 11-bit buckets, and after
+//     a cluster barrier sums the C histograms, which gives each bucket's place
+//     in the output and this CTA's cursor inside it (the CTAs before it in the
+//     cluster come first);
+//  3. every CTA writes its keys of the buckets down to the cut into CTA 0's
+//     ordered buffer (remote stores);
+//  4. CTA c owns the buckets that start in its share [c need / C, (c + 1)
+//     need / C) of the buffer, copies them into its own shared memory first,
+//     ranks their elements and writes them out.
+// Every CTA takes the same cluster barriers (the decisions between them are
+// made from the same summed data); a row that cannot be certified is re-scored
+// by CTA 0 alone after the last barrier.  The cluster size comes from the
+// device's occupancy query at launch, never from the compute capability.
+struct ClusterInfo {
+    uint32_t n, kmin, kmax, overflow;
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(v));
+    return v;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t v;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(v));
+    return v;
+}
+// All threads of all CTAs of the cluster; orders shared-memory writes before
+// it with remote reads after it.
+__device__ __forceinline__ void cluster_barrier()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `local` (this CTA's shared memory) in CTA `cta` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *local, uint32_t cta)
+{
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(cta));
+    return a;
+}
+// Remote loads carry no memory clobber: the cluster barriers order them with
+// the writes they read, and the compiler may issue several before the first
+// result is used.
+__device__ __forceinline__ uint4 peer_ld128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint64_t peer_ld64(uint32_t a)
+{
+    uint64_t v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void peer_st64(uint32_t a, uint64_t v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(CT, 2)
+cand_cluster_kernel(const SelectParams p)
+{
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    CandShared &sh = *reinterpret_cast<CandShared *>(smem_raw);                 // hist: summed counts
+    uint64_t *bq = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD);          // k + SLACK entries
+    uint32_t *a_key = reinterpret_cast<uint32_t *>(bq + p.k + SLACK);            // cap: scores, then keys
+    uint32_t *a_pos = a_key + p.cap;                                             // cap: ~position
+    // NBINS: this CTA's counts, 16-byte aligned for the peers' vector loads
+    uint32_t *own = reinterpret_cast<uint32_t *>((reinterpret_cast<uintptr_t>(a_pos + p.cap) + 15) & ~uintptr_t{15});
+    uint32_t *bstart = own + NBINS;                                              // NBINS: bucket starts
+    ClusterInfo &ci = *reinterpret_cast<ClusterInfo *>(bstart + NBINS);
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const uint32_t C = cluster_nctarank(), c = cluster_ctarank();
+    const int32_t r = static_cast<int32_t>(blockIdx.x / C);
+    for (int i = t; i < NBINS; i += CT) own[i] = 0;
+    if (t == 0) sh.nbig = 0;
+    wait_prior_grid();                      // last kernel of its call: nothing to allow
+    int32_t V = p.row_vis[r];
+    if (V < 0 || V > p.max_len) {
+        if (t == 0 && c == 0) record_error(p.status, ST_BAD_ROW);
+        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
+    }
+    const int32_t kk_target = min(p.k, V);
+    const int32_t nq = ((V + TILE_M - 1) / TILE_M) * 4;
+
+    // ---- 1. this CTA's slice
+    uint32_t done = 0;
+    bool overflow = false;
+    int sbuf = 0;
+    gather_quarters(p, r, static_cast<int32_t>(static_cast<int64_t>(nq) * c / C),
+                    static_cast<int32_t>(static_cast<int64_t>(nq) * (c + 1) / C), a_key, a_pos, sh, sbuf, done,
+                    overflow);
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    if (!overflow) keys_and_range(a_key, done, sh, kmin, kmax);   // uniform in the CTA
+    if (t == 0) ci = ClusterInfo{done, kmin, kmax, overflow ? 1u : 0u};
+    cluster_barrier();                                                          // (1)
+    // ---- 2. the row's count and key range
+    uint32_t n = 0, any_over = 0;
+    {
+        uint4 info[8];                      // C <= 8: every load issued before the first is used
+#pragma unroll
+        for (uint32_t x = 0; x < 8; ++x)
+            if (x < C) info[x] = peer_ld128(peer_addr(&ci, x));
+#pragma unroll
+        for (uint32_t x = 0; x < 8; ++x) {
+            if (x >= C) break;
+            n += info[x].x;
+            kmin = min(kmin, info[x].y);
+            kmax = max(kmax, info[x].z);
+            any_over |= info[x].w;
+        }
+    }
+    auto finish_fallback = [&]() {
+        cluster_barrier();                  // nobody reads this CTA's shared memory any more
+        if (c != 0) return;
+        if (t == 0) {
+            p.row_flag[r] = 1;
+            atomicExch(&p.plan->any_fallback, 1);
+        }
+        __syncthreads();
+        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), bq, a_key, a_pos, p.cap);
+    };
+    if (any_over || n > static_cast<uint32_t>(p.cap) || n < static_cast<uint32_t>(kk_target)) {   // cluster-uniform
+        finish_fallback();
+        return;
+    }
+    int32_t *oi = p.out_idx + static_cast<int64_t>(r) * p.k;
+    float *ov = p.out_val ? p.out_val + static_cast<int64_t>(r) * p.k : nullptr;
+    if (n == 0) {                           // cluster-uniform: nothing visible, all padding
+        cluster_barrier();
+        if (c == 0) {
+            for (int32_t i = t; i < p.k; i += CT) {
+                oi[i] = -1;
+                if (ov) ov[i] = -__int_as_float(0x7f800000);
+            }
+            if (t == 0) p.row_flag[r] = 0;
+        }
+        return;
+    }
+    const uint32_t kk = min(static_cast<uint32_t>(p.k), n);   // >= 1
+    // counting rounds over the keys >= lo (a second, narrower one when the
+    // buckets down to the cut span a much smaller key range, as in the
+    // one-CTA selector); each sums the C histograms between two barriers
+    uint32_t lo = kmin;
+    int shift = span_shift(kmax - kmin);
+    uint32_t bb = 0, need = 0;
+    for (int level = 0; level < 2; ++level) {
+        for (uint32_t i = t; i < done; i += CT) {
+            const uint32_t key = a_key[i];
+            if (key >= lo) atomicAdd(&own[NBINS - 1 - ((key - lo) >> shift)], 1u);
+        }
+        __syncthreads();
+        cluster_barrier();                                                      // (2) every count is in
+        // summed counts of this thread's BPT buckets and this CTA's share before it
+        uint32_t cnt[BPT], mine_before[BPT], sum = 0;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) { cnt[i] = 0; mine_before[i] = 0; }
+        static_assert(BPT == 8, "two 16-byte loads per CTA and thread");
+        {
+            uint4 h[8][2];                  // C <= 8: all loads in flight before the sums
+#pragma unroll
+            for (uint32_t x = 0; x < 8; ++x) {
+                if (x < C) {
+                    const uint32_t a = peer_addr(own + BPT * t, x);
+                    h[x][0] = peer_ld128(a);
+                    h[x][1] = peer_ld128(a + 16);
+                }
+            }
+#pragma unroll
+            for (uint32_t x = 0; x < 8; ++x) {
+                if (x >= C) break;
+                const uint32_t v[8] = {h[x][0].x, h[x][0].y, h[x][0].z, h[x][0].w,
+                                       h[x][1].x, h[x][1].y, h[x][1].z, h[x][1].w};
+#pragma unroll
+                for (int i = 0; i < BPT; ++i) {
+                    if (x < c) mine_before[i] += v[i];
+                    cnt[i] += v[i];
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) sum += cnt[i];
+        uint32_t all;
+        uint32_t start = cand_scan(sum, sh.wtot[sbuf], all);
+        sbuf ^= 1;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+            const int b = BPT * t + i;
+            if (start < kk && kk <= start + cnt[i]) { sh.cut = b; sh.need = start + cnt[i]; }
+            bstart[b] = start;
+            sh.hist[b] = start + mine_before[i];            // this CTA's scatter cursor in bucket b
+            start += cnt[i];
+        }
+        __syncthreads();
+        bb = sh.cut;
+        need = sh.need;
+        cluster_barrier();                                                      // (3) counts read everywhere
+        if (level == 1 || shift == 0) break;
+        const uint32_t lo2 = lo + (static_cast<uint32_t>(NBINS - 1 - bb) << shift);
+        const int shift2 = span_shift(kmax - lo2);
+        if (shift2 + 3 > shift) break;                                          // cluster-uniform
+        lo = lo2;
+        shift = shift2;
+        for (int i = t; i < NBINS; i += CT) own[i] = 0;
+        __syncthreads();
+    }
+    if (need > static_cast<uint32_t>(p.k + SLACK)) {         // cluster-uniform: huge tie bucket at the cut
+        finish_fallback();
+        return;
+    }
+    // ---- 3. this CTA's keys of the buckets down to the cut -> CTA 0's buffer
+    const uint32_t bq0 = peer_addr(bq, 0);
+    for (uint32_t i = t; i < done; i += CT) {
+        const uint32_t key = a_key[i];
+        if (key < lo) continue;
+        const uint32_t b = NBINS - 1 - ((key - lo) >> shift);
+        if (b <= bb) peer_st64(bq0 + 8u * atomicAdd(&sh.hist[b], 1u), (static_cast<uint64_t>(key) << 32) | a_pos[i]);
+    }
+    cluster_barrier();                                                          // (4) CTA 0's buffer complete
+    // ---- 4. the buckets starting in this CTA's share of the buffer
+    auto bucket_of = [&](uint32_t pos) {    // last bucket whose start is <= pos (bstart is non-decreasing)
+        int lo = 0, hi = NBINS - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (bstart[mid] <= pos) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+    auto first_start_at_or_after = [&](uint32_t pos) -> uint32_t {
+        if (pos >= need) return need;
+        const int b = bucket_of(pos);
+        return bstart[b] == pos ? pos : (b + 1 < NBINS ? bstart[b + 1] : need);
+    };
+    const uint32_t s_lo = first_start_at_or_after(static_cast<uint32_t>(static_cast<uint64_t>(need) * c / C));
+    const uint32_t s_hi = c + 1 == C ? need : first_start_at_or_after(static_cast<uint32_t>(static_cast<uint64_t>(need) * (c + 1) / C));
+    // copy [s_lo, s_hi) of CTA 0's buffer to the front of this CTA's own one
+    // (CTA 0 ranks its share in place)
+    uint64_t *loc = bq;
+    const int64_t shift_pos = c == 0 ? 0 : static_cast<int64_t>(s_lo);
+    if (c != 0)
+        for (uint32_t i = s_lo + t; i < s_hi; i += CT) loc[i - s_lo] = peer_ld64(bq0 + 8u * i);
+    __syncthreads();
+    for (uint32_t pos = s_lo + t; pos < s_hi; pos += CT) {
+        const uint64_t x = loc[pos - shift_pos];
+        const uint32_t b = NBINS - 1 - ((static_cast<uint32_t>(x >> 32) - lo) >> shift);
+        const uint32_t s0 = bstart[b], e = b + 1 < NBINS ? bstart[b + 1] : need;
+        if (e - s0 > RANK_MAX) {
+            if (pos == s0) sh.big[atomicAdd(&sh.nbig, 1u)] = b;
+            continue;
+        }
+        uint32_t rk = s0;
+        for (uint32_t q = s0; q < e; ++q) rk += loc[q - shift_pos] > x;
+        if (rk < kk) {
+            oi[rk] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+            if (ov) ov[rk] = key_score(static_cast<uint32_t>(x >> 32));
+        }
+    }
+    __syncthreads();
+    for (uint32_t qb = wid; qb < sh.nbig; qb += CT / 32) {
+        const uint32_t b = sh.big[qb];
+        const uint32_t s0 = bstart[b], m = (b + 1 < NBINS ? bstart[b + 1] : need) - s0;
+        warp_sort_desc(loc + (s0 - shift_pos), static_cast<int32_t>(m));
+        for (uint32_t i = lane; i < m && s0 + i < kk; i += 32) {
+            const uint64_t x = loc[s0 - shift_pos + i];
+            oi[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+            if (ov) ov[s0 + i] = key_score(static_cast<uint32_t>(x >> 32));
+        }
+    }
+    cluster_barrier();                                                          // (5) CTA 0's buffer no longer read
+    if (c == 0) {
+        for (int32_t i = static_cast<int32_t>(kk) + t; i < p.k; i += CT) {
+            oi[i] = -1;
+            if (ov) ov[i] = -__int_as_float(0x7f800000);
+        }
+        if (t == 0) p.row_flag[r] = 0;
+    }
 }
 
 // ------------------------------------------------------------- threshold --
@@ -1093,7 +1441,59 @@ size_t cand_smem_bytes(int32_t k, int32_t cap)
     return CAND_HEAD + static_cast<size_t>(k + SLACK) * 8 + static_cast<size_t>(cap) * 8;
 }
 
-int launch_select(const SelectParams &p, int grid, bool overlap, void *stream)
+size_t cand_cluster_smem_bytes(int32_t k, int32_t cap)
+{
+    return cand_smem_bytes(k, cap) + 16 + 2 * NBINS * 4 + sizeof(ClusterInfo);   // 16: alignment of the counts
+}
+
+namespace {
+
+std::mutex g_cluster_mu;
+int g_max_cluster[64][2] = {};       // per device: the queried maximum and the shared memory it was asked for
+
+// CTAs per row of the candidate selector: pref 0 (automatic) and 1 = one CTA
+// per row; 2, 4, 8 = that cluster size, capped by the largest cluster the
+// device reports it can co-schedule for this kernel and shared-memory size.
+// Automatic stays at one CTA per row: measured on the 64-row decode batch
+// (k 2,048), clusters of 2 / 4 / 8 took the selector from 18.1 us to 18.6 /
+// 24.4 / 58.6 us; the per-row phases are latency-bound and do not shrink by
+// the split as fast as the merge's barriers and remote traffic cost.
+int cand_cluster_size(const SelectParams &p, int pref)
+{
+    if (pref <= 1) return 1;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    (void)sms;
+    const int want = pref;
+    const int csmem = static_cast<int>(cand_cluster_smem_bytes(p.k, p.cap));
+    std::lock_guard<std::mutex> lk(g_cluster_mu);
+    if (g_max_cluster[dev][1] != csmem) {
+        int maxc = 1;
+        if (cudaFuncSetAttribute(cand_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, csmem) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(8);
+            cfg.blockDim = dim3(CT);
+            cfg.dynamicSmemBytes = static_cast<size_t>(csmem);
+            if (cudaOccupancyMaxPotentialClusterSize(&maxc, reinterpret_cast<const void *>(&cand_cluster_kernel), &cfg) !=
+                cudaSuccess)
+                maxc = 1;
+        }
+        cudaGetLastError();
+        g_max_cluster[dev][0] = std::max(1, std::min(8, maxc));
+        g_max_cluster[dev][1] = csmem;
+    }
+    int C = 1;
+    while (C * 2 <= std::min(want, g_max_cluster[dev][0])) C *= 2;
+    return C;
+}
+
+}  // namespace
+
+int last_cluster = 1;
+
+int launch_select(const SelectParams &p, int grid, bool overlap, void *stream, int cluster_pref)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void *args[] = {const_cast<SelectParams *>(&p)};
@@ -1117,6 +1517,37 @@ int launch_select(const SelectParams &p, int grid, bool overlap, void *stream)
         }
     }
     if (p.mode == SEL_CAND) {
+        // few rows: one thread-block cluster per row, its size from the
+        // device's occupancy query; a refused launch retries at half the size
+        // and ends at one CTA per row
+        int C = cand_cluster_size(p, cluster_pref);
+        while (C > 1) {
+            static size_t cdone[64] = {};
+            const size_t csmem = cand_cluster_smem_bytes(p.k, p.cap);
+            if (int rc = set_smem(cand_cluster_kernel, csmem, cdone)) return rc;
+            cudaLaunchAttribute attr[2];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[1].val.programmaticStreamSerializationAllowed = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(static_cast<unsigned>(p.R) * static_cast<unsigned>(C));
+            cfg.blockDim = dim3(CT);
+            cfg.dynamicSmemBytes = csmem;
+            cfg.stream = st;
+            cfg.attrs = attr;
+            cfg.numAttrs = overlap ? 2u : 1u;
+            if (cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&cand_cluster_kernel), args) == cudaSuccess &&
+                cudaGetLastError() == cudaSuccess) {
+                last_cluster = C;
+                return 0;
+            }
+            cudaGetLastError();             // refused: a smaller cluster, or none
+            C /= 2;
+        }
+        last_cluster = 1;
         static size_t done[64] = {};
         const size_t smem = cand_smem_bytes(p.k, p.cap);
         if (int rc = set_smem(cand_kernel, smem, done)) return rc;

@@ -35,6 +35,7 @@ QSA_CFG_PATH = 1
 QSA_CFG_WAIT_LIMIT_NS = 2
 QSA_CFG_KERNEL_TIMING = 3
 QSA_CFG_OVERLAP = 4
+QSA_CFG_CLUSTER = 5
 KERNEL_KINDS = ["plan", "score_logits", "score_sample", "score_filter", "unused4",
                 "select_dense", "select_thresh", "select_cand", "unused8", "pad"]
 PATH_AUTO, PATH_DENSE, PATH_FILTER = 0, 1, 2
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH):
     lib.qsa_set_config.argtypes = [i32, i64]
     lib.qsa_last_launch_count.restype = i32
     lib.qsa_last_launch_count.argtypes = []
+    lib.qsa_last_cluster_size.restype = i32
+    lib.qsa_last_cluster_size.argtypes = []
     lib.qsa_select_paged_tokens_noalloc.restype = ctypes.c_int
     lib.qsa_select_paged_tokens_noalloc.argtypes = [vp, vp, i32, i32, kp, vp, vp, i32, vp, vp, vp]
     lib.qsa_kernel_times.restype = ctypes.c_int
@@ -317,6 +320,10 @@ def set_config(key: int, value: int):
 
 def last_launch_count() -> int:
     return int(load().qsa_last_launch_count())
+
+
+def last_cluster_size() -> int:
+    return int(load().qsa_last_cluster_size())
 
 
 def kernel_times():

@@ -235,7 +235,23 @@ const char *qsa_status_string(qsa_status status);
  * 0: plain stream order.  The first kernel of a call always waits for all of
  * the caller's earlier work on the stream. */
 #define QSA_CFG_OVERLAP 4
+/* CTAs per row of the exact candidate selector on the filter path.  2, 4 or
+ * 8: each row goes to one thread-block cluster of that size, whose CTAs
+ * gather, count and order slices of the row and merge them through
+ * distributed shared memory; the size is capped by what the device's
+ * occupancy query (cudaOccupancyMaxPotentialClusterSize) reports it can
+ * co-schedule, and a refused launch is retried at half the size down to one
+ * CTA per row.  0 (default, automatic) and 1: one CTA per row, which measured
+ * faster on every batch tried (on the 64-row decode batch, 18.1 us against
+ * 18.6 / 24.4 / 58.6 us for clusters of 2 / 4 / 8).  ("qwen4_exp QSA
+ * cooperative_topk cannot launch on NVIDIA Thor (sm_110)": a cluster size
+ * must come from the device, not from its compute capability.) */
+#define QSA_CFG_CLUSTER 5
 qsa_status qsa_set_config(int32_t key, int64_t value);
+
+/* CTAs per row (cluster size) of the most recent launch of the candidate
+ * selector in this process; 1 when it ran one CTA per row. */
+int32_t qsa_last_cluster_size(void);
 
 /* Kernel kinds reported by qsa_kernel_times(). */
 #define QSA_KERNEL_KINDS 10

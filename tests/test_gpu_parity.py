@@ -134,6 +134,46 @@ def test_mixed_sign_weights(dist, wdist, path):
     assert not np.any(np.signbit(gv[gv == 0]))          # the zeros come back as +0
 
 
+@pytest.mark.parametrize("csize", [1, 2, 4, 8])
+@pytest.mark.parametrize("dist,k", [("int4", 512), ("tern", 300)])
+def test_cluster_selector_matches_oracle(csize, dist, k):
+    # Few rows: the candidate selector splits each row over a thread-block
+    # cluster (sizes forced here, capped by the device's own query) and merges
+    # the slices through distributed shared memory.  Integer data: bit-exact.
+    wl = W.make_workload("cl", seed=41 + k, ctx_tokens=[30000, 2000, 60000, 9000], rows_per_req=[3, 2, 1, 4],
+                         k=k, dist=dist)
+    oi, ov, _ = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                           wl.row_visible, wl.k, ld=wl.ld)
+    qsa.set_config(qsa.QSA_CFG_CLUSTER, csize)
+    try:
+        gi, gv = gpu_select(wl, path=qsa.PATH_FILTER)
+        used = qsa.last_cluster_size()
+    finally:
+        qsa.set_config(qsa.QSA_CFG_CLUSTER, 0)
+    assert 1 <= used <= csize and used & (used - 1) == 0
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov)
+
+
+@pytest.mark.parametrize("csize", [1, 4])
+def test_decode_batch_full_rows_on_cluster_and_plain_selectors(csize):
+    # the 64-row decode batch, every row, through both candidate selectors:
+    # exactly the oracle's selection on the GPU's own logits
+    wl = W.CONFIGS["decode"]()
+    d = to_device(wl)
+    gl = gpu_logits(wl, d)
+    ei, ev = oracle.select(gl, wl.row_visible, wl.k)
+    qsa.set_config(qsa.QSA_CFG_CLUSTER, csize)
+    try:
+        gi, gv = gpu_select(wl, d, path=qsa.PATH_FILTER)
+        used = qsa.last_cluster_size()
+    finally:
+        qsa.set_config(qsa.QSA_CFG_CLUSTER, 0)
+    assert used == csize or (csize > 1 and 1 < used < csize)
+    np.testing.assert_array_equal(gi, ei)
+    np.testing.assert_array_equal(gv, ev)
+
+
 def test_filter_path_falls_back_when_sampling_misleads():
     # Scores are high only in sampled key tiles (every 2nd tile for k=256), so
     # the sample threshold keeps fewer than k candidates and rows must take the
