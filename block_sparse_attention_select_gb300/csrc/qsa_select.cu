@@ -627,6 +627,76 @@ select_kernel(const SelectParams p)
         select_row(p, r, false, sh, out64, keys, inv, p.smem_cap);
 }
 
+// ------------------------------------------------------------- small k --
+//
+// Dense rows with k <= WK (the block scorer's top-16 blocks): one warp per
+// row.  Every element becomes its full key (key32 << 32 | ~index), all
+// distinct, so the order is exact.  Each lane keeps the WK largest keys it has
+// seen, sorted, in registers (most elements only compare with the smallest);
+// then min(k, V) rounds of a warp-wide maximum over the lanes' heads emit the
+// result in order, the winning lane dropping its head.
+constexpr int WK = 16;
+
+template <int K>
+__global__ void __launch_bounds__(256)
+warp_topk_kernel(const SelectParams p)
+{
+    const int lane = threadIdx.x & 31;
+    const int32_t r = static_cast<int32_t>(blockIdx.x) * 8 + static_cast<int32_t>(threadIdx.x >> 5);
+    wait_prior_grid();                      // last kernel of its call: nothing to allow
+    if (r >= p.R) return;
+    int32_t V = p.row_vis[r];
+    if (V < 0 || V > p.max_len) {
+        if (lane == 0) record_error(p.status, ST_BAD_ROW);
+        V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
+    }
+    const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
+    uint64_t x[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) x[i] = 0ull;   // below every real key (key32 > 0 for every float)
+    for (int32_t j = lane; j < V; j += 32) {
+        const uint64_t key = (static_cast<uint64_t>(score_key(__ldcg(row + j))) << 32) | ~static_cast<uint32_t>(j);
+        if (key > x[K - 1]) {
+            x[K - 1] = key;
+#pragma unroll
+            for (int i = K - 1; i > 0; --i) {
+                const uint64_t a = x[i - 1], b = x[i];
+                x[i - 1] = b > a ? b : a;
+                x[i] = b > a ? a : b;
+            }
+        }
+    }
+    int64_t ro = r;
+    if (p.out_heads > 1) {                  // virtual row r = h * n + row -> output row row * H + h
+        const int32_t n = p.R / p.out_heads;
+        ro = static_cast<int64_t>(r % n) * p.out_heads + r / n;
+    }
+    int32_t *oi = p.out_idx + ro * p.k;
+    float *ov = p.out_val ? p.out_val + ro * p.k : nullptr;
+    const int32_t kk = min(p.k, V);
+    for (int32_t o = 0; o < kk; ++o) {
+        uint64_t best = x[0];
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) {
+            const uint64_t other = __shfl_xor_sync(0xffffffffu, best, sft);
+            best = other > best ? other : best;
+        }
+        if (x[0] == best) {                 // exactly one lane: the keys are distinct
+#pragma unroll
+            for (int i = 0; i < K - 1; ++i) x[i] = x[i + 1];
+            x[K - 1] = 0ull;
+        }
+        if (lane == 0) {
+            oi[o] = static_cast<int32_t>(~static_cast<uint32_t>(best));
+            if (ov) ov[o] = key_score(static_cast<uint32_t>(best >> 32));
+        }
+    }
+    for (int32_t o = kk + lane; o < p.k; o += 32) {
+        oi[o] = -1;
+        if (ov) ov[o] = -__int_as_float(0x7f800000);
+    }
+}
+
 // ------------------------------------------------------------ candidates --
 //
 // One CTA per row.  The row's candidates (layout in qsa_internal.h) are read
@@ -1554,6 +1624,9 @@ int launch_select(const SelectParams &p, int grid, bool overlap, void *stream, i
         return launch_kernel(reinterpret_cast<const void *>(&cand_kernel), dim3(p.R), dim3(CT), smem, st, overlap,
                              args);
     }
+    if (p.k <= WK)                          // small k: one warp per row
+        return launch_kernel(reinterpret_cast<const void *>(&warp_topk_kernel<WK>), dim3((p.R + 7) / 8), dim3(256), 0,
+                             st, overlap, args);
     static size_t done[64] = {};
     const size_t smem = sizeof(SelShared) + static_cast<size_t>(out_capacity(p)) * 8 +
                         static_cast<size_t>(p.smem_cap) * 8;

@@ -233,7 +233,10 @@ def test_k_equals_one_and_max_k():
 
 @pytest.mark.parametrize("n,k,kind", [(5000, 700, "gauss"), (30000, 2048, "gauss"),
                                       (60000, 2048, "ties"), (60000, 4000, "few"),
-                                      (9000, 8192, "ties"), (100, 64, "ties")])
+                                      (9000, 8192, "ties"), (100, 64, "ties"),
+                                      # k <= 16: the warp-per-row selector
+                                      (1440, 16, "gauss"), (5000, 16, "ties"), (40000, 7, "few"),
+                                      (10, 16, "gauss"), (3000, 1, "ties")])
 def test_topk_exact_on_oracle_style_logits(n, k, kind):
     rng = np.random.default_rng(n + k)
     R = 9
