@@ -48,7 +48,7 @@ struct EpiRows {
     __align__(16) float w[64];   // weights by row pair: w[(r / 2) * 2H + 2h + r % 2], r = row - first row of the warp
     __align__(16) int32_t vis[64];   // V of each row
     __align__(16) float tau[64];     // FILTER threshold of each row
-    uint32_t masks[32];              // FILTER: mask words of the chunk being drained
+    __align__(16) uint32_t masks[32];   // FILTER: mask words of the chunk being drained
 };
 
 static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
@@ -217,24 +217,44 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, 
                     tau[i] = t4.x; tau[i + 1] = t4.y; tau[i + 2] = t4.z; tau[i + 3] = t4.w;
                 }
             }
+            if constexpr (MODE == SCORE_FILTER) {
+                // staged over the block's rows (compares, then ballots, then
+                // ranks and stores), so that the rows' short dependent chains
+                // interleave
+                bool take[B];
+                uint32_t m[B];
 #pragma unroll
-            for (int i = 0; i < B; ++i) {
-                const int32_t el = c0 + b0 + i;
-                const bool live = ALLROWS || el < nmine;      // warp-uniform
-                const bool ok = live && (FULL || j < e.vis[el]);
-                if constexpr (MODE == SCORE_FILTER) {
-                    const bool take = ok && s[i] >= tau[i];
-                    const uint32_t m = __ballot_sync(0xffffffffu, take);
-                    if (lane == 0) e.masks[b0 + i] = m;
+                for (int i = 0; i < B; ++i) {
+                    const int32_t el = c0 + b0 + i;
+                    const bool live = ALLROWS || el < nmine;  // warp-uniform
+                    take[i] = live && (FULL || j < e.vis[el]) && s[i] >= tau[i];
+                }
+#pragma unroll
+                for (int i = 0; i < B; ++i) m[i] = __ballot_sync(0xffffffffu, take[i]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < B; i += 4)
+                        *reinterpret_cast<uint4 *>(&e.masks[b0 + i]) = make_uint4(m[i], m[i + 1], m[i + 2], m[i + 3]);
+                }
+#pragma unroll
+                for (int i = 0; i < B; ++i) {
                     // a passing lane's slot row: the passing lanes below it
-                    const uint32_t rk = static_cast<uint32_t>(__popc(m & lt_mask));
-                    if (take) (slot0 + rk * 4u)[el * TILE_M] = s[i];
-                } else if constexpr (MODE == SCORE_SAMPLE) {
-                    if (ok) out0[el * p.ld] = s[i];
-                } else {
-                    float *dst = out0 + el * p.ld;
-                    if (ok) *dst = s[i];
-                    else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
+                    const uint32_t rk = static_cast<uint32_t>(__popc(m[i] & lt_mask));
+                    if (take[i]) (slot0 + rk * 4u)[(c0 + b0 + i) * TILE_M] = s[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < B; ++i) {
+                    const int32_t el = c0 + b0 + i;
+                    const bool live = ALLROWS || el < nmine;  // warp-uniform
+                    const bool ok = live && (FULL || j < e.vis[el]);
+                    if constexpr (MODE == SCORE_SAMPLE) {
+                        if (ok) out0[el * p.ld] = s[i];
+                    } else {
+                        float *dst = out0 + el * p.ld;
+                        if (ok) *dst = s[i];
+                        else if (live && p.pad_inf && j < p.ld) *dst = -__int_as_float(0x7f800000);
+                    }
                 }
             }
         }
