@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -20,7 +21,8 @@ using namespace qsa;
 __device__ uint32_t g_device_status;   // one per device: error bits recorded by the kernels
 
 constexpr int MAX_DEVICES = 64;
-constexpr float OVERSAMPLE = 1.5f;     // expected candidates per row / k on the filter path
+constexpr double OVERSAMPLE = 1.5;     // least expected candidates per row / k on the filter path
+constexpr double SAMPLE_MARGIN = 4.5;  // standard deviations between the expected candidate count and k
 
 struct DeviceInfo {
     bool probed = false;
@@ -138,20 +140,38 @@ int32_t pow2_floor(double x)
 }
 
 // Sampled-threshold filter parameters for a top-k of k over rows of up to max_len.
+//
+// The threshold is the m-th largest of the scores in every stride-th key tile,
+// so the number of a row's positions at or above it is about m * stride, with a
+// spread of about stride * sqrt(m) (m gaps between consecutive sampled order
+// statistics, each about stride positions wide).  The stride is kept at 16
+// tiles or more (the sampling pass and the threshold then stay a small share
+// of the step) and m is chosen so that the expected count lies SAMPLE_MARGIN
+// spreads above k; the cap holds the count up to five spreads above its mean.
 struct FilterShape {
     int32_t stride;     // sample every stride-th key tile
     int32_t cap;        // candidate slots per row
     int64_t sample_ld;  // columns of the sample matrix
+    float oversample;   // expected candidates / k
 };
 
 FilterShape filter_shape(int64_t max_len, int32_t k)
 {
     FilterShape f;
-    f.stride = std::max(1, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
-    // candidates the selector holds (~1.5 k expected); a multiple of 4 so that
-    // the selector's arrays after the cap-sized one stay 16-byte aligned
+    f.stride = std::max(16, std::min(32, pow2_floor(OVERSAMPLE * k / 128.0)));
+    // sampled scores at or above the threshold: the root of
+    // m - k / stride = SAMPLE_MARGIN * sqrt(m)
+    const double kt = static_cast<double>(k) / f.stride;
+    const double x = 0.5 * (SAMPLE_MARGIN + std::sqrt(SAMPLE_MARGIN * SAMPLE_MARGIN + 4.0 * kt));
+    const double m = std::max(OVERSAMPLE * kt, x * x);
+    f.oversample = static_cast<float>(m / kt);
+    // candidates the selector holds; a multiple of 4 so that the selector's
+    // arrays after the cap-sized one stay 16-byte aligned (the selector adds 8
+    // sampled scores to m)
     const int64_t k64 = k;
-    f.cap = static_cast<int32_t>((std::max<int64_t>(2 * k64 + 256, k64 + 512) + 3) / 4 * 4);
+    const double spread = 5.0 * f.stride * std::sqrt(m + 8.0);
+    const int64_t need = static_cast<int64_t>(std::ceil((m + 8.0) * f.stride + spread));
+    f.cap = static_cast<int32_t>((std::max({2 * k64 + 256, k64 + 512, need}) + 3) / 4 * 4);
     const int64_t tiles = (max_len + TILE_M - 1) / TILE_M;
     f.sample_ld = std::max<int64_t>(TILE_M, (tiles + f.stride - 1) / f.stride * TILE_M);
     return f;
@@ -166,8 +186,8 @@ bool use_filter(int32_t rows, int64_t max_len, int32_t k)
     (void)rows;
     if (g_cfg_path == 1) return false;
     if (g_cfg_path == 2) return true;
-    const FilterShape f = filter_shape(max_len, k);
-    return f.stride >= 4 && max_len >= 3LL * k;
+    // below k ~ 340 the dense selector is the faster one (measured)
+    return OVERSAMPLE * k / 128.0 >= 4.0 && max_len >= 3LL * k;
 }
 
 struct Layout {
@@ -695,7 +715,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     s.sp.out = sample;
     s.sp.ld = f.sample_ld;
     if ((st = launch_rc(timed(K_SCORE_SAMPLE, stream, [&] { return launch_scorer(s, d->sms, stream); }))) != QSA_OK) return st;
-    // 2. per-row threshold tau_r: a sample quantile that keeps ~OVERSAMPLE * k positions
+    // 2. per-row threshold tau_r: a sample quantile that keeps ~oversample * k positions
     SelectParams th = sel;
     th.mode = SEL_THRESH;
     th.logits = sample;
@@ -703,7 +723,7 @@ qsa_status qsa_select_paged_tokens(const void *q, const float *w, int32_t rows, 
     th.cap = f.cap;
     th.sample_stride = f.stride;
     th.tau = tau;
-    th.oversample = OVERSAMPLE;
+    th.oversample = f.oversample;
     th.smem_cap = static_cast<int32_t>(std::min<int64_t>(f.sample_ld, TH_STAGE));   // staged scores per row
     if ((st = launch_rc(timed(K_SEL_THRESH, stream, [&] { return launch_select(th, rows, g_overlap, stream); }))) != QSA_OK) return st;
     // 3. full scoring pass keeping only scores >= tau_r
