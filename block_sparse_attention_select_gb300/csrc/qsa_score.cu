@@ -269,6 +269,128 @@ __device__ __forceinline__ void epilogue_rows(const ScoreParams &p, EpiRows &e, 
     }
 }
 
+// Key-tile producer, warp 0 of both scorers.  The whole warp walks the CTA's
+// items; lane i owns key box i of a tile.  On a group change lane 0 waits
+// until the previous group's MMAs have released the query buffer and calls
+// load_q (which arms q_full).  Block-table entries are loaded PREFETCH items
+// ahead so that the page-id round trip never sits in front of a TMA issue.
+// Before returning (also after an abort) the warp waits, bounded, for every
+// copy it issued, so that none lands in shared memory after the CTA ends.
+template <int KST, typename LoadQ>
+__device__ __forceinline__ void produce_tiles(const ScoreParams &p, const CUtensorMap *tmap_k,
+                                              const CUtensorMap *tmap_k128, uint8_t *k_s, uint64_t *full,
+                                              uint64_t *empty, uint64_t *q_full, uint64_t *q_empty,
+                                              const int32_t *prefix, int32_t n_groups, int32_t it0, int32_t it1,
+                                              int32_t stride, int lane, bool blk, volatile int *abort, uint64_t lim,
+                                              LoadQ load_q)
+{
+    constexpr int PREFETCH = 8;
+    ItemCursor cur, ahead;
+    cur.init_warp(prefix, n_groups, it0, it1, stride, lane);
+    // the first group's queries are requested before the page ids: their
+    // load does not wait for the block-table round trip
+    cur.settle();
+    int32_t cur_g = cur.g, q_loads = 1, stage = 0;
+    Group gr = p.groups[cur_g];
+    if (lane == 0) load_q(gr);
+    ahead = cur;
+    Group ga = gr;
+    int32_t ga_g = cur_g;                   // group held in ga (reloaded on a change only)
+    auto page_id = [&](ItemCursor &a) -> int32_t {
+        if (!a.valid()) return -1;
+        a.settle();
+        if (a.g != ga_g) {
+            ga_g = a.g;
+            ga = p.groups[a.g];
+        }
+        const int32_t pos0 = a.tile() * TILE_M;
+        const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
+        if (lane >= nbox || ga.req < 0) return -1;
+        const int32_t pos = pos0 + lane * p.page_box;
+        const int32_t req = blk ? ga.req % p.blk_reqs : ga.req;   // virtual request -> block-table row
+        return __ldg(p.block_table + static_cast<int64_t>(req) * p.max_pages + (pos >> p.page_pos_shift));
+    };
+    int32_t ring[PREFETCH];
+#pragma unroll
+    for (int d = 0; d < PREFETCH; ++d) {
+        ring[d] = page_id(ahead);
+        ahead.next();
+    }
+    uint32_t phase = 0;
+    uint32_t loaded = 0;                    // bit s: stage s holds an issued copy (of parity bit KST + s)
+    bool stop = false;
+    // the ring slot read in an iteration is refilled in the same iteration
+    // and read again PREFETCH iterations later (no move of a pending load)
+    while (cur.valid() && !stop) {
+#pragma unroll
+        for (int u = 0; u < PREFETCH; ++u) {
+            if (!cur.valid()) break;
+            cur.settle();
+            const int32_t pid = ring[u];
+            ring[u] = page_id(ahead);
+            ahead.next();
+            if (cur.g != cur_g) {
+                cur_g = cur.g;
+                gr = p.groups[cur_g];
+                bool ok = true;
+                if (lane == 0) {
+                    ok = mbar_wait(q_empty, (q_loads - 1) & 1, abort, lim);
+                    if (ok) load_q(gr);
+                }
+                if (__any_sync(0xffffffffu, !ok)) { stop = true; break; }
+                ++q_loads;
+            }
+            if (__any_sync(0xffffffffu, !mbar_wait(&empty[stage], phase ^ 1u, abort, lim))) {
+                stop = true;
+                break;
+            }
+            const int32_t pos0 = cur.tile() * TILE_M;
+            const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
+            __syncwarp();
+            loaded = (loaded & ~(1u << (KST + stage))) | (1u << stage) | (phase << (KST + stage));
+            const int32_t pos = pos0 + lane * p.page_box;
+            const bool good = pid >= 0 && pid < p.num_pages;
+            int32_t y = good ? pid * p.page_pos + (pos & (p.page_pos - 1))
+                             : p.num_pages * p.page_pos;   // past the end: TMA fills zeros
+            if (lane < nbox && !good) record_error(p.status, ST_BAD_PAGE);
+            // a full tile whose pages are physically consecutive is one box per K half
+            const int32_t y0 = __shfl_sync(0xffffffffu, y, 0);
+            const bool run = nbox * p.page_box == TILE_M &&
+                             __all_sync(0xffffffffu, lane >= nbox || (good && y == y0 + lane * p.page_box));
+            uint8_t *dst = k_s + stage * K_STAGE_BYTES;
+            if (blk) {
+                // one 128-token page of head h: two boxes of [128 tokens][64 dims]
+                if (lane == 0) {
+                    const int32_t h = gr.row0 / p.blk_rows;
+                    tma_load_3d(dst, tmap_k, &full[stage], 0, h, y);
+                    tma_load_3d(dst + K_HALF_BYTES, tmap_k, &full[stage], 64, h, y);
+                }
+            } else if (run) {
+                if (lane == 0) {
+                    tma_load_2d(dst, tmap_k128, &full[stage], 0, y0);
+                    tma_load_2d(dst + K_HALF_BYTES, tmap_k128, &full[stage], 64, y0);
+                }
+            } else if (lane < nbox) {
+                dst += lane * p.page_box * 128;
+                tma_load_2d(dst, tmap_k, &full[stage], 0, y);
+                tma_load_2d(dst + K_HALF_BYTES, tmap_k, &full[stage], 64, y);
+            }
+            if (++stage == KST) { stage = 0; phase ^= 1u; }
+            cur.next();
+        }
+    }
+    // copies still in flight (only after an abort: otherwise the MMA thread
+    // has waited for all of them)
+    if (lane == 0) {
+        mbar_wait_bounded(q_full, (q_loads - 1) & 1, lim);
+        for (int s = 0; s < KST; ++s)
+            if (loaded & (1u << s)) mbar_wait_bounded(&full[s], (loaded >> (KST + s)) & 1u, lim);
+    }
+    __syncwarp();
+}
+
 // The four quarter warps of a column block meet: lane 0 arrives, the warp
 // waits (bounded; false when the CTA aborted, and the caller then stops).
 __device__ __forceinline__ bool quarter_sync(uint64_t *bar, uint32_t &phase, volatile int *abort, uint64_t lim)
@@ -436,17 +558,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         // no item for this CTA: straight to the teardown
     } else if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        // The whole warp walks the items; lane i owns key box i of a tile.
-        // Block-table entries are loaded PREFETCH items ahead so that the
-        // page-id round trip never sits in front of a TMA issue.
-        constexpr int PREFETCH = 8;
-        ItemCursor cur, ahead;
-        cur.init_warp(prefix, n_groups, it0, it1, stride, lane);
-        // the first group's queries are requested before the page ids: their
-        // load does not wait for the block-table round trip
-        cur.settle();
-        int32_t cur_g = cur.g, q_loads = 1, stage = 0;
-        Group gr = p.groups[cur_g];
         // the group's queries: rows row0 .. of [rows * H, 128], or for the
         // block scorer rows r0 .. of head h through the 3-D map
         auto load_q = [&](const Group &g) {
@@ -460,94 +571,8 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, g.row0 * H);
             }
         };
-        if (lane == 0) load_q(gr);
-        ahead = cur;
-        Group ga = gr;
-        int32_t ga_g = cur_g;                   // group held in ga (reloaded on a change only)
-        auto page_id = [&](ItemCursor &a) -> int32_t {
-            if (!a.valid()) return -1;
-            a.settle();
-            if (a.g != ga_g) {
-                ga_g = a.g;
-                ga = p.groups[a.g];
-            }
-            const int32_t pos0 = a.tile() * TILE_M;
-            const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
-            if (lane >= nbox || ga.req < 0) return -1;
-            const int32_t pos = pos0 + lane * p.page_box;
-            const int32_t req = blk ? ga.req % p.blk_reqs : ga.req;   // virtual request -> block-table row
-            return __ldg(p.block_table + static_cast<int64_t>(req) * p.max_pages + (pos >> p.page_pos_shift));
-        };
-        int32_t ring[PREFETCH];
-#pragma unroll
-        for (int d = 0; d < PREFETCH; ++d) {
-            ring[d] = page_id(ahead);
-            ahead.next();
-        }
-        uint32_t phase = 0;
-        bool stop = false;
-        // the ring slot read in an iteration is refilled in the same iteration
-        // and read again PREFETCH iterations later (no move of a pending load)
-        while (cur.valid() && !stop) {
-#pragma unroll
-            for (int u = 0; u < PREFETCH; ++u) {
-                if (!cur.valid()) break;
-                cur.settle();
-                const int32_t pid = ring[u];
-                ring[u] = page_id(ahead);
-                ahead.next();
-                if (cur.g != cur_g) {
-                    cur_g = cur.g;
-                    gr = p.groups[cur_g];
-                    bool ok = true;
-                    if (lane == 0) {
-                        ok = q_loads == 0 || mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim);
-                        if (ok) load_q(gr);
-                    }
-                    if (__any_sync(0xffffffffu, !ok)) { stop = true; break; }
-                    ++q_loads;
-                }
-                if (__any_sync(0xffffffffu, !mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim))) {
-                    stop = true;
-                    break;
-                }
-                const int32_t pos0 = cur.tile() * TILE_M;
-                const int32_t nbox = (min(TILE_M, gr.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nbox * p.page_box * 256));
-                __syncwarp();
-                const int32_t pos = pos0 + lane * p.page_box;
-                const bool good = pid >= 0 && pid < p.num_pages;
-                int32_t y = good ? pid * p.page_pos + (pos & (p.page_pos - 1))
-                                 : p.num_pages * p.page_pos;   // past the end: TMA fills zeros
-                if (lane < nbox && !good) record_error(p.status, ST_BAD_PAGE);
-                // a full tile whose pages are physically consecutive is one box per K half
-                const int32_t y0 = __shfl_sync(0xffffffffu, y, 0);
-                const bool run = nbox * p.page_box == TILE_M &&
-                                 __all_sync(0xffffffffu, lane >= nbox || (good && y == y0 + lane * p.page_box));
-                if (blk) {
-                    // one 128-token page of head h: two boxes of [128 tokens][64 dims]
-                    if (lane == 0) {
-                        const int32_t h = gr.row0 / p.blk_rows;
-                        uint8_t *dst = k_s + stage * K_STAGE_BYTES;
-                        tma_load_3d(dst, &tmap_k, &c.full[stage], 0, h, y);
-                        tma_load_3d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, h, y);
-                    }
-                } else if (run) {
-                    if (lane == 0) {
-                        uint8_t *dst = k_s + stage * K_STAGE_BYTES;
-                        tma_load_2d(dst, &tmap_k128, &c.full[stage], 0, y0);
-                        tma_load_2d(dst + K_HALF_BYTES, &tmap_k128, &c.full[stage], 64, y0);
-                    }
-                } else if (lane < nbox) {
-                    uint8_t *dst = k_s + stage * K_STAGE_BYTES + lane * p.page_box * 128;
-                    tma_load_2d(dst, &tmap_k, &c.full[stage], 0, y);
-                    tma_load_2d(dst + K_HALF_BYTES, &tmap_k, &c.full[stage], 64, y);
-                }
-                if (++stage == KSTAGES) { stage = 0; phase ^= 1u; }
-                cur.next();
-            }
-        }
+        produce_tiles<KSTAGES>(p, &tmap_k, &tmap_k128, k_s, c.full, c.empty, &c.q_full, &c.q_empty, prefix,
+                               n_groups, it0, it1, stride, lane, blk, abort, lim, load_q);
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
