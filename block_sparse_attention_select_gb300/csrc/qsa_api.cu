@@ -490,6 +490,7 @@ qsa_status qsa_sparse_attention(const void *q, int32_t rows, int32_t hq, const v
     p.max_pages = max_pages;
     p.scale = scale;
     p.status = d->status;
+    p.wait_limit_ns = g_wait_ns;
     return launch_rc(launch_attend(p, stream));
 }
 

@@ -5,15 +5,32 @@
 //
 // Row r (a query at token t of request b) attends the tokens 4j .. 4j + 3 of
 // every selected index position j and the tokens 4V .. t of its unfinished
-// block (V = (t + 1) / 4).  One CTA per (row, KV head): the GROUP query heads
-// of that KV head share every gathered K / V line.  Tokens go in chunks of 32:
-// the chunk's K and V rows are gathered through the block table into shared
-// memory (K rows padded by one word so that lane-per-token reads hit distinct
-// banks), lane c scores token c for the warp's heads, each head keeps an
-// online softmax (running max and sum), and every thread accumulates two of
-// the 256 output dimensions for all GROUP heads.  FP32 throughout, output FP32.
+// block (V = (t + 1) / 4).  One CTA of 256 threads per (row, KV head): the G
+// query heads of that KV head (G <= 16) share every gathered K / V row.
+// Tokens go in chunks of 128, both contractions on the 5th-generation tensor
+// cores (kind::f16, FP16 operands, FP32 accumulators in TMEM):
+//   S^T[token, head] = K_chunk . Q^T   M = 128 tokens, N = 16 heads, K = 256
+//   O^T[dim, head]  += V^T . P^T       M = 2 x 128 dims, N = 32, K = 128 tokens
+// Every operand is K-major in the 128-byte swizzle layout: K rows are gathered
+// straight into that layout; V rows are gathered into a staging tile and
+// transposed in shared memory (8 x 8 blocks: ldmatrix.trans then stmatrix).
+// Warp w reads TMEM lane quarter w % 4 and takes half w / 4 of the work: in
+// the softmax, tokens 32 (w % 4) .. + 31 of the chunk for heads 8 (w / 4) ..
+// + 7 (scores scaled in FP32; each head's running maximum comes from warp
+// max-reductions combined through shared memory; the numerators p go to the
+// PV product as an FP16 pair, p_hi = fp16(p) and p_lo = fp16(p - p_hi) in
+// columns 0..15 and 16..31 of N, so their rounding stays near FP32); in the
+// output, dimensions 32 (w % 4) + lane + 128 (w / 4) of every head, kept in
+// registers and rescaled by exp(m_old - m_new) per chunk.  Each thread also
+// keeps its share of its heads' softmax denominators, summed over the CTA at
+// the end.
+// The gather of chunk c + 1 (cp.async) is issued as soon as chunk c's score
+// product is done and runs under chunk c's softmax, PV product and output
+// update.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "qsa_device.cuh"
 #include "qsa_internal.h"
@@ -21,70 +38,140 @@
 namespace qsa {
 namespace {
 
-constexpr int AT_D = 256;               // head dimension
-constexpr int AT_THREADS = 128;
-constexpr int AT_WARPS = AT_THREADS / 32;
-constexpr int AT_CHUNK = 32;            // tokens per chunk (one per lane)
-constexpr int AT_MAXG = 16;             // query heads per KV head
-constexpr int K_LD = AT_D + 2;          // halves per padded K row (129 words)
+constexpr int AT_D = 256;                   // head dimension
+constexpr int AT_THREADS = 256;             // two warps per TMEM lane quarter
+constexpr int AT_CHUNK = 128;               // tokens per chunk (MMA M of the score product)
+constexpr int AT_MAXG = 16;                 // query heads per KV head (MMA N of the score product)
+constexpr uint32_t AT_TMEM_COLS = 128;      // S: columns 0..15; O: 32..63 (dims 0..127), 64..95 (128..255)
 
-struct AttendShared {
-    float q[AT_MAXG][AT_D];                 // pre-scaled queries
-    __half k[AT_CHUNK][K_LD];
-    __half v[AT_CHUNK][AT_D];
-    float pw[AT_MAXG][AT_CHUNK];            // this chunk's softmax numerators
-    float alpha[AT_MAXG];                   // rescale of the running output
-    float m[AT_MAXG], l[AT_MAXG];           // running max and sum per head
-    int32_t tok[AT_CHUNK];                  // token positions of the chunk (-1 = none)
+// shared memory, offsets from a 1024-byte aligned base
+constexpr uint32_t SM_K = 0;                         // A of S: [4 K blocks][128 tokens][128 B]
+constexpr uint32_t SM_VS = SM_K + 4 * 16384;          // V staging: [128 tokens][512 B], 16-B chunks swizzled
+constexpr uint32_t SM_VT = SM_VS + 128 * 512;         // A of O: [2 dim halves][2 K blocks][128 dims][128 B]
+constexpr uint32_t SM_Q = SM_VT + 4 * 16384;          // B of S: [4 K blocks][16 heads][128 B]
+constexpr uint32_t SM_P = SM_Q + 4 * 2048;            // B of O: [2 K blocks][32 rows][128 B]
+constexpr uint32_t SM_CTRL = SM_P + 2 * 4096;
+struct AtCtrl {
+    uint64_t bar_s;                         // score product done
+    uint64_t bar_o;                         // PV product done
+    uint32_t tmem_base;
+    int32_t abort;
+    uint32_t wmax[2][4][8];                 // [head set][lane quarter][head]: maxima of the chunk (score keys)
+    float lsum[2][4][8];                    // the same for the denominators (end of the row)
 };
+constexpr uint32_t AT_SMEM = SM_CTRL + sizeof(AtCtrl) + 1024;
+static_assert(AT_SMEM <= 232448, "shared memory budget");
 
-__global__ void __launch_bounds__(AT_THREADS)
+// Byte offset of 16-byte chunk c (0..7) of row `row` in a K-major tile with
+// the 128-byte swizzle (rows of 128 B, 8-row atoms of 1024 B).
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t c)
+{
+    return (row >> 3) * 1024u + (row & 7u) * 128u + ((c ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool fill)
+{
+    // a 16-byte copy, or 16 zero bytes (source size 0: nothing is read)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(fill ? 16 : 0)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t u[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr)
+                 : "memory");
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t u[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(u[i]);
+}
+
+// Every thread waits for the phase; false on every thread when any gave up.
+__device__ __forceinline__ bool wait_all_threads(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t lim)
+{
+    const bool ok = mbar_wait(bar, parity, abort, lim);
+    return __syncthreads_and(ok) != 0;
+}
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
 attend_kernel(const AttendParams p)
 {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    AttendShared &sh = *reinterpret_cast<AttendShared *>(smem_raw);
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sb = smem_u32(smem);
+    AtCtrl &c = *reinterpret_cast<AtCtrl *>(smem + SM_CTRL);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int lq = warp & 3, hs = warp >> 2;      // TMEM lane quarter, half of the work
     const int32_t r = blockIdx.x, g = blockIdx.y;
-    wait_prior_grid();
-    if (r >= p.rows || g >= p.hkv) return;
-    const int group = p.hq / p.hkv;
-    const int32_t b = p.row_req[r];
-    const int32_t tok_r = p.row_token[r];
-    if (b < 0 || b >= p.num_reqs || tok_r < 0 ||
-        static_cast<int64_t>(tok_r) >= static_cast<int64_t>(p.max_pages) * p.page_tokens) {
-        if (t == 0 && g == 0) record_error(p.status, ST_BAD_ROW);
-        return;                                          // uniform: the row's output is left as it was
-    }
-    const int32_t vis = (tok_r + 1) >> 2;               // complete index positions
-    const int32_t tail0 = 4 * vis;                       // first token of the unfinished block
 
-    // queries of this KV head's group, scaled
-    for (int i = t; i < group * AT_D; i += AT_THREADS) {
-        const int h = i / AT_D, d = i % AT_D;
-        sh.q[h][d] = __half2float(static_cast<const __half *>(p.q)[(static_cast<int64_t>(r) * p.hq + g * group + h) *
-                                                                    AT_D + d]) * p.scale;
+    if (t == 0) {
+        mbar_init(&c.bar_s, 1);
+        mbar_init(&c.bar_o, 1);
+        c.abort = 0;
+        fence_barrier_init();
     }
-    if (t < AT_MAXG) {
-        sh.m[t] = -INFINITY;
-        sh.l[t] = 0.0f;
+    if (warp == 0) {
+        tmem_alloc(&c.tmem_base, AT_TMEM_COLS);
+        tmem_relinquish();
     }
-    float acc[AT_MAXG][2];
-#pragma unroll
-    for (int h = 0; h < AT_MAXG; ++h) acc[h][0] = acc[h][1] = 0.0f;
-
-    const int32_t *selr = p.sel + static_cast<int64_t>(r) * p.k;
-    // token stream: 4 tokens per selection slot (slots holding -1 or a bad
-    // position contribute none), then the tail tokens tail0 .. tok_r
-    const int32_t n_stream = 4 * p.k + (tok_r - tail0 + 1);
-    const __half *kc = static_cast<const __half *>(p.k_cache);
-    const __half *vc = static_cast<const __half *>(p.v_cache);
-    const int32_t *bt = p.block_table + static_cast<int64_t>(b) * p.max_pages;
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    volatile int *abort = &c.abort;
+    const uint64_t lim = p.wait_limit_ns;
 
-    for (int32_t c0 = 0; c0 < n_stream; c0 += AT_CHUNK) {
-        // ---- token positions of the chunk
-        if (t < AT_CHUNK) {
-            const int32_t s = c0 + t;
+    const int group = p.hq / p.hkv;
+    const int32_t b = r < p.rows ? p.row_req[r] : -1;
+    const int32_t tok_r = r < p.rows ? p.row_token[r] : -1;
+    const bool row_ok = r < p.rows && g < p.hkv && b >= 0 && b < p.num_reqs && tok_r >= 0 &&
+                        static_cast<int64_t>(tok_r) < static_cast<int64_t>(p.max_pages) * p.page_tokens;
+    if (!row_ok) {
+        if (t == 0 && g == 0 && r < p.rows) record_error(p.status, ST_BAD_ROW);
+    } else {
+        const int32_t vis = (tok_r + 1) >> 2;           // complete index positions
+        const int32_t tail0 = 4 * vis;                   // first token of the unfinished block
+        // token stream: 4 tokens per selection slot (slots holding -1 or a bad
+        // position contribute none), then the tail tokens tail0 .. tok_r
+        const int32_t n_stream = 4 * p.k + (tok_r - tail0 + 1);
+        const int32_t n_chunks = (n_stream + AT_CHUNK - 1) / AT_CHUNK;
+        const int32_t *selr = p.sel + static_cast<int64_t>(r) * p.k;
+        const __half *kc = static_cast<const __half *>(p.k_cache);
+        const __half *vc = static_cast<const __half *>(p.v_cache);
+        const int32_t *bt = p.block_table + static_cast<int64_t>(b) * p.max_pages;
+
+        // queries of this KV head's group as the B operand (heads past the
+        // group are zero rows)
+        const __half *qr = static_cast<const __half *>(p.q) + (static_cast<int64_t>(r) * p.hq + g * group) * AT_D;
+        for (int i = t; i < AT_MAXG * 32; i += AT_THREADS) {
+            const int h = i >> 5, l = i & 31;                // head, 16-byte chunk of its 512-byte row
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (h < group) v = __ldg(reinterpret_cast<const uint4 *>(qr + h * AT_D) + l);
+            *reinterpret_cast<uint4 *>(smem + SM_Q + (l >> 3) * 2048 + sw128(h, l & 7)) = v;
+        }
+
+        // token of stream index s (or -1), with the device-side checks
+        auto token_at = [&](int32_t s) -> int32_t {
             int32_t pos = -1;
             if (s < 4 * p.k) {
                 const int32_t j = selr[s >> 2];
@@ -93,121 +180,223 @@ attend_kernel(const AttendParams p)
             } else if (s < n_stream) {
                 pos = tail0 + (s - 4 * p.k);
             }
-            sh.tok[t] = pos;
-        }
-        __syncthreads();
-        // ---- gather K and V rows: warp w takes tokens w, w + 4, ...; lane l
-        //      copies halves [8l, 8l + 8) of a row (16 bytes)
-        for (int c = warp; c < AT_CHUNK; c += AT_WARPS) {
-            const int32_t pos = sh.tok[c];
-            uint4 kv4 = make_uint4(0u, 0u, 0u, 0u), vv4 = make_uint4(0u, 0u, 0u, 0u);
-            if (pos >= 0) {
-                const int32_t page = bt[pos >> p.page_shift];
-                if (page >= 0 && page < p.num_pages) {
-                    const int64_t line = ((static_cast<int64_t>(page) * p.page_tokens + (pos & (p.page_tokens - 1))) *
-                                          p.hkv + g) * AT_D;
-                    kv4 = __ldg(reinterpret_cast<const uint4 *>(kc + line) + lane);
-                    vv4 = __ldg(reinterpret_cast<const uint4 *>(vc + line) + lane);
-                } else if (lane == 0) {
-                    record_error(p.status, ST_BAD_PAGE);
-                }
+            return pos;
+        };
+        // gather of chunk ch: every thread looks up its softmax token
+        // 32 lq + lane; warp w copies tokens 32 lq + 16 hs + j, j < 16 (one
+        // 512-byte K row and V row each, lane l taking 16-byte chunk l);
+        // returns whether the thread's softmax token is live
+        const int32_t t_soft = lq * 32 + lane;
+        auto gather = [&](int32_t ch) -> bool {
+            const int32_t pos_mine = token_at(ch * AT_CHUNK + t_soft);
+            int32_t line_mine = -1;                        // page-token row of the cache, -1 = none
+            if (pos_mine >= 0) {
+                const int32_t page = bt[pos_mine >> p.page_shift];
+                if (page >= 0 && page < p.num_pages) line_mine = page * p.page_tokens + (pos_mine & (p.page_tokens - 1));
+                else record_error(p.status, ST_BAD_PAGE);
             }
-            // K rows are 129 words apart: store word by word
-            const uint32_t kw[4] = {kv4.x, kv4.y, kv4.z, kv4.w};
-            uint32_t *krow = reinterpret_cast<uint32_t *>(&sh.k[c][0]);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) krow[4 * lane + i] = kw[i];
-            reinterpret_cast<uint4 *>(&sh.v[c][0])[lane] = vv4;
-        }
-        __syncthreads();
-        // ---- scores: warp w handles heads w, w + 4, ...; lane c token c
-        const bool live = sh.tok[lane] >= 0;
-        for (int h = warp; h < group; h += AT_WARPS) {
-            float s = 0.0f;
-            const __half2 *krow = reinterpret_cast<const __half2 *>(&sh.k[lane][0]);
-            const float2 *qh = reinterpret_cast<const float2 *>(&sh.q[h][0]);
-#pragma unroll 8
-            for (int d2 = 0; d2 < AT_D / 2; ++d2) {
-                const float2 kf = __half22float2(krow[d2]);
-                const float2 qf = qh[d2];
-                s = fmaf(qf.x, kf.x, s);
-                s = fmaf(qf.y, kf.y, s);
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                const int32_t line = __shfl_sync(0xffffffffu, line_mine, hs * 16 + j);
+                const uint32_t T = static_cast<uint32_t>(lq * 32 + hs * 16 + j);
+                const int64_t off = (static_cast<int64_t>(line < 0 ? 0 : line) * p.hkv + g) * AT_D + lane * 8;
+                cp_async16(sb + SM_K + (lane >> 3) * 16384 + sw128(T, lane & 7), kc + off, line >= 0);
+                cp_async16(sb + SM_VS + T * 512 + ((lane ^ (T & 7)) << 4), vc + off, line >= 0);
             }
-            s = live ? s : -INFINITY;
-            float mx = s;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float m_old = sh.m[h];
-            const float m_new = fmaxf(m_old, mx);
-            // no live token yet: nothing to weigh (m stays -inf)
-            const float e = (live && m_new > -INFINITY) ? __expf(s - m_new) : 0.0f;
-            float se = e;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
-            sh.pw[h][lane] = e;
-            if (lane == 0) {
-                const float a = m_old > -INFINITY ? __expf(m_old - m_new) : 0.0f;
-                sh.alpha[h] = a;
-                sh.l[h] = sh.l[h] * a + se;
-                sh.m[h] = m_new;
-            }
-        }
-        __syncthreads();
-        // ---- PV: thread t owns dimensions 2t, 2t + 1 of every head
+            return line_mine >= 0;
+        };
+
+        float o[AT_MAXG];                                 // dimension 32 lq + lane + 128 hs of every head
+        float m_run[AT_MAXG], alpha[AT_MAXG];             // every head (the same in all threads)
+        float l_part[8];                                  // heads 8 hs .. 8 hs + 7
 #pragma unroll
         for (int h = 0; h < AT_MAXG; ++h) {
-            if (h < group) {                              // acc stays in registers: constant indices only
-                const float a = sh.alpha[h];
-                acc[h][0] *= a;
-                acc[h][1] *= a;
+            o[h] = 0.0f;
+            m_run[h] = -INFINITY;
+            alpha[h] = 0.0f;
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) l_part[h] = 0.0f;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+        constexpr uint32_t idesc_s = umma_idesc_f16_f32(AT_CHUNK, AT_MAXG);
+        constexpr uint32_t idesc_o = umma_idesc_f16_f32(128, 2 * AT_MAXG);
+        // output update with chunk c's PV product (alpha: that chunk's rescale)
+        auto take_o = [&]() {
+            float a[16], bq[16];
+            tmem_ld_x16(taddr + 32u + 32u * hs, a);
+            tmem_ld_x16(taddr + 48u + 32u * hs, bq);
+#pragma unroll
+            for (int h = 0; h < AT_MAXG; ++h) o[h] = fmaf(o[h], alpha[h], a[h] + bq[h]);
+        };
+
+        bool live = n_chunks > 0 ? gather(0) : false;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int32_t ch = 0; ch < n_chunks; ++ch) {
+            // 1. the chunk's K and V rows (and, first time, Q) are in shared memory
+            cp_async_wait_all();
+            fence_proxy_async_smem();
+            __syncthreads();
+            // 2. S^T = K . Q^T
+            if (t == 0) {
+                tc_fence_after();
+                const uint64_t a0 = sw128_kmajor_desc(sb + SM_K), b0 = sw128_kmajor_desc(sb + SM_Q);
+#pragma unroll
+                for (int kk = 0; kk < AT_D / 16; ++kk) {
+                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
+                    umma_f16(tmem, a0 + (((kk >> 2) * 16384u + off) >> 4), b0 + (((kk >> 2) * 2048u + off) >> 4),
+                             idesc_s, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&c.bar_s);
+            }
+            // 3. the previous chunk's PV product into the output (V^T and P are free after it)
+            if (ch > 0) {
+                if (!wait_all_threads(&c.bar_o, (ph - 1) & 1u, abort, lim)) { ok = false; break; }
+                tc_fence_after();
+                take_o();
+            }
+            // 4. V^T: 8 x 8 blocks (8 tokens x 8 dims), four per instruction
+            for (int it = warp; it < 128; it += AT_THREADS / 32) {
+                const uint32_t tb = static_cast<uint32_t>(it >> 3), dq = static_cast<uint32_t>(it & 7);
+                const uint32_t i = static_cast<uint32_t>(lane >> 3), j = static_cast<uint32_t>(lane & 7);
+                const uint32_t T = tb * 8 + j, db = dq * 4 + i;    // source row (token) and 16-B chunk (dims)
+                uint32_t x0, x1, x2, x3;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                             : "r"(sb + SM_VS + T * 512 + ((db ^ (T & 7)) << 4)));
+                const uint32_t D = db * 8 + j;                     // destination row (dim)
+                const uint32_t dst = sb + SM_VT + (D >> 7) * 32768u + (tb >> 3) * 16384u + sw128(D & 127u, tb & 7);
+                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(x0),
+                             "r"(x1), "r"(x2), "r"(x3)
+                             : "memory");
+            }
+            // 5. softmax of the chunk (token t_soft, heads 8 hs .. 8 hs + 7)
+            if (!wait_all_threads(&c.bar_s, ph & 1u, abort, lim)) { ok = false; break; }
+            tc_fence_after();
+            float s[8];
+            tmem_ld_x8(taddr + 8u * hs, s);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                s[h] = live ? s[h] * p.scale : -INFINITY;
+                const uint32_t kmax = __reduce_max_sync(0xffffffffu, score_key(s[h]));
+                if (lane == 0) c.wmax[hs][lq][h] = kmax;
+            }
+            __syncthreads();
+            // the next chunk's rows: K and the V staging are free (S is done,
+            // every warp has finished its part of V^T), so the copies run
+            // under this chunk's softmax, PV product and output update
+            const bool live_next = ch + 1 < n_chunks ? gather(ch + 1) : false;
+            float my_m[8], my_alpha[8];                   // this thread's heads (constant indices only)
+#pragma unroll
+            for (int h = 0; h < AT_MAXG; ++h) {
+                uint32_t km = c.wmax[h >> 3][0][h & 7];
+#pragma unroll
+                for (int q = 1; q < 4; ++q) km = max(km, c.wmax[h >> 3][q][h & 7]);
+                const float m_new = fmaxf(m_run[h], key_score(km));
+                alpha[h] = m_run[h] > -INFINITY ? __expf(m_run[h] - m_new) : 0.0f;
+                m_run[h] = m_new;
+                if ((h >> 3) == hs) {
+                    my_m[h & 7] = m_new;
+                    my_alpha[h & 7] = alpha[h];
+                }
+            }
+            // P rows h (hi) and 16 + h (lo), column t_soft: K block t_soft / 64, element t_soft % 64
+            const uint32_t cb = static_cast<uint32_t>((t_soft & 63) >> 3), eo = static_cast<uint32_t>(t_soft & 7) * 2;
+            uint8_t *pb = smem + SM_P + (t_soft >> 6) * 4096;
+#pragma unroll
+            for (int h8 = 0; h8 < 8; ++h8) {
+                const int h = hs * 8 + h8;
+                const float m_new = my_m[h8];
+                const float e = (live && m_new > -INFINITY) ? __expf(s[h8] - m_new) : 0.0f;
+                l_part[h8] = fmaf(l_part[h8], my_alpha[h8], e);
+                const __half e_hi = __float2half_rn(e);
+                const __half e_lo = __float2half_rn(e - __half2float(e_hi));
+                *reinterpret_cast<__half *>(pb + sw128(h, cb) + eo) = e_hi;
+                *reinterpret_cast<__half *>(pb + sw128(16 + h, cb) + eo) = e_lo;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            // 6. O^T (this chunk's share, fresh accumulators) = V^T . P^T
+            if (t == 0) {
+                tc_fence_after();
+                const uint64_t b0 = sw128_kmajor_desc(sb + SM_P);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint64_t a0 = sw128_kmajor_desc(sb + SM_VT + half * 32768u);
+#pragma unroll
+                    for (int kk = 0; kk < AT_CHUNK / 16; ++kk) {
+                        const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
+                        umma_f16(tmem + 32u + 32u * half, a0 + (((kk >> 2) * 16384u + off) >> 4),
+                                 b0 + (((kk >> 2) * 4096u + off) >> 4), idesc_o, kk > 0 ? 1u : 0u);
+                    }
+                }
+                umma_commit(&c.bar_o);
+            }
+            ++ph;
+            live = live_next;
+        }
+        if (ok && n_chunks > 0) {
+            if (wait_all_threads(&c.bar_o, (ph - 1) & 1u, abort, lim)) {
+                tc_fence_after();
+                take_o();
+            } else {
+                ok = false;
             }
         }
-#pragma unroll 4
-        for (int c = 0; c < AT_CHUNK; ++c) {
-            const float2 vf = __half22float2(reinterpret_cast<const __half2 *>(&sh.v[c][0])[t]);
+        cp_async_wait_all();
+        // 8. denominators over the CTA, then the output
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            float v = l_part[h];
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
+            if (lane == 0) c.lsum[hs][lq][h] = v;
+        }
+        __syncthreads();
+        if (ok) {
+            const int32_t d = lq * 32 + lane + 128 * hs;
 #pragma unroll
             for (int h = 0; h < AT_MAXG; ++h) {
                 if (h < group) {
-                    const float w = sh.pw[h][c];
-                    acc[h][0] = fmaf(w, vf.x, acc[h][0]);
-                    acc[h][1] = fmaf(w, vf.y, acc[h][1]);
+                    const float l = (c.lsum[h >> 3][0][h & 7] + c.lsum[h >> 3][1][h & 7]) +
+                                    (c.lsum[h >> 3][2][h & 7] + c.lsum[h >> 3][3][h & 7]);
+                    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                    p.out[(static_cast<int64_t>(r) * p.hq + g * group + h) * AT_D + d] = o[h] * inv;
                 }
             }
         }
-        __syncthreads();                                  // tok / k / v / pw are rewritten next chunk
     }
-    // ---- normalise and store
-#pragma unroll
-    for (int h = 0; h < AT_MAXG; ++h) {
-        if (h < group) {
-            const float l = sh.l[h];
-            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            const float2 o = make_float2(acc[h][0] * inv, acc[h][1] * inv);
-            reinterpret_cast<float2 *>(p.out + (static_cast<int64_t>(r) * p.hq + g * group + h) * AT_D)[t] = o;
-        }
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (c.abort && t == 0) record_error(p.status, ST_TIMEOUT);
+    if (warp == 0) tmem_dealloc(tmem, AT_TMEM_COLS);
 }
 
 }  // namespace
 
-size_t attend_smem_bytes() { return sizeof(AttendShared); }
+size_t attend_smem_bytes() { return AT_SMEM; }
 
 int launch_attend(const AttendParams &p, void *stream)
 {
-    static size_t done[64] = {};
+    static std::mutex mu;
+    static bool done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
-    const size_t smem = sizeof(AttendShared);
-    if (smem > done[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(smem));
-        if (e != cudaSuccess) return static_cast<int>(e);
-        done[dev] = smem;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!done[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(AT_SMEM));
+            if (e != cudaSuccess) return static_cast<int>(e);
+            done[dev] = true;
+        }
     }
     void *args[] = {const_cast<AttendParams *>(&p)};
     return launch_kernel(reinterpret_cast<const void *>(&attend_kernel), dim3(p.rows, p.hkv), dim3(AT_THREADS),
-                         smem, static_cast<cudaStream_t>(stream), false, args);
+                         AT_SMEM, static_cast<cudaStream_t>(stream), false, args);
 }
 
 }  // namespace qsa

@@ -171,6 +171,7 @@ struct AttendParams {
     int32_t rows, hq, hkv, k, num_pages, page_tokens, page_shift, num_reqs, max_pages;
     float scale;
     uint32_t *status;
+    uint64_t wait_limit_ns;     // a tensor-core wait that takes longer gives up (QSA_ERR_TIMEOUT)
 };
 
 // Launchers (one translation unit each); return cudaError_t as int.  With
