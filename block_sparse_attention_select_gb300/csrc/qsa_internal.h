@@ -192,7 +192,8 @@ int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, c
 // that cluster size (capped by the query)
 int launch_select(const SelectParams &p, int grid, bool overlap, void *stream, int cluster_pref = 0);
 size_t select_smem_bytes(int32_t smem_cap);
-size_t cand_smem_bytes(int32_t k, int32_t cap);
+// cand_kernel's shared memory; fb_cap (if given): keys its fallback stages
+size_t cand_smem_bytes(int32_t k, int32_t cap, bool pos16, int32_t *fb_cap = nullptr);
 size_t cand_cluster_smem_bytes(int32_t k, int32_t cap);
 extern int last_cluster;    // CTAs per row of the most recent candidate-selector launch
 uint32_t score_smem_bytes();

@@ -725,6 +725,16 @@ struct CandShared {
 };
 
 constexpr size_t CAND_HEAD = ((sizeof(CandShared) > sizeof(SelShared) ? sizeof(CandShared) : sizeof(SelShared)) + 15) / 16 * 16;
+constexpr size_t CAND_HEAD_C = (sizeof(CandShared) + 15) / 16 * 16;   // cand_kernel: its own head only
+constexpr size_t SEL_HEAD = (sizeof(SelShared) + 15) / 16 * 16;
+
+// Positions of the candidates: 32-bit, stored inverted (~position), or, for
+// rows of at most 65,536 positions, 16-bit, stored as is.  Either way an
+// element's full key is (key32 << 32) | ~position.
+__device__ __forceinline__ void put_pos(uint32_t *a, uint32_t i, uint32_t pos) { a[i] = ~pos; }
+__device__ __forceinline__ void put_pos(uint16_t *a, uint32_t i, uint32_t pos) { a[i] = static_cast<uint16_t>(pos); }
+__device__ __forceinline__ uint32_t inv_pos(const uint32_t *a, uint32_t i) { return a[i]; }
+__device__ __forceinline__ uint32_t inv_pos(const uint16_t *a, uint32_t i) { return ~static_cast<uint32_t>(a[i]); }
 
 // Exclusive prefix of v over the block with a single barrier; wt alternates
 // between two buffers so that consecutive calls need no barrier in between.
@@ -770,8 +780,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // region) to a_key[done + ...], its ~position to a_pos.  Stops with overflow
 // set (the count past cap) instead of writing past cap.  The copies are
 // complete after cp_async_wait_all() and a barrier.
+template <typename PosT>
 __device__ __forceinline__ void gather_quarters(const SelectParams &p, int32_t r, int32_t e_lo, int32_t e_hi,
-                                                uint32_t *a_key, uint32_t *a_pos, CandShared &sh, int &sbuf,
+                                                uint32_t *a_key, PosT *a_pos, CandShared &sh, int &sbuf,
                                                 uint32_t &done, bool &overflow)
 {
     const int t = threadIdx.x;
@@ -802,7 +813,7 @@ __device__ __forceinline__ void gather_quarters(const SelectParams &p, int32_t r
                 const uint32_t bit = static_cast<uint32_t>(__ffs(mm) - 1);
                 mm &= mm - 1u;
                 cp_async4(a_key + o, slot + 4 * j);
-                a_pos[o] = ~(pos0 + bit);
+                put_pos(a_pos, o, pos0 + bit);
                 ++o;
             }
         }
@@ -865,14 +876,23 @@ __device__ __forceinline__ void count_and_cut(const uint32_t *a_key, uint32_t n,
     need = sh.need;
 }
 
-__global__ void __launch_bounds__(CT, 3)
+// Shared memory of cand_kernel<PosT>: its own head, bq[k + SLACK], a_key[cap],
+// a_pos[cap]; a row that falls back reuses the same bytes as SelShared,
+// out64[k + SLACK] and fb_cap (p.smem_cap) staged keys and positions, so the
+// fallback's larger head costs no resident CTAs.  With 16-bit positions a
+// top-2,048 CTA takes 55 KB: four per SM.
+template <typename PosT>
+constexpr int cand_ctas_per_sm() { return sizeof(PosT) == 2 ? 4 : 3; }
+
+template <typename PosT>
+__global__ void __launch_bounds__(CT, cand_ctas_per_sm<PosT>())
 cand_kernel(const SelectParams p)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     CandShared &sh = *reinterpret_cast<CandShared *>(smem_raw);
-    uint64_t *bq = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD);          // k + SLACK entries
+    uint64_t *bq = reinterpret_cast<uint64_t *>(smem_raw + CAND_HEAD_C);        // k + SLACK entries
     uint32_t *a_key = reinterpret_cast<uint32_t *>(bq + p.k + SLACK);            // cap entries: scores, then keys
-    uint32_t *a_pos = a_key + p.cap;                                             // cap entries: ~position
+    PosT *a_pos = reinterpret_cast<PosT *>(a_key + p.cap);                       // cap entries: positions
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const int32_t r = blockIdx.x;
     for (int i = t; i < NBINS; i += CT) sh.hist[i] = 0;
@@ -887,7 +907,9 @@ cand_kernel(const SelectParams p)
             atomicExch(&p.plan->any_fallback, 1);
         }
         __syncthreads();
-        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), bq, a_key, a_pos, p.cap);
+        uint64_t *out64 = reinterpret_cast<uint64_t *>(smem_raw + SEL_HEAD);
+        uint32_t *keys = reinterpret_cast<uint32_t *>(out64 + p.k + SLACK);
+        select_row_cold(p, r, *reinterpret_cast<SelShared *>(smem_raw), out64, keys, keys + p.smem_cap, p.smem_cap);
     };
     int32_t V = p.row_vis[r];
     if (V < 0 || V > p.max_len) {
@@ -948,7 +970,7 @@ cand_kernel(const SelectParams p)
             const uint32_t key = a_key[i];
             if (key < lo) continue;
             const uint32_t b = NBINS - 1 - ((key - lo) >> shift);
-            if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = (static_cast<uint64_t>(key) << 32) | a_pos[i];
+            if (b <= bb) bq[atomicAdd(&sh.hist[b], 1u)] = (static_cast<uint64_t>(key) << 32) | inv_pos(a_pos, i);
         }
         __syncthreads();
         // ---- rank inside the bucket = place in the output (hist[b] is now
@@ -1506,14 +1528,22 @@ int set_smem(K kernel, size_t smem, size_t (&done)[64])
 
 }  // namespace
 
-size_t cand_smem_bytes(int32_t k, int32_t cap)
+size_t cand_smem_bytes(int32_t k, int32_t cap, bool pos16, int32_t *fb_cap)
 {
-    return CAND_HEAD + static_cast<size_t>(k + SLACK) * 8 + static_cast<size_t>(cap) * 8;
+    const size_t out = static_cast<size_t>(k + SLACK) * 8;
+    const size_t plain = CAND_HEAD_C + out + static_cast<size_t>(cap) * (4 + (pos16 ? 2 : 4));
+    // the fallback stages at least max(k, 1024) keys and positions
+    const size_t fb_min = SEL_HEAD + out + static_cast<size_t>(std::max(k, 1024)) * 8;
+    const size_t bytes = (std::max(plain, fb_min) + 15) / 16 * 16;
+    if (fb_cap) *fb_cap = static_cast<int32_t>((bytes - SEL_HEAD - out) / 8);
+    return bytes;
 }
 
 size_t cand_cluster_smem_bytes(int32_t k, int32_t cap)
 {
-    return cand_smem_bytes(k, cap) + 16 + 2 * NBINS * 4 + sizeof(ClusterInfo);   // 16: alignment of the counts
+    // the cluster kernel keeps the layout with the larger head and 32-bit positions
+    const size_t base = CAND_HEAD + static_cast<size_t>(k + SLACK) * 8 + static_cast<size_t>(cap) * 8;
+    return base + 16 + 2 * NBINS * 4 + sizeof(ClusterInfo);   // 16: alignment of the counts
 }
 
 namespace {
@@ -1618,11 +1648,21 @@ int launch_select(const SelectParams &p, int grid, bool overlap, void *stream, i
             C /= 2;
         }
         last_cluster = 1;
-        static size_t done[64] = {};
-        const size_t smem = cand_smem_bytes(p.k, p.cap);
-        if (int rc = set_smem(cand_kernel, smem, done)) return rc;
-        return launch_kernel(reinterpret_cast<const void *>(&cand_kernel), dim3(p.R), dim3(CT), smem, st, overlap,
-                             args);
+        // 16-bit positions when every row fits (four CTAs per SM at k = 2,048)
+        const bool pos16 = p.max_len <= 65536;
+        SelectParams q = p;
+        const size_t smem = cand_smem_bytes(p.k, p.cap, pos16, &q.smem_cap);
+        void *qargs[] = {&q};
+        if (pos16) {
+            static size_t done16[64] = {};
+            if (int rc = set_smem(cand_kernel<uint16_t>, smem, done16)) return rc;
+            return launch_kernel(reinterpret_cast<const void *>(&cand_kernel<uint16_t>), dim3(p.R), dim3(CT), smem,
+                                 st, overlap, qargs);
+        }
+        static size_t done32[64] = {};
+        if (int rc = set_smem(cand_kernel<uint32_t>, smem, done32)) return rc;
+        return launch_kernel(reinterpret_cast<const void *>(&cand_kernel<uint32_t>), dim3(p.R), dim3(CT), smem, st,
+                             overlap, qargs);
     }
     if (p.k <= WK)                          // small k: one warp per row
         return launch_kernel(reinterpret_cast<const void *>(&warp_topk_kernel<WK>), dim3((p.R + 7) / 8), dim3(256), 0,

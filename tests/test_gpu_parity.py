@@ -80,6 +80,8 @@ CASES = [
     ([5000, 3000, 12000, 800, 20000], [1, 2, 1, 1, 3], 128, "int4", 4, 16),
     ([7000, 900, 15000], [2, 1, 1], 96, "int4", 8, 16),
     ([30000, 2000, 11000, 6000], [1, 1, 2, 1], 512, "gauss", 4, 16),
+    # rows longer than 65,536 positions: the candidate selector's 32-bit positions
+    ([282000, 5000], [3, 2], 400, "int4", 4, 64),
 ]
 
 
@@ -193,11 +195,13 @@ def test_filter_path_falls_back_when_sampling_misleads():
         np.testing.assert_array_equal(gv, ov)
 
 
-def test_filter_path_falls_back_on_candidate_overflow():
+@pytest.mark.parametrize("ctx", [40000, 280000])
+def test_filter_path_falls_back_on_candidate_overflow(ctx):
     # every score equal (w = 0): the threshold admits every position, more than
-    # the candidate capacity -> fallback; the answer is the pure tie order.
+    # the candidate capacity -> fallback; the answer is the pure tie order
+    # (280,000 tokens: rows past 65,536 positions, 32-bit candidate positions)
     k = 300
-    wl = W.make_workload("of", seed=2, ctx_tokens=[40000], rows_per_req=[5], k=k,
+    wl = W.make_workload("of", seed=2, ctx_tokens=[ctx], rows_per_req=[5], k=k,
                          dist="int4", wdist="zero")
     gi, gv = gpu_select(wl, path=qsa.PATH_FILTER)
     for r in range(wl.rows):
