@@ -1370,9 +1370,11 @@ __device__ __forceinline__ void th_reduce(ThShared<TH_THREADS> &sh, uint32_t &a_
 
 // The key that about m of the n_s keys key_at(i) reach, searched in [lo, hi]
 // (every key counted lies there).
-template <int TH_THREADS, typename KeyAt>
-__device__ uint32_t thresh_search(ThShared<TH_THREADS> &sh, KeyAt key_at, int32_t n_s, uint32_t m, uint32_t lo,
-                                  uint32_t hi)
+// STAGED: the keys are in stage[] (16-byte aligned); otherwise the scores are
+// read from row[] in every pass.
+template <int TH_THREADS, bool STAGED>
+__device__ uint32_t thresh_search(ThShared<TH_THREADS> &sh, const uint32_t *stage, const float *row, int32_t n_s,
+                                  uint32_t m, uint32_t lo, uint32_t hi)
 {
     const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
     const uint32_t stop = max(8u, m / 16);
@@ -1383,9 +1385,27 @@ __device__ uint32_t thresh_search(ThShared<TH_THREADS> &sh, KeyAt key_at, int32_
         const int shift = bits > 8 ? bits - 8 : 0;            // (hi - lo) >> shift < TH_BINS
         for (int b = t; b < TH_BINS; b += TH_THREADS) sh.hist[b] = 0;
         __syncthreads();
-        for (int32_t i = t; i < n_s; i += TH_THREADS) {
-            const uint32_t kv = key_at(i);
-            if (kv >= lo && kv <= hi) atomicAdd(&sh.hist[(kv - lo) >> shift], 1u);
+        // one unsigned compare per key: kv in [lo, hi] <=> kv - lo <= span
+        if constexpr (STAGED) {
+            const uint4 *st4 = reinterpret_cast<const uint4 *>(stage);
+            const int32_t nv = n_s >> 2;
+            for (int32_t v = t; v < nv; v += TH_THREADS) {
+                const uint4 kq = st4[v];
+                const uint32_t d0 = kq.x - lo, d1 = kq.y - lo, d2 = kq.z - lo, d3 = kq.w - lo;
+                if (d0 <= span) atomicAdd(&sh.hist[d0 >> shift], 1u);
+                if (d1 <= span) atomicAdd(&sh.hist[d1 >> shift], 1u);
+                if (d2 <= span) atomicAdd(&sh.hist[d2 >> shift], 1u);
+                if (d3 <= span) atomicAdd(&sh.hist[d3 >> shift], 1u);
+            }
+            for (int32_t i = 4 * nv + t; i < n_s; i += TH_THREADS) {
+                const uint32_t d = stage[i] - lo;
+                if (d <= span) atomicAdd(&sh.hist[d >> shift], 1u);
+            }
+        } else {
+            for (int32_t i = t; i < n_s; i += TH_THREADS) {
+                const uint32_t d = score_key(__ldcg(row + i)) - lo;
+                if (d <= span) atomicAdd(&sh.hist[d >> shift], 1u);
+            }
         }
         __syncthreads();
         if (wid == 0) {
@@ -1484,8 +1504,8 @@ thresh_kernel(const SelectParams p)
         th_reduce(sh, lo, hi, lo_pos, npos);                  // its barrier also publishes stage[]
         if (npos >= m) lo = lo_pos;
         const uint32_t T = staged
-            ? thresh_search(sh, [&](int32_t i) { return stage[i]; }, n_s, m, lo, hi)
-            : thresh_search(sh, [&](int32_t i) { return score_key(__ldcg(row + i)); }, n_s, m, lo, hi);
+            ? thresh_search<TH_THREADS, true>(sh, stage, row, n_s, m, lo, hi)
+            : thresh_search<TH_THREADS, false>(sh, stage, row, n_s, m, lo, hi);
         tau = key_score(T);
     }
     if (t == 0) p.tau[r] = tau;
