@@ -14,14 +14,14 @@
 // Every operand is K-major in the 128-byte swizzle layout: K rows are gathered
 // straight into that layout; V rows are gathered into a staging tile and
 // transposed in shared memory (8 x 8 blocks: ldmatrix.trans then stmatrix).
-// Warp w reads TMEM lane quarter w % 4 and takes half w / 4 of the work: in
-// the softmax, tokens 32 (w % 4) .. + 31 of the chunk for heads 8 (w / 4) ..
-// + 7 (scores scaled in FP32; each head's running maximum comes from warp
-// max-reductions combined through shared memory; the numerators p go to the
-// PV product as an FP16 pair, p_hi = fp16(p) and p_lo = fp16(p - p_hi) in
-// columns 0..15 and 16..31 of N, so their rounding stays near FP32); in the
-// output, dimensions 32 (w % 4) + lane + 128 (w / 4) of every head, kept in
-// registers and rescaled by exp(m_old - m_new) per chunk.  Each thread also
+// Warp w reads TMEM lane quarter w % 4 and owns heads 8 (w / 4) .. + 7: in
+// the softmax, tokens 32 (w % 4) .. + 31 of the chunk (scores scaled in FP32;
+// each head's running maximum comes from warp max-reductions combined
+// through shared memory; the numerators p go to the PV product as an FP16
+// pair, p_hi = fp16(p) and p_lo = fp16(p - p_hi) in columns 0..15 and 16..31
+// of N, so their rounding stays near FP32); in the output, dimensions
+// 32 (w % 4) + lane and that + 128, kept in registers and rescaled by
+// exp(m_old - m_new) per chunk.  Each thread also
 // keeps its share of its heads' softmax denominators, summed over the CTA at
 // the end.
 // The gather of chunk c + 1 (cp.async) is issued as soon as chunk c's score
@@ -88,21 +88,6 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8])
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(u[i]);
-}
-
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16])
-{
-    uint32_t u[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
-          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
-        : "r"(taddr)
-        : "memory");
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(u[i]);
 }
 
 // Every thread waits for the phase; false on every thread when any gave up.
@@ -187,6 +172,15 @@ attend_kernel(const AttendParams p)
         // 512-byte K row and V row each, lane l taking 16-byte chunk l);
         // returns whether the thread's softmax token is live
         const int32_t t_soft = lq * 32 + lane;
+        // copy destinations: the warp's tokens T0 + j (T0 a multiple of 8, so
+        // T & 7 = j & 7) in the K tile (16-byte chunk lane % 8 of K block
+        // lane / 8) and in the V staging tile (chunk lane, swizzled by T & 7)
+        const uint32_t T0 = static_cast<uint32_t>(lq * 32 + hs * 16);
+        const uint32_t k_dst0 = sb + SM_K + static_cast<uint32_t>(lane >> 3) * 16384u + (T0 >> 3) * 1024u;
+        const uint32_t v_dst0 = sb + SM_VS + T0 * 512u;
+        const __half *kc_l = kc + g * AT_D + lane * 8;     // this lane's 16 bytes of KV head g
+        const __half *vc_l = vc + g * AT_D + lane * 8;
+        const int64_t line_elems = static_cast<int64_t>(p.hkv) * AT_D;
         auto gather = [&](int32_t ch) -> bool {
             const int32_t pos_mine = token_at(ch * AT_CHUNK + t_soft);
             int32_t line_mine = -1;                        // page-token row of the cache, -1 = none
@@ -195,38 +189,45 @@ attend_kernel(const AttendParams p)
                 if (page >= 0 && page < p.num_pages) line_mine = page * p.page_tokens + (pos_mine & (p.page_tokens - 1));
                 else record_error(p.status, ST_BAD_PAGE);
             }
-#pragma unroll 4
+#pragma unroll
             for (int j = 0; j < 16; ++j) {
                 const int32_t line = __shfl_sync(0xffffffffu, line_mine, hs * 16 + j);
-                const uint32_t T = static_cast<uint32_t>(lq * 32 + hs * 16 + j);
-                const int64_t off = (static_cast<int64_t>(line < 0 ? 0 : line) * p.hkv + g) * AT_D + lane * 8;
-                cp_async16(sb + SM_K + (lane >> 3) * 16384 + sw128(T, lane & 7), kc + off, line >= 0);
-                cp_async16(sb + SM_VS + T * 512 + ((lane ^ (T & 7)) << 4), vc + off, line >= 0);
+                const int64_t off = static_cast<int64_t>(line < 0 ? 0 : line) * line_elems;
+                const uint32_t jj = static_cast<uint32_t>(j & 7);
+                cp_async16(k_dst0 + (j >> 3) * 1024u + jj * 128u + (((static_cast<uint32_t>(lane) & 7u) ^ jj) << 4),
+                           kc_l + off, line >= 0);
+                cp_async16(v_dst0 + static_cast<uint32_t>(j) * 512u + ((static_cast<uint32_t>(lane) ^ jj) << 4),
+                           vc_l + off, line >= 0);
             }
             return line_mine >= 0;
         };
 
-        float o[AT_MAXG];                                 // dimension 32 lq + lane + 128 hs of every head
-        float m_run[AT_MAXG], alpha[AT_MAXG];             // every head (the same in all threads)
-        float l_part[8];                                  // heads 8 hs .. 8 hs + 7
+        // this thread's heads 8 hs .. 8 hs + 7: output dims d0 = 32 lq + lane
+        // and d0 + 128, the running maximum and rescale (the same in every
+        // thread of the head set) and its share of the denominators
+        float o_lo[8], o_hi[8], m_run[8], alpha[8], l_part[8];
 #pragma unroll
-        for (int h = 0; h < AT_MAXG; ++h) {
-            o[h] = 0.0f;
+        for (int h = 0; h < 8; ++h) {
+            o_lo[h] = o_hi[h] = 0.0f;
             m_run[h] = -INFINITY;
             alpha[h] = 0.0f;
+            l_part[h] = 0.0f;
         }
-#pragma unroll
-        for (int h = 0; h < 8; ++h) l_part[h] = 0.0f;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
         constexpr uint32_t idesc_s = umma_idesc_f16_f32(AT_CHUNK, AT_MAXG);
         constexpr uint32_t idesc_o = umma_idesc_f16_f32(128, 2 * AT_MAXG);
         // output update with chunk c's PV product (alpha: that chunk's rescale)
+        // (columns 32 + 32 half + head for p_hi, + 16 for p_lo)
         auto take_o = [&]() {
-            float a[16], bq[16];
-            tmem_ld_x16(taddr + 32u + 32u * hs, a);
-            tmem_ld_x16(taddr + 48u + 32u * hs, bq);
+            float a[8], bq[8];
+            tmem_ld_x8(taddr + 32u + 8u * hs, a);
+            tmem_ld_x8(taddr + 48u + 8u * hs, bq);
 #pragma unroll
-            for (int h = 0; h < AT_MAXG; ++h) o[h] = fmaf(o[h], alpha[h], a[h] + bq[h]);
+            for (int h = 0; h < 8; ++h) o_lo[h] = fmaf(o_lo[h], alpha[h], a[h] + bq[h]);
+            tmem_ld_x8(taddr + 64u + 8u * hs, a);
+            tmem_ld_x8(taddr + 80u + 8u * hs, bq);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) o_hi[h] = fmaf(o_hi[h], alpha[h], a[h] + bq[h]);
         };
 
         bool live = n_chunks > 0 ? gather(0) : false;
@@ -255,20 +256,28 @@ attend_kernel(const AttendParams p)
                 tc_fence_after();
                 take_o();
             }
-            // 4. V^T: 8 x 8 blocks (8 tokens x 8 dims), four per instruction
-            for (int it = warp; it < 128; it += AT_THREADS / 32) {
-                const uint32_t tb = static_cast<uint32_t>(it >> 3), dq = static_cast<uint32_t>(it & 7);
-                const uint32_t i = static_cast<uint32_t>(lane >> 3), j = static_cast<uint32_t>(lane & 7);
-                const uint32_t T = tb * 8 + j, db = dq * 4 + i;    // source row (token) and 16-B chunk (dims)
-                uint32_t x0, x1, x2, x3;
-                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
-                             : "r"(sb + SM_VS + T * 512 + ((db ^ (T & 7)) << 4)));
-                const uint32_t D = db * 8 + j;                     // destination row (dim)
-                const uint32_t dst = sb + SM_VT + (D >> 7) * 32768u + (tb >> 3) * 16384u + sw128(D & 127u, tb & 7);
-                asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(x0),
-                             "r"(x1), "r"(x2), "r"(x3)
-                             : "memory");
+            // 4. V^T: 8 x 8 blocks (8 tokens x 8 dims), four per instruction.
+            //    Warp w moves dims 32 w .. 32 w + 31 (16-byte chunks 4 w + i of
+            //    the staging rows, i = lane / 8) of every 8-token block tb;
+            //    lane l addresses row l % 8 of matrix l / 8.
+            {
+                const uint32_t tj = static_cast<uint32_t>(lane & 7);
+                const uint32_t db = static_cast<uint32_t>(warp * 4 + (lane >> 3));   // source chunk (dims 8 db ..)
+                const uint32_t src0 = sb + SM_VS + tj * 512u + ((db ^ tj) << 4);    // token 8 tb + tj: + tb * 4 KiB
+                const uint32_t D = db * 8u + tj;                                     // destination row (dim)
+                const uint32_t dst0 = sb + SM_VT + (D >> 7) * 32768u + ((D & 127u) >> 3) * 1024u + tj * 128u;
+#pragma unroll
+                for (int tb = 0; tb < AT_CHUNK / 8; ++tb) {
+                    uint32_t x0, x1, x2, x3;
+                    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                                 : "r"(src0 + static_cast<uint32_t>(tb) * 4096u));
+                    const uint32_t dst = dst0 + static_cast<uint32_t>(tb >> 3) * 16384u +
+                                         (((static_cast<uint32_t>(tb) & 7u) ^ tj) << 4);
+                    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(x0),
+                                 "r"(x1), "r"(x2), "r"(x3)
+                                 : "memory");
+                }
             }
             // 5. softmax of the chunk (token t_soft, heads 8 hs .. 8 hs + 7)
             if (!wait_all_threads(&c.bar_s, ph & 1u, abort, lim)) { ok = false; break; }
@@ -286,19 +295,14 @@ attend_kernel(const AttendParams p)
             // every warp has finished its part of V^T), so the copies run
             // under this chunk's softmax, PV product and output update
             const bool live_next = ch + 1 < n_chunks ? gather(ch + 1) : false;
-            float my_m[8], my_alpha[8];                   // this thread's heads (constant indices only)
 #pragma unroll
-            for (int h = 0; h < AT_MAXG; ++h) {
-                uint32_t km = c.wmax[h >> 3][0][h & 7];
+            for (int h = 0; h < 8; ++h) {
+                uint32_t km = c.wmax[hs][0][h];
 #pragma unroll
-                for (int q = 1; q < 4; ++q) km = max(km, c.wmax[h >> 3][q][h & 7]);
+                for (int q = 1; q < 4; ++q) km = max(km, c.wmax[hs][q][h]);
                 const float m_new = fmaxf(m_run[h], key_score(km));
                 alpha[h] = m_run[h] > -INFINITY ? __expf(m_run[h] - m_new) : 0.0f;
                 m_run[h] = m_new;
-                if ((h >> 3) == hs) {
-                    my_m[h & 7] = m_new;
-                    my_alpha[h & 7] = alpha[h];
-                }
             }
             // P rows h (hi) and 16 + h (lo), column t_soft: K block t_soft / 64, element t_soft % 64
             const uint32_t cb = static_cast<uint32_t>((t_soft & 63) >> 3), eo = static_cast<uint32_t>(t_soft & 7) * 2;
@@ -306,9 +310,9 @@ attend_kernel(const AttendParams p)
 #pragma unroll
             for (int h8 = 0; h8 < 8; ++h8) {
                 const int h = hs * 8 + h8;
-                const float m_new = my_m[h8];
+                const float m_new = m_run[h8];
                 const float e = (live && m_new > -INFINITY) ? __expf(s[h8] - m_new) : 0.0f;
-                l_part[h8] = fmaf(l_part[h8], my_alpha[h8], e);
+                l_part[h8] = fmaf(l_part[h8], alpha[h8], e);
                 const __half e_hi = __float2half_rn(e);
                 const __half e_lo = __float2half_rn(e - __half2float(e_hi));
                 *reinterpret_cast<__half *>(pb + sw128(h, cb) + eo) = e_hi;
@@ -355,14 +359,16 @@ attend_kernel(const AttendParams p)
         }
         __syncthreads();
         if (ok) {
-            const int32_t d = lq * 32 + lane + 128 * hs;
+            const int32_t d0 = lq * 32 + lane;
 #pragma unroll
-            for (int h = 0; h < AT_MAXG; ++h) {
+            for (int h8 = 0; h8 < 8; ++h8) {
+                const int h = hs * 8 + h8;
                 if (h < group) {
-                    const float l = (c.lsum[h >> 3][0][h & 7] + c.lsum[h >> 3][1][h & 7]) +
-                                    (c.lsum[h >> 3][2][h & 7] + c.lsum[h >> 3][3][h & 7]);
+                    const float l = (c.lsum[hs][0][h8] + c.lsum[hs][1][h8]) + (c.lsum[hs][2][h8] + c.lsum[hs][3][h8]);
                     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-                    p.out[(static_cast<int64_t>(r) * p.hq + g * group + h) * AT_D + d] = o[h] * inv;
+                    float *out = p.out + (static_cast<int64_t>(r) * p.hq + g * group + h) * AT_D;
+                    out[d0] = o_lo[h8] * inv;
+                    out[d0 + 128] = o_hi[h8] * inv;
                 }
             }
         }
