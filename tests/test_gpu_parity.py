@@ -233,6 +233,21 @@ def test_k_equals_one_and_max_k():
         np.testing.assert_array_equal(gv, ov)
 
 
+@pytest.mark.parametrize("ctx", [160000, 280000])
+def test_filter_path_at_max_k(ctx):
+    # The candidate selector at its largest shared-memory footprint (k =
+    # QSA_MAX_K): 40,000 positions (16-bit candidate positions) and 70,000
+    # (32-bit), both against the oracle.
+    k = qsa.QSA_MAX_K
+    wl = W.make_workload("kmax", seed=5, ctx_tokens=[ctx], rows_per_req=[3], k=k, dist="int4")
+    assert wl.row_visible.min() >= 3 * k
+    oi, ov, _ = oracle.select_paged_tokens(wl.q, wl.w, wl.k_cache, wl.block_table, wl.row_req,
+                                           wl.row_visible, k, ld=wl.ld)
+    gi, gv = gpu_select(wl, path=qsa.PATH_FILTER)
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov)
+
+
 # ---------------------------------------------------- selector on its own ----
 
 @pytest.mark.parametrize("n,k,kind", [(5000, 700, "gauss"), (30000, 2048, "gauss"),
