@@ -725,7 +725,7 @@ def run_attend(args, ws, rank, local):
         "config": {"workload": inp.name, "rows": R, "q_heads": hq, "kv_heads": hkv, "head_dim": D, "k": 2048,
                    "tokens_attended": toks, "gathered_gb": gathered / 1e9,
                    "l2": "flushed between steps (512 MiB write)", "median_ms": statistics.median(step_ms)},
-        # QK and PV are contractions: judged against the dense FP16 tensor peak;
+        # QK and PV are contractions: measured against the dense FP16 tensor peak;
         # the gathered K / V lines (~12 FLOP per byte, each row reading its own
         # tokens from a cache larger than L2) give the memory-side bound beside it
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
