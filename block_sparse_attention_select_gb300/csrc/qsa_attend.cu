@@ -39,9 +39,15 @@ namespace qsa {
 namespace {
 
 constexpr int AT_D = 256;                   // head dimension
-constexpr int AT_THREADS = 256;             // two warps per TMEM lane quarter
+// head sets (warps per TMEM lane quarter): 2 measured 5.01 ms at the 1,616-row
+// bench, 4 (512 threads, 4 heads per warp) 5.24 ms
+constexpr int AT_SETS = 2;
+constexpr int AT_THREADS = 128 * AT_SETS;
+constexpr int AT_WARPS = AT_THREADS / 32;
 constexpr int AT_CHUNK = 128;               // tokens per chunk (MMA M of the score product)
 constexpr int AT_MAXG = 16;                 // query heads per KV head (MMA N of the score product)
+constexpr int AT_HPW = AT_MAXG / AT_SETS;   // heads per warp
+constexpr int AT_TPW = 32 / AT_SETS;        // tokens each warp copies per chunk
 constexpr uint32_t AT_TMEM_COLS = 128;      // S: columns 0..15; O: 32..63 (dims 0..127), 64..95 (128..255)
 
 // shared memory, offsets from a 1024-byte aligned base
@@ -56,8 +62,8 @@ struct AtCtrl {
     uint64_t bar_o;                         // PV product done
     uint32_t tmem_base;
     int32_t abort;
-    uint32_t wmax[2][4][8];                 // [head set][lane quarter][head]: maxima of the chunk (score keys)
-    float lsum[2][4][8];                    // the same for the denominators (end of the row)
+    uint32_t wmax[AT_SETS][4][AT_HPW];      // [head set][lane quarter][head]: maxima of the chunk (score keys)
+    float lsum[AT_SETS][4][AT_HPW];         // the same for the denominators (end of the row)
 };
 constexpr uint32_t AT_SMEM = SM_CTRL + sizeof(AtCtrl) + 1024;
 static_assert(AT_SMEM <= 232448, "shared memory budget");
@@ -78,16 +84,26 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool f
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8])
+// N (4 or 8) consecutive 32-bit columns of this warp's 32 TMEM lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N])
 {
-    uint32_t u[8];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
-                 : "r"(taddr)
-                 : "memory");
+    static_assert(N == 4 || N == 8, "x4 or x8");
+    uint32_t u[N];
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                     : "r"(taddr)
+                     : "memory");
+    }
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(u[i]);
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(u[i]);
 }
 
 // Every thread waits for the phase; false on every thread when any gave up.
@@ -106,7 +122,7 @@ attend_kernel(const AttendParams p)
     const uint32_t sb = smem_u32(smem);
     AtCtrl &c = *reinterpret_cast<AtCtrl *>(smem + SM_CTRL);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int lq = warp & 3, hs = warp >> 2;      // TMEM lane quarter, half of the work
+    const int lq = warp & 3, hs = warp >> 2;      // TMEM lane quarter, head set
     const int32_t r = blockIdx.x, g = blockIdx.y;
 
     if (t == 0) {
@@ -168,14 +184,14 @@ attend_kernel(const AttendParams p)
             return pos;
         };
         // gather of chunk ch: every thread looks up its softmax token
-        // 32 lq + lane; warp w copies tokens 32 lq + 16 hs + j, j < 16 (one
+        // 32 lq + lane; warp w copies tokens 32 lq + AT_TPW hs + j, j < AT_TPW (one
         // 512-byte K row and V row each, lane l taking 16-byte chunk l);
         // returns whether the thread's softmax token is live
         const int32_t t_soft = lq * 32 + lane;
         // copy destinations: the warp's tokens T0 + j (T0 a multiple of 8, so
         // T & 7 = j & 7) in the K tile (16-byte chunk lane % 8 of K block
         // lane / 8) and in the V staging tile (chunk lane, swizzled by T & 7)
-        const uint32_t T0 = static_cast<uint32_t>(lq * 32 + hs * 16);
+        const uint32_t T0 = static_cast<uint32_t>(lq * 32 + hs * AT_TPW);
         const uint32_t k_dst0 = sb + SM_K + static_cast<uint32_t>(lane >> 3) * 16384u + (T0 >> 3) * 1024u;
         const uint32_t v_dst0 = sb + SM_VS + T0 * 512u;
         const __half *kc_l = kc + g * AT_D + lane * 8;     // this lane's 16 bytes of KV head g
@@ -190,8 +206,8 @@ attend_kernel(const AttendParams p)
                 else record_error(p.status, ST_BAD_PAGE);
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int32_t line = __shfl_sync(0xffffffffu, line_mine, hs * 16 + j);
+            for (int j = 0; j < AT_TPW; ++j) {
+                const int32_t line = __shfl_sync(0xffffffffu, line_mine, hs * AT_TPW + j);
                 const int64_t off = static_cast<int64_t>(line < 0 ? 0 : line) * line_elems;
                 const uint32_t jj = static_cast<uint32_t>(j & 7);
                 cp_async16(k_dst0 + (j >> 3) * 1024u + jj * 128u + (((static_cast<uint32_t>(lane) & 7u) ^ jj) << 4),
@@ -202,12 +218,12 @@ attend_kernel(const AttendParams p)
             return line_mine >= 0;
         };
 
-        // this thread's heads 8 hs .. 8 hs + 7: output dims d0 = 32 lq + lane
+        // this thread's heads AT_HPW hs .. + AT_HPW - 1: output dims d0 = 32 lq + lane
         // and d0 + 128, the running maximum and rescale (the same in every
         // thread of the head set) and its share of the denominators
-        float o_lo[8], o_hi[8], m_run[8], alpha[8], l_part[8];
+        float o_lo[AT_HPW], o_hi[AT_HPW], m_run[AT_HPW], alpha[AT_HPW], l_part[AT_HPW];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
+        for (int h = 0; h < AT_HPW; ++h) {
             o_lo[h] = o_hi[h] = 0.0f;
             m_run[h] = -INFINITY;
             alpha[h] = 0.0f;
@@ -219,15 +235,16 @@ attend_kernel(const AttendParams p)
         // output update with chunk c's PV product (alpha: that chunk's rescale)
         // (columns 32 + 32 half + head for p_hi, + 16 for p_lo)
         auto take_o = [&]() {
-            float a[8], bq[8];
-            tmem_ld_x8(taddr + 32u + 8u * hs, a);
-            tmem_ld_x8(taddr + 48u + 8u * hs, bq);
+            float a[AT_HPW], bq[AT_HPW];
+            const uint32_t hc = static_cast<uint32_t>(AT_HPW * hs);
+            tmem_ld_cols(taddr + 32u + hc, a);
+            tmem_ld_cols(taddr + 48u + hc, bq);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) o_lo[h] = fmaf(o_lo[h], alpha[h], a[h] + bq[h]);
-            tmem_ld_x8(taddr + 64u + 8u * hs, a);
-            tmem_ld_x8(taddr + 80u + 8u * hs, bq);
+            for (int h = 0; h < AT_HPW; ++h) o_lo[h] = fmaf(o_lo[h], alpha[h], a[h] + bq[h]);
+            tmem_ld_cols(taddr + 64u + hc, a);
+            tmem_ld_cols(taddr + 80u + hc, bq);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) o_hi[h] = fmaf(o_hi[h], alpha[h], a[h] + bq[h]);
+            for (int h = 0; h < AT_HPW; ++h) o_hi[h] = fmaf(o_hi[h], alpha[h], a[h] + bq[h]);
         };
 
         bool live = n_chunks > 0 ? gather(0) : false;
@@ -257,17 +274,18 @@ attend_kernel(const AttendParams p)
                 take_o();
             }
             // 4. V^T: 8 x 8 blocks (8 tokens x 8 dims), four per instruction.
-            //    Warp w moves dims 32 w .. 32 w + 31 (16-byte chunks 4 w + i of
-            //    the staging rows, i = lane / 8) of every 8-token block tb;
-            //    lane l addresses row l % 8 of matrix l / 8.
+            //    Warp w moves dims 32 (w % 8) .. + 31 (16-byte chunks 4 (w % 8) + i
+            //    of the staging rows, i = lane / 8) of the 8-token blocks
+            //    tb = w / 8, w / 8 + AT_WARPS / 8, ...; lane l addresses row
+            //    l % 8 of matrix l / 8.
             {
                 const uint32_t tj = static_cast<uint32_t>(lane & 7);
-                const uint32_t db = static_cast<uint32_t>(warp * 4 + (lane >> 3));   // source chunk (dims 8 db ..)
+                const uint32_t db = static_cast<uint32_t>((warp & 7) * 4 + (lane >> 3));   // source chunk (dims 8 db ..)
                 const uint32_t src0 = sb + SM_VS + tj * 512u + ((db ^ tj) << 4);    // token 8 tb + tj: + tb * 4 KiB
                 const uint32_t D = db * 8u + tj;                                     // destination row (dim)
                 const uint32_t dst0 = sb + SM_VT + (D >> 7) * 32768u + ((D & 127u) >> 3) * 1024u + tj * 128u;
 #pragma unroll
-                for (int tb = 0; tb < AT_CHUNK / 8; ++tb) {
+                for (int tb = warp >> 3; tb < AT_CHUNK / 8; tb += AT_WARPS / 8) {
                     uint32_t x0, x1, x2, x3;
                     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                                  : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
@@ -279,13 +297,13 @@ attend_kernel(const AttendParams p)
                                  : "memory");
                 }
             }
-            // 5. softmax of the chunk (token t_soft, heads 8 hs .. 8 hs + 7)
+            // 5. softmax of the chunk (token t_soft, this warp's heads)
             if (!wait_all_threads(&c.bar_s, ph & 1u, abort, lim)) { ok = false; break; }
             tc_fence_after();
-            float s[8];
-            tmem_ld_x8(taddr + 8u * hs, s);
+            float s[AT_HPW];
+            tmem_ld_cols(taddr + static_cast<uint32_t>(AT_HPW * hs), s);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
+            for (int h = 0; h < AT_HPW; ++h) {
                 s[h] = live ? s[h] * p.scale : -INFINITY;
                 const uint32_t kmax = __reduce_max_sync(0xffffffffu, score_key(s[h]));
                 if (lane == 0) c.wmax[hs][lq][h] = kmax;
@@ -296,7 +314,7 @@ attend_kernel(const AttendParams p)
             // under this chunk's softmax, PV product and output update
             const bool live_next = ch + 1 < n_chunks ? gather(ch + 1) : false;
 #pragma unroll
-            for (int h = 0; h < 8; ++h) {
+            for (int h = 0; h < AT_HPW; ++h) {
                 uint32_t km = c.wmax[hs][0][h];
 #pragma unroll
                 for (int q = 1; q < 4; ++q) km = max(km, c.wmax[hs][q][h]);
@@ -308,8 +326,8 @@ attend_kernel(const AttendParams p)
             const uint32_t cb = static_cast<uint32_t>((t_soft & 63) >> 3), eo = static_cast<uint32_t>(t_soft & 7) * 2;
             uint8_t *pb = smem + SM_P + (t_soft >> 6) * 4096;
 #pragma unroll
-            for (int h8 = 0; h8 < 8; ++h8) {
-                const int h = hs * 8 + h8;
+            for (int h8 = 0; h8 < AT_HPW; ++h8) {
+                const int h = hs * AT_HPW + h8;
                 const float m_new = m_run[h8];
                 const float e = (live && m_new > -INFINITY) ? __expf(s[h8] - m_new) : 0.0f;
                 l_part[h8] = fmaf(l_part[h8], alpha[h8], e);
@@ -351,7 +369,7 @@ attend_kernel(const AttendParams p)
         cp_async_wait_all();
         // 8. denominators over the CTA, then the output
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
+        for (int h = 0; h < AT_HPW; ++h) {
             float v = l_part[h];
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o2);
@@ -361,8 +379,8 @@ attend_kernel(const AttendParams p)
         if (ok) {
             const int32_t d0 = lq * 32 + lane;
 #pragma unroll
-            for (int h8 = 0; h8 < 8; ++h8) {
-                const int h = hs * 8 + h8;
+            for (int h8 = 0; h8 < AT_HPW; ++h8) {
+                const int h = hs * AT_HPW + h8;
                 if (h < group) {
                     const float l = (c.lsum[hs][0][h8] + c.lsum[hs][1][h8]) + (c.lsum[hs][2][h8] + c.lsum[hs][3][h8]);
                     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
