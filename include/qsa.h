@@ -109,9 +109,11 @@ qsa_status qsa_topk_exact(const float *logits, int64_t ld_logits, int32_t rows,
  * this file).  q, w, keys, row_req, row_visible as for qsa_index_score; k,
  * out_idx, out_val as for qsa_topk_exact; ws must hold qsa_workspace_bytes(rows,
  * max_pages_per_req * page_positions, k, 0) bytes, 256-byte aligned.
- * For long rows (at least 3k positions) it scores every 16th-or-so key tile
- * first, takes from that sample a per-row threshold expected to keep ~1.5 k
- * positions, scores every tile keeping only the positions at or above it, and
+ * For long rows (at least 3k positions, k >= 342) it scores every 16th key
+ * tile (32nd for k >= 2,731) first, takes from that sample a per-row
+ * threshold expected to keep 1.5 k positions or more (more for smaller k, so
+ * that the expected count stays 4.5 standard deviations above k), scores
+ * every tile keeping only the positions at or above it, and
  * selects among those; a row that kept fewer than min(k, V_r) (or too many to
  * hold) is re-scored in plain FP32 and selected from all its positions, so the
  * result never depends on the sample.  Shorter rows are scored into the
