@@ -171,38 +171,46 @@ attend_kernel(const AttendParams p)
             *reinterpret_cast<uint4 *>(smem + SM_Q + (l >> 3) * 2048 + sw128(h, l & 7)) = v;
         }
 
-        // token of stream index s (or -1), with the device-side checks
-        auto token_at = [&](int32_t s) -> int32_t {
-            int32_t pos = -1;
-            if (s < 4 * p.k) {
-                const int32_t j = selr[s >> 2];
-                if (j >= 0 && j < vis) pos = 4 * j + (s & 3);
-                else if (j >= vis && (s & 3) == 0) record_error(p.status, ST_BAD_ROW);
-            } else if (s < n_stream) {
-                pos = tail0 + (s - 4 * p.k);
-            }
-            return pos;
-        };
-        // gather of chunk ch: every thread looks up its softmax token
-        // 32 lq + lane; warp w copies tokens 32 lq + AT_TPW hs + j, j < AT_TPW (one
-        // 512-byte K row and V row each, lane l taking 16-byte chunk l);
-        // returns whether the thread's softmax token is live
+        // Token lookups of the thread's softmax token 32 lq + lane of each
+        // chunk, run ahead of the copies: while chunk c is copied, the page of
+        // chunk c + 1 and the selection slot of chunk c + 2 are loaded, so no
+        // copy waits for a dependent global load.
         const int32_t t_soft = lq * 32 + lane;
+        auto slot_of = [&](int32_t ch) -> int32_t {          // selection slot value (or 0 past the slots)
+            const int32_t st = ch * AT_CHUNK + t_soft;
+            return ch < n_chunks && st < 4 * p.k ? selr[st >> 2] : 0;
+        };
+        auto pos_of = [&](int32_t ch, int32_t j) -> int32_t {  // token position, -1 = none (with the checks)
+            const int32_t st = ch * AT_CHUNK + t_soft;
+            if (ch >= n_chunks) return -1;
+            if (st < 4 * p.k) {
+                if (j >= 0 && j < vis) return 4 * j + (st & 3);
+                if (j >= vis && (st & 3) == 0) record_error(p.status, ST_BAD_ROW);
+                return -1;
+            }
+            return st < n_stream ? tail0 + (st - 4 * p.k) : -1;
+        };
+        auto page_of = [&](int32_t pos) -> int32_t { return pos >= 0 ? bt[pos >> p.page_shift] : -1; };
+        int32_t pos_c = pos_of(0, slot_of(0));
+        int32_t page_c = page_of(pos_c);
+        int32_t slot_n = slot_of(1);
         // copy destinations: the warp's tokens T0 + j (T0 a multiple of 8, so
         // T & 7 = j & 7) in the K tile (16-byte chunk lane % 8 of K block
-        // lane / 8) and in the V staging tile (chunk lane, swizzled by T & 7)
+        // lane / 8) and in the V staging tile (chunk lane, swizzled by T & 7);
+        // warp w copies tokens 32 lq + AT_TPW hs + j, j < AT_TPW (one 512-byte
+        // K row and V row each, lane l taking 16-byte chunk l)
         const uint32_t T0 = static_cast<uint32_t>(lq * 32 + hs * AT_TPW);
         const uint32_t k_dst0 = sb + SM_K + static_cast<uint32_t>(lane >> 3) * 16384u + (T0 >> 3) * 1024u;
         const uint32_t v_dst0 = sb + SM_VS + T0 * 512u;
         const __half *kc_l = kc + g * AT_D + lane * 8;     // this lane's 16 bytes of KV head g
         const __half *vc_l = vc + g * AT_D + lane * 8;
         const int64_t line_elems = static_cast<int64_t>(p.hkv) * AT_D;
+        // gather of chunk ch (the chunks in order); returns whether the
+        // thread's softmax token is live
         auto gather = [&](int32_t ch) -> bool {
-            const int32_t pos_mine = token_at(ch * AT_CHUNK + t_soft);
             int32_t line_mine = -1;                        // page-token row of the cache, -1 = none
-            if (pos_mine >= 0) {
-                const int32_t page = bt[pos_mine >> p.page_shift];
-                if (page >= 0 && page < p.num_pages) line_mine = page * p.page_tokens + (pos_mine & (p.page_tokens - 1));
+            if (pos_c >= 0) {
+                if (page_c >= 0 && page_c < p.num_pages) line_mine = page_c * p.page_tokens + (pos_c & (p.page_tokens - 1));
                 else record_error(p.status, ST_BAD_PAGE);
             }
 #pragma unroll
@@ -215,6 +223,9 @@ attend_kernel(const AttendParams p)
                 cp_async16(v_dst0 + static_cast<uint32_t>(j) * 512u + ((static_cast<uint32_t>(lane) ^ jj) << 4),
                            vc_l + off, line >= 0);
             }
+            pos_c = pos_of(ch + 1, slot_n);
+            page_c = page_of(pos_c);                       // in flight until the next call
+            slot_n = slot_of(ch + 2);
             return line_mine >= 0;
         };
 
