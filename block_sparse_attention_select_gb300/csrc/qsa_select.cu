@@ -631,18 +631,29 @@ select_kernel(const SelectParams p)
 //
 // Dense rows with k <= WK (the block scorer's top-16 blocks): one warp per
 // row.  Every element becomes its full key (key32 << 32 | ~index), all
-// distinct, so the order is exact.  Each lane keeps the WK largest keys it has
-// seen, sorted, in registers (most elements only compare with the smallest);
-// then min(k, V) rounds of a warp-wide maximum over the lanes' heads emit the
-// result in order, the winning lane dropping its head.
+// distinct, so the order is exact.  Pass 1: each lane's largest key; T = the
+// K-th largest of the 32 lane maxima, so at least K elements reach T and the
+// top K lie among those that do.  Pass 2 collects the elements >= T into the
+// warp's buffer (ballot compaction) and a warp sort orders them.  When more
+// than WT_CAP elements reach T (one lane holding many of the largest), the
+// row falls back to per-lane sorted lists of the K largest keys (most
+// elements only compare with the smallest) merged by min(k, V) rounds of a
+// warp-wide maximum.
 constexpr int WK = 16;
+constexpr int WT_CAP = 128;             // elements >= T the warp buffer holds
+
+__device__ __forceinline__ uint64_t dense_key(const float *row, int32_t j)
+{
+    return (static_cast<uint64_t>(score_key(__ldg(row + j))) << 32) | ~static_cast<uint32_t>(j);
+}
 
 template <int K>
 __global__ void __launch_bounds__(256)
 warp_topk_kernel(const SelectParams p)
 {
-    const int lane = threadIdx.x & 31;
-    const int32_t r = static_cast<int32_t>(blockIdx.x) * 8 + static_cast<int32_t>(threadIdx.x >> 5);
+    __shared__ uint64_t wbuf[8][WT_CAP];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int32_t r = static_cast<int32_t>(blockIdx.x) * 8 + static_cast<int32_t>(wid);
     wait_prior_grid();                      // last kernel of its call: nothing to allow
     if (r >= p.R) return;
     int32_t V = p.row_vis[r];
@@ -651,21 +662,6 @@ warp_topk_kernel(const SelectParams p)
         V = static_cast<int32_t>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(V), p.max_len)));
     }
     const float *row = p.logits + static_cast<int64_t>(r) * p.ld;
-    uint64_t x[K];
-#pragma unroll
-    for (int i = 0; i < K; ++i) x[i] = 0ull;   // below every real key (key32 > 0 for every float)
-    for (int32_t j = lane; j < V; j += 32) {
-        const uint64_t key = (static_cast<uint64_t>(score_key(__ldcg(row + j))) << 32) | ~static_cast<uint32_t>(j);
-        if (key > x[K - 1]) {
-            x[K - 1] = key;
-#pragma unroll
-            for (int i = K - 1; i > 0; --i) {
-                const uint64_t a = x[i - 1], b = x[i];
-                x[i - 1] = b > a ? b : a;
-                x[i] = b > a ? a : b;
-            }
-        }
-    }
     int64_t ro = r;
     if (p.out_heads > 1) {                  // virtual row r = h * n + row -> output row row * H + h
         const int32_t n = p.R / p.out_heads;
@@ -674,21 +670,73 @@ warp_topk_kernel(const SelectParams p)
     int32_t *oi = p.out_idx + ro * p.k;
     float *ov = p.out_val ? p.out_val + ro * p.k : nullptr;
     const int32_t kk = min(p.k, V);
-    for (int32_t o = 0; o < kk; ++o) {
-        uint64_t best = x[0];
-#pragma unroll
-        for (int sft = 16; sft > 0; sft >>= 1) {
-            const uint64_t other = __shfl_xor_sync(0xffffffffu, best, sft);
-            best = other > best ? other : best;
-        }
-        if (x[0] == best) {                 // exactly one lane: the keys are distinct
-#pragma unroll
-            for (int i = 0; i < K - 1; ++i) x[i] = x[i + 1];
-            x[K - 1] = 0ull;
-        }
-        if (lane == 0) {
+    uint64_t *buf = wbuf[wid];
+
+    // pass 1: the lane's largest key (0, below every real key, for none)
+    uint64_t mx = 0ull;
+    for (int32_t j = lane; j < V; j += 32) {
+        const uint64_t key = dense_key(row, j);
+        mx = key > mx ? key : mx;
+    }
+    buf[lane] = mx;
+    __syncwarp();
+    warp_sort32_desc(buf, 32);
+    __syncwarp();
+    const uint64_t T = buf[K - 1];
+    __syncwarp();
+    // pass 2: the elements >= T, in index order, into the buffer
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t cnt = 0;
+    for (int32_t j0 = 0; j0 < V; j0 += 32) {
+        const int32_t j = j0 + lane;
+        const uint64_t key = j < V ? dense_key(row, j) : 0ull;
+        const bool take = j < V && key >= T;
+        const uint32_t bal = __ballot_sync(0xffffffffu, take);
+        const uint32_t at = cnt + static_cast<uint32_t>(__popc(bal & lt));
+        if (take && at < static_cast<uint32_t>(WT_CAP)) buf[at] = key;
+        cnt += static_cast<uint32_t>(__popc(bal));
+    }
+    __syncwarp();
+    if (cnt <= static_cast<uint32_t>(WT_CAP)) {               // uniform
+        warp_sort_desc(buf, static_cast<int32_t>(cnt));
+        __syncwarp();
+        for (int32_t o = lane; o < kk; o += 32) {
+            const uint64_t best = buf[o];
             oi[o] = static_cast<int32_t>(~static_cast<uint32_t>(best));
             if (ov) ov[o] = key_score(static_cast<uint32_t>(best >> 32));
+        }
+    } else {
+        uint64_t x[K];
+#pragma unroll
+        for (int i = 0; i < K; ++i) x[i] = 0ull;
+        for (int32_t j = lane; j < V; j += 32) {
+            const uint64_t key = dense_key(row, j);
+            if (key > x[K - 1]) {
+                x[K - 1] = key;
+#pragma unroll
+                for (int i = K - 1; i > 0; --i) {
+                    const uint64_t a = x[i - 1], b = x[i];
+                    x[i - 1] = b > a ? b : a;
+                    x[i] = b > a ? a : b;
+                }
+            }
+        }
+        for (int32_t o = 0; o < kk; ++o) {
+            uint64_t best = x[0];
+#pragma unroll
+            for (int sft = 16; sft > 0; sft >>= 1) {
+                const uint64_t other = __shfl_xor_sync(0xffffffffu, best, sft);
+                best = other > best ? other : best;
+            }
+            if (x[0] == best) {             // exactly one lane: the keys are distinct
+#pragma unroll
+                for (int i = 0; i < K - 1; ++i) x[i] = x[i + 1];
+                x[K - 1] = 0ull;
+            }
+            if (lane == 0) {
+                oi[o] = static_cast<int32_t>(~static_cast<uint32_t>(best));
+                if (ov) ov[o] = key_score(static_cast<uint32_t>(best >> 32));
+            }
         }
     }
     for (int32_t o = kk + lane; o < p.k; o += 32) {
