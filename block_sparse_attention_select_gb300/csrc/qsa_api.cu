@@ -792,12 +792,12 @@ qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *
     if (!aligned(ws, 256)) return QSA_ERR_INVALID_ARG;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     auto i32 = [&](size_t off) { return reinterpret_cast<int32_t *>(w8 + off); };
-    // queries [rows][H][128], boxes of one head x 256 rows; keys [pages * 128
-    // tokens][H][128], boxes of one head x 128 tokens (strides increase with the
-    // dimension in both maps)
+    // queries [rows][H][128], boxes of one head x BR_ROWS rows; keys [pages *
+    // 128 tokens][H][128], boxes of one head x 128 tokens (strides increase
+    // with the dimension in both maps)
     CUtensorMap tq, tk;
     if ((st = make_tmap3(&tq, q, static_cast<uint64_t>(H), static_cast<uint64_t>(rows), HEAD_DIM * 2,
-                         static_cast<uint64_t>(H) * HEAD_DIM * 2, 1, N_MAX)) != QSA_OK)
+                         static_cast<uint64_t>(H) * HEAD_DIM * 2, 1, BR_ROWS)) != QSA_OK)
         return st;
     if ((st = make_tmap3(&tk, k_cache, static_cast<uint64_t>(H), static_cast<uint64_t>(num_pages) * TILE_M,
                          HEAD_DIM * 2, static_cast<uint64_t>(H) * HEAD_DIM * 2, 1, TILE_M)) != QSA_OK)
@@ -807,10 +807,11 @@ qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *
                                           i32(L.vblk), d->status, stream))) != QSA_OK)
         return st;
     if ((st = launch_rc(timed(K_PLAN, stream, [&] {
-             return launch_plan(i32(L.vreq), i32(L.vtok), RVi, N_MAX, num_reqs * H,
+             // groups of BR_ROWS virtual rows of one head, tiles of two 128-token blocks
+             return launch_plan(i32(L.vreq), i32(L.vtok), RVi, BR_ROWS, num_reqs * H,
                                 static_cast<int64_t>(max_blocks) * TILE_M, 1, i32(L.row_vis),
                                 reinterpret_cast<Group *>(w8 + L.groups), i32(L.item_prefix), i32(L.sample_prefix),
-                                reinterpret_cast<Plan *>(w8 + L.plan), d->status, stream);
+                                reinterpret_cast<Plan *>(w8 + L.plan), d->status, stream, 8);
          }))) != QSA_OK)
         return st;
     ScoreParams sp;
@@ -839,7 +840,7 @@ qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *
     sp.blk_reqs = num_reqs;
     sp.blk_rows = rows;
     if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] {
-             return launch_score(sp, &tq, &tk, &tk, d->sms, g_overlap, stream);
+             return launch_score_blockrows(sp, &tq, &tk, d->sms, g_overlap, stream);
          }))) != QSA_OK)
         return st;
     SelectParams sel;

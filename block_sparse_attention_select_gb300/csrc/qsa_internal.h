@@ -180,12 +180,21 @@ struct AttendParams {
 // (once every CTA of that kernel has allowed it) and waits for that kernel's
 // completion itself before it touches global memory.  The first kernel of a
 // call is launched without it, so a call never overlaps the caller's work.
+// tile_shift: log2 of the key positions per work item (7: the scorers'
+// 128-position tiles; 8: the block scorer's 256-token tiles)
 int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t group_rows,
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
-                uint32_t *status, void *stream);
+                uint32_t *status, void *stream, int32_t tile_shift = 7);
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
                  int grid, bool overlap, void *stream);
+// Block scorer with the virtual rows on the TMEM lanes (BLOCKMAX): groups of
+// BR_ROWS rows of one head, tiles of 2 blocks (256 tokens); tmap_q3 is the
+// query map [rows][H][128] with boxes 64 x 1 x BR_ROWS, tmap_k the key map
+// [tokens][H][128] with boxes 64 x 1 x 128 (one page).
+constexpr int BR_ROWS = 128;
+int launch_score_blockrows(const ScoreParams &p, const void *tmap_q3, const void *tmap_k, int grid, bool overlap,
+                           void *stream);
 // cluster_pref (SEL_CAND only): CTAs per row of the candidate selector, 0 =
 // automatic (a thread-block cluster per row when rows are fewer than SMs, its
 // size from the device's occupancy query), 1 = one CTA per row, 2 / 4 / 8 =

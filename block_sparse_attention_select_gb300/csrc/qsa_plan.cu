@@ -49,7 +49,7 @@ struct OpAdd { __device__ int32_t operator()(int32_t a, int32_t b) const { retur
 
 __global__ void __launch_bounds__(PLAN_THREADS)
 plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row_visible,
-            int32_t R, int32_t G, int32_t num_reqs, int64_t max_len, int32_t sample_stride,
+            int32_t R, int32_t G, int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t tile_shift,
             int32_t *__restrict__ row_vis, Group *__restrict__ groups,
             int32_t *__restrict__ item_prefix, int32_t *__restrict__ sample_prefix,
             Plan *__restrict__ plan, uint32_t *status)
@@ -141,7 +141,7 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
         const int32_t g = base + tid;
         int32_t tiles = 0, stiles = 0;
         if (g < n_groups) {
-            tiles = ((g < PLAN_SMEM_GROUPS ? s_vmax[g] : groups[g].vmax) + TILE_M - 1) / TILE_M;
+            tiles = ((g < PLAN_SMEM_GROUPS ? s_vmax[g] : groups[g].vmax) + (1 << tile_shift) - 1) >> tile_shift;
             stiles = (tiles + sample_stride - 1) / sample_stride;
         }
         const int32_t it = block_incl_scan(tiles, wbuf, OpAdd(), 0);
@@ -172,11 +172,11 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
 int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, int32_t group_rows,
                 int32_t num_reqs, int64_t max_len, int32_t sample_stride, int32_t *row_vis,
                 Group *groups, int32_t *item_prefix, int32_t *sample_prefix, Plan *plan,
-                uint32_t *status, void *stream)
+                uint32_t *status, void *stream, int32_t tile_shift)
 {
     const int32_t G = group_rows;
     plan_kernel<<<1, PLAN_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(
-        row_req, row_visible, R, G, num_reqs, max_len, sample_stride, row_vis, groups,
+        row_req, row_visible, R, G, num_reqs, max_len, sample_stride, tile_shift, row_vis, groups,
         item_prefix, sample_prefix, plan, status);
     return static_cast<int>(cudaGetLastError());
 }

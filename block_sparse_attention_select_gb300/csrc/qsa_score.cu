@@ -722,6 +722,295 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *t
                          SMEM_BYTES, s, overlap, args);
 }
 
+// ---------------------------------------------------------------------------
+// Block scorer with the virtual rows on the TMEM lanes (BLOCKMAX).
+//
+// D[row, token] = Q_h K^T with M = 128 virtual rows of one head (A: the
+// group's queries, resident in shared memory), N = 256 tokens of two 128-token
+// pages (B: the tile's keys) and K = 128.  A block score is the maximum of a
+// row's dot products over the block's tokens, so each drain thread owns one
+// row and reduces its block's 128 accumulator columns in registers: no
+// exchange between warps.  8 drain warps: lane quarter w % 4, block w / 4 of
+// the tile.  Operand reads from shared memory: 4 KB of A and 8 KB of B per
+// 128 MMA cycles, as in the indexer's scorer.
+constexpr int BR_THREADS = 64 + 32 * 8;                  // TMA warp, MMA warp, 8 drain warps
+constexpr int BR_KST = 3;                                 // key stages of 64 KiB
+constexpr uint32_t BR_QHALF = BR_ROWS * 128;              // queries: one K half, 16 KiB
+constexpr uint32_t BR_KHALF = 2 * TILE_M * 128;           // keys: one K half of 256 tokens, 32 KiB
+constexpr uint32_t BR_STAGE = 2 * BR_KHALF;
+constexpr uint32_t BR_TILES = 2 * BR_QHALF + BR_KST * BR_STAGE;
+
+struct __align__(8) BrCtrl {
+    uint64_t full[BR_KST];
+    uint64_t empty[BR_KST];
+    uint64_t q_full;
+    uint64_t q_empty;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+constexpr uint32_t BR_SMEM = BR_TILES + sizeof(BrCtrl) + 1024;
+static_assert(BR_SMEM <= 232448, "shared memory budget");
+
+// The producer warp of the block scorer: per tile, pages 2t and 2t + 1 of the
+// group's (virtual) request, each as two boxes of [128 tokens][64 dims] (lane
+// i issues page i).  Like produce_tiles, it waits (bounded) for its own
+// copies before returning.
+__device__ __forceinline__ void produce_block_tiles(const ScoreParams &p, const CUtensorMap *tmap_q,
+                                                    const CUtensorMap *tmap_k, uint8_t *q_s, uint8_t *k_s,
+                                                    BrCtrl &c, const int32_t *prefix, int32_t n_groups,
+                                                    int32_t it0, int32_t it1, int lane, volatile int *abort,
+                                                    uint64_t lim)
+{
+    ItemCursor cur;
+    cur.init_warp(prefix, n_groups, it0, it1, 1, lane);
+    cur.settle();
+    int32_t cur_g = cur.g, q_loads = 1, stage = 0;
+    Group gr = p.groups[cur_g];
+    auto load_q = [&](const Group &g) {
+        const int32_t h = g.row0 / p.blk_rows, r0 = g.row0 - h * p.blk_rows;
+        mbar_arrive_expect_tx(&c.q_full, 2 * BR_QHALF);
+        tma_load_3d(q_s, tmap_q, &c.q_full, 0, h, r0);
+        tma_load_3d(q_s + BR_QHALF, tmap_q, &c.q_full, 64, h, r0);
+    };
+    if (lane == 0) load_q(gr);
+    uint32_t phase = 0, loaded = 0;
+    bool stop = false;
+    for (; cur.valid() && !stop; cur.next()) {
+        cur.settle();
+        if (cur.g != cur_g) {
+            cur_g = cur.g;
+            gr = p.groups[cur_g];
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(&c.q_empty, (q_loads - 1) & 1, abort, lim);
+                if (ok) load_q(gr);
+            }
+            if (__any_sync(0xffffffffu, !ok)) break;
+            ++q_loads;
+        }
+        const int32_t blk0 = cur.tile() * 2;
+        const int32_t nblk = min(2, (gr.vmax + TILE_M - 1) / TILE_M - blk0);
+        // page ids of the tile's blocks (before the stage wait: the round trip overlaps it)
+        int32_t pid = -1;
+        if (lane < nblk && gr.req >= 0)
+            pid = __ldg(p.block_table + static_cast<int64_t>(gr.req % p.blk_reqs) * p.max_pages + blk0 + lane);
+        if (__any_sync(0xffffffffu, !mbar_wait(&c.empty[stage], phase ^ 1u, abort, lim))) {
+            stop = true;
+            break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&c.full[stage], static_cast<uint32_t>(nblk) * 2u * TILE_M * 128u);
+        __syncwarp();
+        loaded = (loaded & ~(1u << (BR_KST + stage))) | (1u << stage) | (phase << (BR_KST + stage));
+        if (lane < nblk) {
+            const bool good = pid >= 0 && pid < p.num_pages;
+            if (!good) record_error(p.status, ST_BAD_PAGE);
+            const int32_t y = (good ? pid : p.num_pages) * TILE_M;      // past the end: TMA fills zeros
+            const int32_t h = gr.row0 / p.blk_rows;
+            uint8_t *dst = k_s + stage * BR_STAGE + lane * (TILE_M * 128);
+            tma_load_3d(dst, tmap_k, &c.full[stage], 0, h, y);
+            tma_load_3d(dst + BR_KHALF, tmap_k, &c.full[stage], 64, h, y);
+        }
+        if (++stage == BR_KST) { stage = 0; phase ^= 1u; }
+    }
+    if (lane == 0) {
+        mbar_wait_bounded(&c.q_full, (q_loads - 1) & 1, lim);
+        for (int s = 0; s < BR_KST; ++s)
+            if (loaded & (1u << s)) mbar_wait_bounded(&c.full[s], (loaded >> (BR_KST + s)) & 1u, lim);
+    }
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(BR_THREADS, 1)
+score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                       const ScoreParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t *q_s = smem;                        // [K half][128 rows][128 B]
+    uint8_t *k_s = smem + 2 * BR_QHALF;         // stages of [K half][256 tokens][128 B]
+    BrCtrl &c = *reinterpret_cast<BrCtrl *>(smem + BR_TILES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < BR_KST; ++s) {
+            mbar_init(&c.full[s], 1);
+            mbar_init(&c.empty[s], 1);
+        }
+        mbar_init(&c.q_full, 1);
+        mbar_init(&c.q_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&c.acc_full[b], 1);
+            mbar_init(&c.acc_empty[b], 8);
+        }
+        mbar_init(&c.drain, 1);
+        c.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) {
+        tmem_alloc(&c.tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmap_q);
+        tma_prefetch_desc(&tmap_k);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+    volatile int *abort = &c.abort;
+    const uint64_t lim = p.wait_limit_ns;
+    wait_prior_grid();
+
+    const int32_t n_items = p.plan->n_items;
+    const int32_t it0 = static_cast<int32_t>((static_cast<int64_t>(n_items) * blockIdx.x) / gridDim.x);
+    const int32_t it1 = static_cast<int32_t>((static_cast<int64_t>(n_items) * (blockIdx.x + 1)) / gridDim.x);
+    const int32_t n_groups = p.plan->n_groups;
+    const int32_t *prefix = p.item_prefix;
+
+    if (it0 >= it1) {
+        // no item for this CTA
+    } else if (warp == 0) {
+        produce_block_tiles(p, &tmap_q, &tmap_k, q_s, k_s, c, prefix, n_groups, it0, it1, lane, abort, lim);
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            ItemCursor cur;
+            cur.init(prefix, n_groups, it0, it1, 1);
+            constexpr uint32_t idesc = umma_idesc_f16_f32(BR_ROWS, 2 * TILE_M);
+            const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(q_s));
+            int32_t cur_g = -1, stage = 0, q_uses = 0;
+            uint32_t phase = 0, acc_cnt = 0;
+            bool have_q = false;
+            for (; cur.valid(); cur.next()) {
+                cur.settle();
+                if (cur.g != cur_g) {
+                    cur_g = cur.g;
+                    if (have_q) umma_commit(&c.q_empty);   // previous group's MMAs done -> queries free
+                    if (!mbar_wait(&c.q_full, q_uses & 1, abort, lim)) break;
+                    ++q_uses;
+                    have_q = true;
+                }
+                if (!mbar_wait(&c.full[stage], phase, abort, lim)) break;
+                const uint32_t b = acc_cnt & 1u;
+                if (!mbar_wait(&c.acc_empty[b], ((acc_cnt >> 1) & 1u) ^ 1u, abort, lim)) break;
+                tc_fence_after();
+                // descriptor of base + off = descriptor of base + off / 16 (the
+                // 14-bit start-address field cannot carry within shared memory)
+                const uint64_t k_desc0 = sw128_kmajor_desc(smem_u32(k_s + stage * BR_STAGE));
+#pragma unroll
+                for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
+                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
+                    umma_f16(tmem + b * 256u, q_desc0 + (((kk >> 2) * BR_QHALF + off) >> 4),
+                             k_desc0 + (((kk >> 2) * BR_KHALF + off) >> 4), idesc, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&c.empty[stage]);
+                umma_commit(&c.acc_full[b]);
+                if (++stage == BR_KST) { stage = 0; phase ^= 1u; }
+                ++acc_cnt;
+            }
+            umma_commit(&c.drain);
+            mbar_wait(&c.drain, 0, abort, lim);
+        }
+    } else {
+        // --------------------------------------------------- epilogue --
+        const int ew = warp - 2;
+        const int lq = warp & 3;                // TMEM lanes [32 lq, +32): virtual rows of the group
+        const int bt = ew >> 2;                 // block bt of each tile: columns [128 bt, +128)
+        const int32_t rig = lq * 32 + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(bt * TILE_M);
+        ItemCursor cur;
+        cur.init(prefix, n_groups, it0, it1, 1);
+        int32_t cur_g = -1;
+        uint32_t acc_cnt = 0;
+        bool mine = false;
+        int32_t vis = 0;                        // tokens the row sees
+        float *orow = nullptr;
+        for (; cur.valid(); cur.next()) {
+            cur.settle();
+            if (cur.g != cur_g) {
+                cur_g = cur.g;
+                const Group gr = p.groups[cur_g];
+                mine = rig < gr.nrows;
+                const int64_t v = static_cast<int64_t>(gr.row0) + rig;
+                vis = mine ? __ldg(p.row_vis + v) : 0;
+                orow = p.out + v * p.ld;
+            }
+            const uint32_t b = acc_cnt & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim))) break;
+            tc_fence_after();
+            const int32_t blk = cur.tile() * 2 + bt;        // the block this warp reduces
+            const int32_t tok0 = blk * TILE_M;
+            // the block's 128 columns, 32 at a time, three-operand maxima;
+            // tokens at or past the row's end are left out
+            float mx = -__int_as_float(0x7f800000);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t u[32];
+                tmem_ld_32x32b_x32(taddr + b * 256u + static_cast<uint32_t>(ch * 32), u);
+                tmem_ld_wait();
+                const int32_t lim_c = vis - (tok0 + ch * 32);   // columns of this chunk the row sees
+                if (lim_c >= 32) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float m3;
+                        asm("max.f32 %0, %1, %2, %3;" : "=f"(m3) : "f"(mx), "f"(__uint_as_float(u[i])),
+                            "f"(__uint_as_float(u[i + 1])));
+                        mx = m3;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (i < lim_c) mx = fmaxf(mx, __uint_as_float(u[i]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.acc_empty[b]);
+            if (mine && tok0 < vis) orow[blk] = mx;
+            ++acc_cnt;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    allow_next_grid();
+    if (c.abort && threadIdx.x == 0) record_error(p.status, ST_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+int launch_score_blockrows(const ScoreParams &p, const void *tmap_q3, const void *tmap_k, int grid, bool overlap,
+                           void *stream)
+{
+    static std::mutex mu;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return static_cast<int>(cudaErrorInvalidDevice);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!attr_done[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(score_blockrows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(BR_SMEM));
+            if (e != cudaSuccess) return static_cast<int>(e);
+            attr_done[dev] = true;
+        }
+    }
+    void *args[] = {const_cast<void *>(tmap_q3), const_cast<void *>(tmap_k), const_cast<ScoreParams *>(&p)};
+    return launch_kernel(reinterpret_cast<const void *>(&score_blockrows_kernel), dim3(grid), dim3(BR_THREADS),
+                         BR_SMEM, static_cast<cudaStream_t>(stream), overlap, args);
+}
+
+namespace {
 }  // namespace
 
 uint32_t score_smem_bytes() { return SMEM_BYTES; }
