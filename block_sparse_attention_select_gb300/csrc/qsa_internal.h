@@ -56,7 +56,7 @@ enum ScoreMode : int32_t {
     SCORE_LOGITS = 0,      // logits for j < V_r (and -inf up to the tile end when pad_inf)
     SCORE_SAMPLE = 1,      // sampled tiles only, into the sample matrix
     SCORE_FILTER = 2,      // append (score, j) with score >= tau_r to the candidate lists
-    SCORE_BLOCKMAX = 3,    // block scorer: per (row, head) the max over each 128-token block
+    SCORE_BLOCKMAX = 3,    // block scorer (its own kernel): per (row, head) the max over each 128-token block
 };
 
 struct ScoreParams {
@@ -88,10 +88,11 @@ struct ScoreParams {
     int32_t tiles_ld;           // key tiles per row in the candidate arrays (multiple of 8)
     uint32_t *status;
     uint64_t wait_limit_ns;
-    // BLOCKMAX (the M3-style block scorer): rows are virtual rows v = h * blk_rows
-    // + r, one per (query row r, KV head h); a group's req is the virtual
-    // request h * blk_reqs + b.  Queries are read through a 3-D map [H][rows][128]
-    // and keys through [tokens][H][128] (one 128-token page per tile).
+    // BLOCKMAX (the M3-style block scorer, score_blockrows_kernel): rows are
+    // virtual rows v = h * blk_rows + r, one per (query row r, KV head h); a
+    // group's req is the virtual request h * blk_reqs + b.  Queries are read
+    // through a 3-D map [rows][H][128] and keys through [tokens][H][128], two
+    // 128-token pages per tile.
     int32_t blk_heads;          // KV heads (0 outside BLOCKMAX)
     int32_t blk_reqs;           // requests of the block table
     int32_t blk_rows;           // query rows

@@ -11,6 +11,9 @@
 // per SM: warp 0 issues TMA, warp 1 issues MMAs, 16 epilogue warps drain TMEM
 // (double-buffered accumulators, 2 x 256 columns; each warp owns one lane
 // quarter x 64 columns) and write the results.
+//
+// The block scorer (per-head maximum over 128-token blocks) has its own
+// kernel at the end of this file, with the virtual rows on the TMEM lanes.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -37,7 +40,6 @@ struct __align__(8) Ctrl {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
-    uint64_t blk_bar[4];        // BLOCKMAX: the four quarter warps of a column block meet here
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -52,10 +54,7 @@ struct EpiRows {
 };
 
 static_assert(sizeof(Ctrl) % 16 == 0, "EpiRows must stay 16-byte aligned");
-// BLOCKMAX: per accumulator column, the running maximum (as an order-preserving
-// key) of the four lane-quarter warps
-constexpr uint32_t BLKMAX_BYTES = N_MAX * 4;
-constexpr uint32_t SMEM_BYTES = SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows) + BLKMAX_BYTES + 1024;
+constexpr uint32_t SMEM_BYTES = SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // Walks the same (group, tile) sequence in every role of a CTA.  The current
@@ -281,7 +280,7 @@ __device__ __forceinline__ void produce_tiles(const ScoreParams &p, const CUtens
                                               const CUtensorMap *tmap_k128, uint8_t *k_s, uint64_t *full,
                                               uint64_t *empty, uint64_t *q_full, uint64_t *q_empty,
                                               const int32_t *prefix, int32_t n_groups, int32_t it0, int32_t it1,
-                                              int32_t stride, int lane, bool blk, volatile int *abort, uint64_t lim,
+                                              int32_t stride, int lane, volatile int *abort, uint64_t lim,
                                               LoadQ load_q)
 {
     constexpr int PREFETCH = 8;
@@ -307,8 +306,7 @@ __device__ __forceinline__ void produce_tiles(const ScoreParams &p, const CUtens
         const int32_t nbox = (min(TILE_M, ga.vmax - pos0) + p.page_box - 1) >> p.page_box_shift;
         if (lane >= nbox || ga.req < 0) return -1;
         const int32_t pos = pos0 + lane * p.page_box;
-        const int32_t req = blk ? ga.req % p.blk_reqs : ga.req;   // virtual request -> block-table row
-        return __ldg(p.block_table + static_cast<int64_t>(req) * p.max_pages + (pos >> p.page_pos_shift));
+        return __ldg(p.block_table + static_cast<int64_t>(ga.req) * p.max_pages + (pos >> p.page_pos_shift));
     };
     int32_t ring[PREFETCH];
 #pragma unroll
@@ -360,14 +358,7 @@ __device__ __forceinline__ void produce_tiles(const ScoreParams &p, const CUtens
             const bool run = nbox * p.page_box == TILE_M &&
                              __all_sync(0xffffffffu, lane >= nbox || (good && y == y0 + lane * p.page_box));
             uint8_t *dst = k_s + stage * K_STAGE_BYTES;
-            if (blk) {
-                // one 128-token page of head h: two boxes of [128 tokens][64 dims]
-                if (lane == 0) {
-                    const int32_t h = gr.row0 / p.blk_rows;
-                    tma_load_3d(dst, tmap_k, &full[stage], 0, h, y);
-                    tma_load_3d(dst + K_HALF_BYTES, tmap_k, &full[stage], 64, h, y);
-                }
-            } else if (run) {
+            if (run) {
                 if (lane == 0) {
                     tma_load_2d(dst, tmap_k128, &full[stage], 0, y0);
                     tma_load_2d(dst + K_HALF_BYTES, tmap_k128, &full[stage], 64, y0);
@@ -389,88 +380,6 @@ __device__ __forceinline__ void produce_tiles(const ScoreParams &p, const CUtens
             if (loaded & (1u << s)) mbar_wait_bounded(&full[s], (loaded >> (KST + s)) & 1u, lim);
     }
     __syncwarp();
-}
-
-// The four quarter warps of a column block meet: lane 0 arrives, the warp
-// waits (bounded; false when the CTA aborted, and the caller then stops).
-__device__ __forceinline__ bool quarter_sync(uint64_t *bar, uint32_t &phase, volatile int *abort, uint64_t lim)
-{
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase, abort, lim);
-    phase ^= 1u;
-    return __all_sync(0xffffffffu, ok);
-}
-
-// BLOCKMAX drain (block scorer, one head per virtual row, 64 rows per warp):
-// the block score of row c is the maximum over the tile's 128 tokens (lanes of
-// the four quarter warps) of its dot products, tokens past the row's last one
-// excluded.  Each warp reduces its 32 lanes for 32 columns at once with a
-// transposing butterfly (31 shuffles per 32 columns: after the stage of width s
-// each lane keeps the half of its columns selected by its lane bit s, and
-// ends with column `lane`), folds the result into the shared per-column
-// maximum, and after the four quarter warps of the column block have met at a
-// column block's mbarrier, the quarter-0 warp writes the block scores and
-// clears the slots; a second meeting keeps the next tile's maxima out of the
-// slots until they are clear.  Returns false when a wait gave up (abort).
-template <bool FULL, bool ALLROWS>
-__device__ __forceinline__ bool epilogue_blockmax(const ScoreParams &p, EpiRows &e, uint32_t *bmax, const Group &gr,
-                                                  int32_t tile, uint32_t taddr, int cq, int quarter, int lane,
-                                                  int32_t nmine, uint64_t *bar, uint32_t &bphase,
-                                                  volatile int *abort, uint64_t lim)
-{
-    const int32_t j = tile * TILE_M + quarter * 32 + lane;      // this lane's token
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-        const int32_t c0 = ch * 32;
-        if (!ALLROWS && c0 >= nmine) break;                     // the same in all four quarter warps
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(cq * 64 + c0), raw);
-        tmem_ld_wait();
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            v[i] = __uint_as_float(raw[i]);
-            if (!FULL && j >= e.vis[c0 + i]) v[i] = -__int_as_float(0x7f800000);
-        }
-#pragma unroll
-        for (int sw = 16; sw >= 1; sw >>= 1) {
-            const bool up = (lane & sw) != 0;
-#pragma unroll
-            for (int i = 0; i < sw; ++i) {
-                const float send = up ? v[i] : v[i + sw];
-                const float keep = up ? v[i + sw] : v[i];
-                v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, sw));
-            }
-        }
-        atomicMax(bmax + cq * 64 + c0 + lane, score_key(v[0]));
-    }
-    if (!quarter_sync(bar, bphase, abort, lim)) return false;
-    if (quarter == 0) {
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-            const int32_t col = ch * 32 + lane;
-            uint32_t *slot = bmax + cq * 64 + col;
-            if (ALLROWS || col < nmine) {
-                const uint32_t key = *slot;
-                p.out[(static_cast<int64_t>(gr.row0) + cq * 64 + col) * p.ld + tile] = key_score(key);
-            }
-            *slot = 0u;
-        }
-    }
-    return quarter_sync(bar, bphase, abort, lim);
-}
-
-template <bool FULL>
-__device__ __forceinline__ bool epilogue_blockmax_tile(const ScoreParams &p, EpiRows &e, uint32_t *bmax,
-                                                       const Group &gr, int32_t tile, uint32_t taddr, int cq,
-                                                       int quarter, int lane, uint64_t *bar, uint32_t &bphase,
-                                                       volatile int *abort, uint64_t lim)
-{
-    const int32_t nmine = min(64, gr.nrows - cq * 64);
-    if (nmine == 64)
-        return epilogue_blockmax<FULL, true>(p, e, bmax, gr, tile, taddr, cq, quarter, lane, nmine, bar, bphase, abort, lim);
-    return epilogue_blockmax<FULL, false>(p, e, bmax, gr, tile, taddr, cq, quarter, lane, nmine, bar, bphase, abort, lim);
 }
 
 template <int H, int MODE>
@@ -503,12 +412,9 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
     uint8_t *k_s = smem + Q_BYTES;
     Ctrl &c = *reinterpret_cast<Ctrl *>(smem + SMEM_TILES);
     EpiRows *epi_rows = reinterpret_cast<EpiRows *>(smem + SMEM_TILES + sizeof(Ctrl));
-    uint32_t *bmax = reinterpret_cast<uint32_t *>(smem + SMEM_TILES + sizeof(Ctrl) + EPI_WARPS * sizeof(EpiRows));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const bool blk = p.mode == SCORE_BLOCKMAX;
-    for (int i = threadIdx.x; i < N_MAX; i += blockDim.x) bmax[i] = 0u;
 
     // prologue: barriers, TMEM and descriptor prefetch touch no global
     // memory, so they run while the previous kernel of the stream finishes
@@ -524,7 +430,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             mbar_init(&c.acc_empty[b], EPI_WARPS);
         }
         mbar_init(&c.drain, 1);
-        for (int b = 0; b < 4; ++b) mbar_init(&c.blk_bar[b], 4);
         c.abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -558,21 +463,14 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         // no item for this CTA: straight to the teardown
     } else if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        // the group's queries: rows row0 .. of [rows * H, 128], or for the
-        // block scorer rows r0 .. of head h through the 3-D map
+        // the group's queries: rows row0 .. of [rows * H, 128]
         auto load_q = [&](const Group &g) {
             mbar_arrive_expect_tx(&c.q_full, Q_BYTES);
-            if (blk) {
-                const int32_t h = g.row0 / p.blk_rows, r0 = g.row0 - h * p.blk_rows;
-                tma_load_3d(q_s, &tmap_q, &c.q_full, 0, h, r0);
-                tma_load_3d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, h, r0);
-            } else {
-                tma_load_2d(q_s, &tmap_q, &c.q_full, 0, g.row0 * H);
-                tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, g.row0 * H);
-            }
+            tma_load_2d(q_s, &tmap_q, &c.q_full, 0, g.row0 * H);
+            tma_load_2d(q_s + Q_HALF_BYTES, &tmap_q, &c.q_full, 64, g.row0 * H);
         };
         produce_tiles<KSTAGES>(p, &tmap_k, &tmap_k128, k_s, c.full, c.empty, &c.q_full, &c.q_empty, prefix,
-                               n_groups, it0, it1, stride, lane, blk, abort, lim, load_q);
+                               n_groups, it0, it1, stride, lane, abort, lim, load_q);
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
@@ -635,8 +533,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
         cur.init(prefix, n_groups, it0, it1, stride);
         int32_t cur_g = -1;
         uint32_t acc_cnt = 0;
-        uint32_t bphase = 0;                    // BLOCKMAX: phase of this column block's meeting barrier
-        bool blk_ok = true;
         Group gr{};
         for (; cur.valid(); cur.next()) {
             cur.settle();
@@ -647,7 +543,7 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 const int32_t first = cq * RPW;
                 const int32_t nmine = max(0, min(RPW, gr.nrows - first));
                 __syncwarp();
-                for (int32_t i = lane; i < (blk ? 0 : RPW * H); i += 32) {
+                for (int32_t i = lane; i < RPW * H; i += 32) {
                     const int32_t rr = i / H, h = i % H;          // rows past the group weigh 0
                     er.w[(rr >> 1) * 2 * H + 2 * h + (rr & 1)] =
                         rr < nmine ? __ldg(p.w + static_cast<int64_t>(gr.row0 + first + rr) * H + h) : 0.0f;
@@ -664,19 +560,12 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
                 ++acc_cnt;
                 continue;
             }
-            if (!mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim)) break;
+            // (every lane gives up together: the TMEM loads are warp-wide)
+            if (!__all_sync(0xffffffffu, mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim))) break;
             tc_fence_after();
             const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + b * 256u;
             const int32_t t = cur.tile();
             switch (p.mode) {
-            case SCORE_BLOCKMAX:
-                if constexpr (H == 1) {
-                    const bool ok = (t + 1) * TILE_M <= gr.vmin
-                        ? epilogue_blockmax_tile<true>(p, er, bmax, gr, t, taddr, cq, quarter, lane, &c.blk_bar[cq], bphase, abort, lim)
-                        : epilogue_blockmax_tile<false>(p, er, bmax, gr, t, taddr, cq, quarter, lane, &c.blk_bar[cq], bphase, abort, lim);
-                    blk_ok = ok;
-                }
-                break;
             case SCORE_FILTER: epilogue_tile<H, SCORE_FILTER>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
             case SCORE_SAMPLE: epilogue_tile<H, SCORE_SAMPLE>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
             default: epilogue_tile<H, SCORE_LOGITS>(p, er, gr, t, taddr, cq, quarter, lane, lt_mask); break;
@@ -685,7 +574,6 @@ score_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(&c.acc_empty[b]);
             ++acc_cnt;
-            if (!blk_ok) break;                 // a quarter meeting gave up: the CTA is aborting
         }
     }
 
