@@ -808,7 +808,7 @@ def run_blocks(args, ws, rank, local):
     torch.cuda.synchronize()
     kt = qsa.kernel_times()
     qsa.set_config(qsa.QSA_CFG_KERNEL_TIMING, 0)
-    score_ms = kt.get("score_logits", (ms * n_kt, n_kt))[0] / n_kt
+    score_ms = kt.get("score_blocks", (ms * n_kt, n_kt))[0] / n_kt
     achieved = flops / (score_ms / 1e3) / 1e12
     e2e = None
     if not args.no_e2e:
@@ -844,7 +844,7 @@ def run_blocks(args, ws, rank, local):
                    "block_tokens": 128, "visible_tokens": tokens, "l2": "flushed between steps (512 MiB write)",
                    "accumulate": "f32", "median_ms": statistics.median(step_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "score_blockmax",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "score_blockrows",
                      "kernel_ms": score_ms, "gflop": flops / 1e9, "peak_source": peaks["source"]},
         "kernels_ms_per_step": {k: v[0] / n_kt for k, v in kt.items()},
         "cpu_baseline": cpu,

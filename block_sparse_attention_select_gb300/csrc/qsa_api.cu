@@ -43,8 +43,8 @@ std::atomic<int> g_cluster{0};              // candidate selector CTAs per row (
 thread_local int32_t g_launches = 0;
 
 // Optional per-launch CUDA-event timing (test / benchmark instrument).
-enum Kind { K_PLAN = 0, K_SCORE_LOGITS, K_SCORE_SAMPLE, K_SCORE_FILTER, K_SCORE_FALLBACK,
-            K_SEL_DENSE, K_SEL_THRESH, K_SEL_CAND, K_SEL_FLAGGED, K_PAD, K_KINDS };
+enum Kind { K_PLAN = 0, K_SCORE_LOGITS, K_SCORE_SAMPLE, K_SCORE_FILTER, K_SCORE_BLOCKS,
+            K_SEL_DENSE, K_SEL_THRESH, K_SEL_CAND, K_SEL_UNUSED, K_PAD, K_KINDS };
 struct Pending { cudaEvent_t a, b; int kind; };
 std::atomic<bool> g_timing{false};
 std::vector<Pending> g_pending;
@@ -839,7 +839,7 @@ qsa_status qsa_block_select(const void *q, int32_t rows, int32_t H, const void *
     sp.blk_heads = H;
     sp.blk_reqs = num_reqs;
     sp.blk_rows = rows;
-    if ((st = launch_rc(timed(K_SCORE_LOGITS, stream, [&] {
+    if ((st = launch_rc(timed(K_SCORE_BLOCKS, stream, [&] {
              return launch_score_blockrows(sp, &tq, &tk, d->sms, g_overlap, stream);
          }))) != QSA_OK)
         return st;

@@ -827,7 +827,10 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 const Group gr = p.groups[cur_g];
                 mine = rig < gr.nrows;
                 const int64_t v = static_cast<int64_t>(gr.row0) + rig;
-                vis = mine ? __ldg(p.row_vis + v) : 0;
+                // a lane past the group's rows takes the unmasked path: its
+                // maximum is never stored, and a masked pass over all 128
+                // columns would hold up the whole warp
+                vis = mine ? __ldg(p.row_vis + v) : INT32_MAX;
                 orow = p.out + v * p.ld;
             }
             const uint32_t b = acc_cnt & 1u;
@@ -852,7 +855,7 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                             "f"(__uint_as_float(u[i + 1])));
                         mx = m3;
                     }
-                } else {
+                } else if (lim_c > 0) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (i < lim_c) mx = fmaxf(mx, __uint_as_float(u[i]));

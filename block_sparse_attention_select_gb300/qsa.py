@@ -36,7 +36,7 @@ QSA_CFG_WAIT_LIMIT_NS = 2
 QSA_CFG_KERNEL_TIMING = 3
 QSA_CFG_OVERLAP = 4
 QSA_CFG_CLUSTER = 5
-KERNEL_KINDS = ["plan", "score_logits", "score_sample", "score_filter", "unused4",
+KERNEL_KINDS = ["plan", "score_logits", "score_sample", "score_filter", "score_blocks",
                 "select_dense", "select_thresh", "select_cand", "unused8", "pad"]
 PATH_AUTO, PATH_DENSE, PATH_FILTER = 0, 1, 2
 

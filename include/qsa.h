@@ -258,9 +258,9 @@ int32_t qsa_last_cluster_size(void);
 /* Kernel kinds reported by qsa_kernel_times(). */
 #define QSA_KERNEL_KINDS 10
 /* 0 plan, 1 score (logits), 2 score (sampled tiles), 3 score (threshold filter),
- * 4 and 8 reserved (not launched), 5 select (dense rows), 6 select
+ * 4 score (block maxima, qsa_block_select), 5 select (dense rows), 6 select
  * (threshold), 7 select (candidates, including rows re-scored in place),
- * 9 -inf padding. */
+ * 8 reserved (not launched), 9 -inf padding. */
 
 /* With QSA_CFG_KERNEL_TIMING on: synchronises the pending events, adds each
  * launch's elapsed time to ms[kind] and its count to launches[kind] for the
