@@ -190,10 +190,11 @@ int launch_plan(const int32_t *row_req, const int32_t *row_visible, int32_t R, i
 int launch_score(const ScoreParams &p, const void *tmap_q, const void *tmap_k, const void *tmap_k128,
                  int grid, bool overlap, void *stream);
 // Block scorer with the virtual rows on the TMEM lanes (BLOCKMAX): groups of
-// BR_ROWS rows of one head, tiles of 2 blocks (256 tokens); tmap_q3 is the
-// query map [rows][H][128] with boxes 64 x 1 x BR_ROWS, tmap_k the key map
-// [tokens][H][128] with boxes 64 x 1 x 128 (one page).
-constexpr int BR_ROWS = 128;
+// up to BR_ROWS rows of one head (two MMA halves of 128 rows), tiles of 2
+// blocks (256 tokens); tmap_q3 is the query map [rows][H][128] with boxes
+// 64 x 1 x BR_ROWS, tmap_k the key map [tokens][H][128] with boxes 64 x 1 x 128
+// (one page).
+constexpr int BR_ROWS = 256;
 int launch_score_blockrows(const ScoreParams &p, const void *tmap_q3, const void *tmap_k, int grid, bool overlap,
                            void *stream);
 // cluster_pref (SEL_CAND only): CTAs per row of the candidate selector, 0 =

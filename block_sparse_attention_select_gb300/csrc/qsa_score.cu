@@ -613,27 +613,31 @@ int launch_h(const ScoreParams &p, const void *tq, const void *tk, const void *t
 // ---------------------------------------------------------------------------
 // Block scorer with the virtual rows on the TMEM lanes (BLOCKMAX).
 //
-// D[row, token] = Q_h K^T with M = 128 virtual rows of one head (A: the
-// group's queries, resident in shared memory), N = 256 tokens of two 128-token
-// pages (B: the tile's keys) and K = 128.  A block score is the maximum of a
-// row's dot products over the block's tokens, so each drain thread owns one
-// row and reduces its block's 128 accumulator columns in registers: no
-// exchange between warps.  8 drain warps: lane quarter w % 4, block w / 4 of
-// the tile.  Operand reads from shared memory: 4 KB of A and 8 KB of B per
-// 128 MMA cycles, as in the indexer's scorer.
-constexpr int BR_THREADS = 64 + 32 * 8;                  // TMA warp, MMA warp, 8 drain warps
-constexpr int BR_KST = 3;                                 // key stages of 64 KiB
-constexpr uint32_t BR_QHALF = BR_ROWS * 128;              // queries: one K half, 16 KiB
+// D[row, token] = Q_h K^T for a group of up to 256 virtual rows of one head
+// (the queries, resident in shared memory) against a tile of N = 256 tokens of
+// two 128-token pages (the keys), K = 128.  The group is split into two halves
+// of 128 rows; each half is one M = 128 MMA into its own 256-column TMEM
+// accumulator, so one key tile (64 KB) feeds 2 x 8.4 MFLOP, half the key bytes
+// per FLOP of a 128-row group.  A block score is the maximum of a row's dot
+// products over the block's tokens, so each drain thread owns one row and
+// reduces its block's 128 accumulator columns in registers: no exchange
+// between warps.  16 drain warps: half w / 8, lane quarter w % 4, block
+// (w / 4) % 2 of the tile; half 1 drains while half 0's next MMA runs.
+constexpr int BR_M = 128;                                 // rows per MMA: one half of a group
+constexpr int BR_THREADS = 64 + 32 * 16;                  // TMA warp, MMA warp, 2 x 8 drain warps
+constexpr int BR_KST = 2;                                 // key stages of 64 KiB
+constexpr uint32_t BR_QHALF = BR_ROWS * 128;              // queries: one K half of 256 rows, 32 KiB
 constexpr uint32_t BR_KHALF = 2 * TILE_M * 128;           // keys: one K half of 256 tokens, 32 KiB
 constexpr uint32_t BR_STAGE = 2 * BR_KHALF;
 constexpr uint32_t BR_TILES = 2 * BR_QHALF + BR_KST * BR_STAGE;
+static_assert(BR_ROWS == 2 * BR_M, "a group is two MMA halves");
 
 struct __align__(8) BrCtrl {
     uint64_t full[BR_KST];
     uint64_t empty[BR_KST];
     uint64_t q_full;
     uint64_t q_empty;
-    uint64_t acc_full[2];
+    uint64_t acc_full[2];       // per half
     uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
@@ -718,7 +722,7 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint8_t *q_s = smem;                        // [K half][128 rows][128 B]
+    uint8_t *q_s = smem;                        // [K half][256 rows][128 B]
     uint8_t *k_s = smem + 2 * BR_QHALF;         // stages of [K half][256 tokens][128 B]
     BrCtrl &c = *reinterpret_cast<BrCtrl *>(smem + BR_TILES);
     const int warp = threadIdx.x >> 5;
@@ -771,37 +775,42 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
         if (lane == 0) {
             ItemCursor cur;
             cur.init(prefix, n_groups, it0, it1, 1);
-            constexpr uint32_t idesc = umma_idesc_f16_f32(BR_ROWS, 2 * TILE_M);
+            constexpr uint32_t idesc = umma_idesc_f16_f32(BR_M, 2 * TILE_M);
             const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(q_s));
-            int32_t cur_g = -1, stage = 0, q_uses = 0;
-            uint32_t phase = 0, acc_cnt = 0;
+            int32_t cur_g = -1, stage = 0, q_uses = 0, halves = 1;
+            uint32_t phase = 0, uses[2] = {0, 0};
             bool have_q = false;
             for (; cur.valid(); cur.next()) {
                 cur.settle();
                 if (cur.g != cur_g) {
                     cur_g = cur.g;
+                    halves = p.groups[cur_g].nrows > BR_M ? 2 : 1;
                     if (have_q) umma_commit(&c.q_empty);   // previous group's MMAs done -> queries free
                     if (!mbar_wait(&c.q_full, q_uses & 1, abort, lim)) break;
                     ++q_uses;
                     have_q = true;
                 }
                 if (!mbar_wait(&c.full[stage], phase, abort, lim)) break;
-                const uint32_t b = acc_cnt & 1u;
-                if (!mbar_wait(&c.acc_empty[b], ((acc_cnt >> 1) & 1u) ^ 1u, abort, lim)) break;
-                tc_fence_after();
                 // descriptor of base + off = descriptor of base + off / 16 (the
                 // 14-bit start-address field cannot carry within shared memory)
                 const uint64_t k_desc0 = sw128_kmajor_desc(smem_u32(k_s + stage * BR_STAGE));
+                bool ok = true;
+                for (int hf = 0; hf < halves; ++hf) {
+                    if (!mbar_wait(&c.acc_empty[hf], (uses[hf] & 1u) ^ 1u, abort, lim)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
-                    const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
-                    umma_f16(tmem + b * 256u, q_desc0 + (((kk >> 2) * BR_QHALF + off) >> 4),
-                             k_desc0 + (((kk >> 2) * BR_KHALF + off) >> 4), idesc, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
+                        const uint32_t off = static_cast<uint32_t>((kk & 3) * 32);
+                        umma_f16(tmem + static_cast<uint32_t>(hf) * 256u,
+                                 q_desc0 + (((kk >> 2) * BR_QHALF + static_cast<uint32_t>(hf) * BR_M * 128u + off) >> 4),
+                                 k_desc0 + (((kk >> 2) * BR_KHALF + off) >> 4), idesc, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&c.acc_full[hf]);
+                    ++uses[hf];
                 }
+                if (!ok) break;
                 umma_commit(&c.empty[stage]);
-                umma_commit(&c.acc_full[b]);
                 if (++stage == BR_KST) { stage = 0; phase ^= 1u; }
-                ++acc_cnt;
             }
             umma_commit(&c.drain);
             mbar_wait(&c.drain, 0, abort, lim);
@@ -809,14 +818,17 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
     } else {
         // --------------------------------------------------- epilogue --
         const int ew = warp - 2;
-        const int lq = warp & 3;                // TMEM lanes [32 lq, +32): virtual rows of the group
-        const int bt = ew >> 2;                 // block bt of each tile: columns [128 bt, +128)
-        const int32_t rig = lq * 32 + lane;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(bt * TILE_M);
+        const int hf = ew >> 3;                 // half of the group: accumulator columns [256 hf, +256)
+        const int lq = warp & 3;                // TMEM lanes [32 lq, +32): virtual rows of the half
+        const int bt = (ew >> 2) & 1;           // block bt of each tile: columns [128 bt, +128)
+        const int32_t rig = hf * BR_M + lq * 32 + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) +
+                               static_cast<uint32_t>(hf * 256 + bt * TILE_M);
         ItemCursor cur;
         cur.init(prefix, n_groups, it0, it1, 1);
         int32_t cur_g = -1;
-        uint32_t acc_cnt = 0;
+        uint32_t uses = 0;
+        bool active = false;                    // the group has rows in this half
         bool mine = false;
         int32_t vis = 0;                        // tokens the row sees
         float *orow = nullptr;
@@ -825,6 +837,7 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
             if (cur.g != cur_g) {
                 cur_g = cur.g;
                 const Group gr = p.groups[cur_g];
+                active = gr.nrows > hf * BR_M;
                 mine = rig < gr.nrows;
                 const int64_t v = static_cast<int64_t>(gr.row0) + rig;
                 // a lane past the group's rows takes the unmasked path: its
@@ -833,8 +846,8 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 vis = mine ? __ldg(p.row_vis + v) : INT32_MAX;
                 orow = p.out + v * p.ld;
             }
-            const uint32_t b = acc_cnt & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(&c.acc_full[b], (acc_cnt >> 1) & 1u, abort, lim))) break;
+            if (!active) continue;              // no MMA for this half either
+            if (!__all_sync(0xffffffffu, mbar_wait(&c.acc_full[hf], uses & 1u, abort, lim))) break;
             tc_fence_after();
             const int32_t blk = cur.tile() * 2 + bt;        // the block this warp reduces
             const int32_t tok0 = blk * TILE_M;
@@ -844,7 +857,7 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t u[32];
-                tmem_ld_32x32b_x32(taddr + b * 256u + static_cast<uint32_t>(ch * 32), u);
+                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(ch * 32), u);
                 tmem_ld_wait();
                 const int32_t lim_c = vis - (tok0 + ch * 32);   // columns of this chunk the row sees
                 if (lim_c >= 32) {
@@ -863,9 +876,9 @@ score_blockrows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c.acc_empty[b]);
+            if (lane == 0) mbar_arrive(&c.acc_empty[hf]);
             if (mine && tok0 < vis) orow[blk] = mx;
-            ++acc_cnt;
+            ++uses;
         }
     }
 
