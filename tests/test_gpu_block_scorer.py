@@ -68,8 +68,15 @@ def test_block_scorer_against_oracle(case):
         np.testing.assert_array_equal(gi, oi)
         np.testing.assert_array_equal(gv, ov.astype(np.float32))
         return
-    R, H, _ = gi.shape
-    for r in range(R):
+    _check_gauss(inp, gi, gv, oi, range(gi.shape[0]), k)
+
+
+def _check_gauss(inp, gi, gv, oi, rows, k):
+    """Rows `rows` of the GPU result (gi, gv: [R, H, k]) against the oracle's
+    selection oi ([len(rows), H, k]): values within tolerance of the oracle's
+    block scores, sets equal up to near-ties of the cut."""
+    H = gi.shape[1]
+    for j, r in enumerate(rows):
         for h in range(H):
             sc = _oracle_scores(inp, r, h)
             n = min(k, len(sc))
@@ -79,9 +86,47 @@ def test_block_scorer_against_oracle(case):
             o = sc[sel]
             assert np.all(np.abs(gv[r, h, :n] - o) <= RTOL * np.abs(o) + ATOL), (r, h)
             assert np.all(np.diff(gv[r, h, :n].astype(np.float64)) <= 0)
-            kth = sc[oi[r, h, n - 1]]
-            for c in set(sel.tolist()) ^ set(oi[r, h, :n].tolist()):
+            kth = sc[oi[j, h, n - 1]]
+            for c in set(sel.tolist()) ^ set(oi[j, h, :n].tolist()):
                 assert abs(sc[c] - kth) <= RTOL * abs(kth) + ATOL, (r, h, c)
+
+
+def test_block_scorer_group_half_boundaries():
+    # A group holds up to 256 rows of one request and head as two MMA halves of
+    # 128: requests of 128 rows (one half), 129 (a second half of one row) and
+    # 257 (a full group, then a group of one row).
+    inp = W.make_block_scorer_inputs("halves", seed=11, ctx_tokens=[1500, 1400, 2600], rows_per_req=[129, 128, 257],
+                                     k=10, heads=2, dist="int")
+    gi, gv = _run(inp)
+    oi, ov = BS.select_blocks(inp.q, inp.k_cache, inp.block_table, inp.row_req, inp.row_token, inp.k)
+    assert qsa.get_device_status() == qsa.QSA_OK
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov.astype(np.float32))
+
+
+@pytest.mark.parametrize("dist", ["int", "gauss"])
+def test_block_scorer_full_size(dist):
+    # The benchmarked shape (1,616 rows at the end of a 184,320-token context,
+    # 2 KV heads, top 16 of 1,440 blocks): every row checked for k distinct
+    # visible blocks in non-increasing score order; sampled rows, among them
+    # both sides of a half and of a group boundary and the last, 80-row group,
+    # against the oracle.
+    inp = W.make_block_scorer_inputs(f"blocks_full_{dist}", seed=41, ctx_tokens=[184_320], rows_per_req=[1616],
+                                     k=16, heads=2, dist=dist)
+    gi, gv = _run(inp)
+    assert qsa.get_device_status() == qsa.QSA_OK
+    R, H, k = gi.shape
+    nvis = (inp.row_token.astype(np.int64) // 128 + 1)[:, None, None]
+    assert np.all(gi >= 0) and np.all(gi < nvis)
+    assert np.all(np.diff(np.sort(gi, axis=2), axis=2) > 0)
+    assert np.all(np.diff(gv.astype(np.float64), axis=2) <= 0)
+    rows = sorted(set(np.linspace(0, R - 1, 10).astype(int).tolist()) | {127, 128, 255, 256, 767, 768, 1535, 1536, 1600})
+    oi, ov = BS.select_blocks(inp.q[rows], inp.k_cache, inp.block_table, inp.row_req[rows], inp.row_token[rows], k)
+    if dist == "int":
+        np.testing.assert_array_equal(gi[rows], oi)
+        np.testing.assert_array_equal(gv[rows], ov.astype(np.float32))
+    else:
+        _check_gauss(inp, gi, gv, oi, rows, k)
 
 
 def test_block_scorer_k_above_visible_blocks_and_ties():
