@@ -135,37 +135,46 @@ __device__ uint32_t kth_largest(SelShared &sh, int32_t n, uint32_t k_rem, uint32
     return lo;
 }
 
-// In-place descending sort of a[0, m) by one warp: bitonic network in the
-// variant whose comparators all point the same way, so positions >= m act as
-// -infinity padding and are never touched.
-__device__ void warp_sort_desc(uint64_t *a, int32_t m)
+// In-place descending sort of a[0, m) by NTHR threads (thread index tid):
+// bitonic network in the variant whose comparators all point the same way, so
+// positions >= m act as -infinity padding and are never touched.  Every block
+// and stride is a power of two, so comparator indices are shifts and masks.
+// BLOCK: the whole CTA sorts (barriers between stages), else one warp.
+template <int NTHR, bool BLOCK>
+__device__ __forceinline__ void bitonic_sort_desc(uint64_t *a, int32_t m, int tid)
 {
-    const int lane = threadIdx.x & 31;
-    int32_t M = 1;
-    while (M < m) M <<= 1;
-    for (int32_t size = 2; size <= M; size <<= 1) {
-        const int32_t half = size >> 1;
-        for (int32_t i = lane; i < (M >> 1); i += 32) {
-            const int32_t blk = i / half, off = i % half;
-            const int32_t x = blk * size + off, y = blk * size + size - 1 - off;
+    int lm = 0;
+    while ((1 << lm) < m) ++lm;
+    const int32_t npairs = (1 << lm) >> 1;
+    auto sync = [] {
+        if constexpr (BLOCK) __syncthreads();
+        else __syncwarp();
+    };
+    for (int ls = 1; ls <= lm; ++ls) {                    // merge blocks of 2^ls
+        const int lh = ls - 1;
+        for (int32_t i = tid; i < npairs; i += NTHR) {
+            const int32_t blk = i >> lh, off = i & ((1 << lh) - 1);
+            const int32_t x = (blk << ls) + off, y = (blk << ls) + (1 << ls) - 1 - off;
             if (y < m) {
                 const uint64_t u = a[x], v = a[y];
                 if (u < v) { a[x] = v; a[y] = u; }
             }
         }
-        __syncwarp();
-        for (int32_t stride = half >> 1; stride > 0; stride >>= 1) {
-            for (int32_t i = lane; i < (M >> 1); i += 32) {
-                const int32_t x = 2 * stride * (i / stride) + (i % stride), y = x + stride;
+        sync();
+        for (int lst = lh - 1; lst >= 0; --lst) {          // stride 2^lst
+            for (int32_t i = tid; i < npairs; i += NTHR) {
+                const int32_t x = ((i >> lst) << (lst + 1)) + (i & ((1 << lst) - 1)), y = x + (1 << lst);
                 if (y < m) {
                     const uint64_t u = a[x], v = a[y];
                     if (u < v) { a[x] = v; a[y] = u; }
                 }
             }
-            __syncwarp();
+            sync();
         }
     }
 }
+
+__device__ void warp_sort_desc(uint64_t *a, int32_t m) { bitonic_sort_desc<32, false>(a, m, threadIdx.x & 31); }
 
 // bstart[b] = elements in buckets before b (bucket 0 holds the largest keys);
 // hist[] becomes the scatter cursors.
@@ -762,6 +771,7 @@ warp_topk_kernel(const SelectParams p)
 constexpr int CT = 256;               // threads per row
 static_assert(CT == NT, "the in-kernel fallback runs the dense selection with the same block");
 constexpr int BIG_MAX = 320;          // > (QSA_MAX_K + SLACK) / (RANK_MAX + 1)
+constexpr uint32_t BLOCK_SORT_MIN = 128;   // larger buckets are sorted by the whole CTA
 constexpr int QPR = 8;                // quarters per thread whose mask words are loaded together
 
 struct CandShared {
@@ -1063,9 +1073,25 @@ cand_kernel(const SelectParams p)
             }
         }
         __syncthreads();
-        for (uint32_t q = wid; q < sh.nbig; q += CT / 32) {
+        // buckets too large for rank counting: those above BLOCK_SORT_MIN (a
+        // tie bucket at the cut, typically one) by the whole CTA in turn, the
+        // others by one warp each
+        const uint32_t nbig = sh.nbig;
+        for (uint32_t q = 0; q < nbig; ++q) {                      // uniform
             const uint32_t b = sh.big[q];
             const uint32_t s0 = b ? sh.hist[b - 1] : 0u, m = sh.hist[b] - s0;
+            if (m <= BLOCK_SORT_MIN) continue;
+            bitonic_sort_desc<CT, true>(bq + s0, static_cast<int32_t>(m), t);
+            for (uint32_t i = t; i < m && s0 + i < kk; i += CT) {
+                const uint64_t x = bq[s0 + i];
+                oi[s0 + i] = static_cast<int32_t>(~static_cast<uint32_t>(x));
+                if (ov) ov[s0 + i] = key_score(static_cast<uint32_t>(x >> 32));
+            }
+        }
+        for (uint32_t q = wid; q < nbig; q += CT / 32) {
+            const uint32_t b = sh.big[q];
+            const uint32_t s0 = b ? sh.hist[b - 1] : 0u, m = sh.hist[b] - s0;
+            if (m > BLOCK_SORT_MIN) continue;
             warp_sort_desc(bq + s0, static_cast<int32_t>(m));
             for (uint32_t i = lane; i < m && s0 + i < kk; i += 32) {
                 const uint64_t x = bq[s0 + i];
