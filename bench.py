@@ -384,16 +384,7 @@ def run_ours(args, ws, rank, local):
     t_flop = alg["flops"] / (peaks["bf16_tflops"] * 1e12)
     t_mem = alg["bytes"] / (peaks["hbm_gbs"] * 1e9)
     t_roof = max(t_flop, t_mem)
-    roof_traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            tr = json.load(open(tr_path))
-            ent = tr.get(wl.name, {}).get(dom_name)
-            if ent and ent.get("kernel_rev") == kernel_revision(dom_name):
-                roof_traffic = ent["bytes_per_launch"]
-        except Exception:
-            roof_traffic = None
+    roof_traffic = recorded_traffic(wl.name, dom_name)
 
     # end to end through the public API: host inputs in, host result out
     e2e = None
@@ -437,7 +428,24 @@ KERNEL_SOURCES = {
     "score": ("qsa_score.cu", "qsa_device.cuh", "qsa_internal.h"),
     "select": ("qsa_select.cu", "qsa_device.cuh", "qsa_internal.h"),
     "produce": ("qsa_produce.cu", "qsa_device.cuh", "qsa_internal.h"),
+    "attend": ("qsa_attend.cu", "qsa_device.cuh", "qsa_internal.h"),
 }
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the ncu record in
+    profiles/traffic.json, or None when there is none or the kernel's sources
+    have changed since it was taken."""
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tr_path):
+        return None
+    try:
+        ent = json.load(open(tr_path)).get(workload, {}).get(kernel)
+    except Exception:
+        return None
+    if ent and ent.get("kernel_rev") == kernel_revision(kernel):
+        return ent["bytes_per_launch"]
+    return None
 
 
 def kernel_revision(kernel: str) -> str:
@@ -619,15 +627,7 @@ def run_produce(args, ws, rank, local):
         el = time.perf_counter() - t
         cpu = {"value": len(done) / el, "unit": "keys/s", "cores": 1, "kind": "oracle",
                "sample": f"all {len(done)} keys of {inp.name} (numpy float64, one thread), {el:.1f} s"}
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            ent = json.load(open(tr_path)).get(f"{inp.name}_w{inp.window}", {}).get("produce")
-            if ent and ent.get("kernel_rev") == kernel_revision("produce"):
-                traffic = ent["bytes_per_launch"]
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic(f"{inp.name}_w{inp.window}", "produce")
     line = {
         "metric": PRODUCE_METRIC, "value": nkeys * ws / (ms / 1e3), "unit": "keys/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -729,7 +729,7 @@ def run_attend(args, ws, rank, local):
         # the gathered K / V lines (~12 FLOP per byte, each row reading its own
         # tokens from a cache larger than L2) give the memory-side bound beside it
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "attend", "kernel_ms": ms,
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": recorded_traffic(inp.name, "attend"), "kernel": "attend", "kernel_ms": ms,
                      "gathered_gb_per_s": gathered / (ms / 1e3) / 1e9, "peak_source": peaks["source"]},
         "gather_bound": {"bytes": gathered, "t_hbm_ms": gathered / (peaks["hbm_gbs"] * 1e9) * 1e3,
                          "t_tensor_ms": flops / (peaks["bf16_tflops"] * 1e12) * 1e3,
@@ -844,7 +844,7 @@ def run_blocks(args, ws, rank, local):
                    "block_tokens": 128, "visible_tokens": tokens, "l2": "flushed between steps (512 MiB write)",
                    "accumulate": "f32", "median_ms": statistics.median(step_ms)},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "kernel": "score_blockrows",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": recorded_traffic(inp.name, "score_blocks"), "kernel": "score_blockrows",
                      "kernel_ms": score_ms, "gflop": flops / 1e9, "peak_source": peaks["source"]},
         "kernels_ms_per_step": {k: v[0] / n_kt for k, v in kt.items()},
         "cpu_baseline": cpu,
