@@ -185,3 +185,33 @@ def test_misaligned_arrays_are_rejected_on_the_host(lib):
     for bt, rr, rt, sel in ((18, 16, 16, 16), (16, 18, 16, 16), (16, 16, 18, 16), (16, 16, 16, 18)):
         assert a(vp(16), 2, 24, vp(16), vp(16), 4, 64, 2, 256, vp(bt), 1, 4, vp(rr), vp(rt), vp(sel), 16,
                  0.0625, vp(16), None) == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_block_select_host_checks(lib):
+    vp = ctypes.c_void_p
+    f = lib.qsa_block_select                                          # prototypes set by the binding
+    assert lib.qsa_block_select_workspace_bytes(1616, 2, 1440, 16) > 1616 * 2 * 1440 * 4   # the score matrix
+
+    def call(**kw):
+        a = dict(q=vp(16), rows=4, H=2, kc=vp(16), npg=8, bt=vp(16), nr=1, mb=8, rr=vp(16), rt=vp(16), k=4,
+                 oi=vp(16), ov=vp(16), ws=vp(256), wsb=1 << 30)
+        a.update(kw)
+        return f(a["q"], a["rows"], a["H"], a["kc"], a["npg"], a["bt"], a["nr"], a["mb"], a["rr"], a["rt"], a["k"],
+                 a["oi"], a["ov"], a["ws"], a["wsb"], None)
+
+    assert call(rows=-1) == qsa.QSA_ERR_INVALID_ARG
+    assert call(k=-1) == qsa.QSA_ERR_INVALID_ARG
+    assert call(H=0) == qsa.QSA_ERR_INVALID_ARG
+    assert call(npg=0) == qsa.QSA_ERR_INVALID_ARG
+    assert call(mb=0) == qsa.QSA_ERR_INVALID_ARG
+    assert call(H=17) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(k=qsa.QSA_MAX_K + 1) == qsa.QSA_ERR_UNSUPPORTED
+    assert call(rows=0) == qsa.QSA_OK                                 # nothing to do
+    assert call(k=0) == qsa.QSA_OK
+    assert call(q=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(oi=None) == qsa.QSA_ERR_INVALID_ARG
+    assert call(q=vp(24)) == qsa.QSA_ERR_INVALID_ARG                  # 16-byte alignment
+    assert call(kc=vp(24)) == qsa.QSA_ERR_INVALID_ARG
+    assert call(rr=vp(18)) == qsa.QSA_ERR_INVALID_ARG                 # 4-byte alignment
+    assert call(ov=vp(18)) == qsa.QSA_ERR_INVALID_ARG
+    assert call() == qsa.QSA_ERR_NO_DEVICE
