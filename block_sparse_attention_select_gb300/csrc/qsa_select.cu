@@ -438,6 +438,30 @@ struct RowView {
     __device__ __forceinline__ float ld(int32_t i) const { return __ldcg(at(i)); }
 };
 
+// Calls f(i, key32 of element i) for i = threadIdx.x, ... over [0, n) of the
+// row, in some order.  A row whose base and tile stride are 16-byte multiples
+// is read four elements per load, four loads in flight per thread (a 128-float
+// tile holds whole groups of four); other rows element by element.
+template <typename F>
+__device__ __forceinline__ void for_each_key(const RowView row, int32_t n, F f)
+{
+    int32_t done = 0;
+    if ((reinterpret_cast<uintptr_t>(row.base) & 15u) == 0 && (row.tile_stride & 3) == 0) {
+        const int32_t n4 = n >> 2;
+#pragma unroll 4
+        for (int32_t v = threadIdx.x; v < n4; v += NT) {
+            const int32_t i = v << 2;
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(row.at(i)));
+            f(i, score_key(x.x));
+            f(i + 1, score_key(x.y));
+            f(i + 2, score_key(x.z));
+            f(i + 3, score_key(x.w));
+        }
+        done = n4 << 2;
+    }
+    for (int32_t i = done + threadIdx.x; i < n; i += NT) f(i, score_key(row.ld(i)));
+}
+
 // Streaming narrowing over a long row in global memory (fixed 11/11/10-bit
 // digits of key32): stops as soon as every element at or above the current
 // cut digit fits in shared memory (gathers them and returns their count), or
@@ -452,10 +476,11 @@ __device__ int32_t stream_narrow(SelShared &sh, const RowView row, int32_t n, ui
     uint32_t prefix = 0, pmask = 0, k_rem = k, above = 0;
     for (int lv = 0; lv < 3; ++lv) {
         clear_hist(sh);
-        for (int32_t i = threadIdx.x; i < n; i += NT) {
-            const uint32_t key = score_key(row.ld(i));
-            if ((key & pmask) == prefix) atomicAdd(&sh.hist[(key >> level_shift(lv)) & level_mask(lv)], 1u);
-        }
+        const int sft = level_shift(lv);
+        const uint32_t msk = level_mask(lv);
+        for_each_key(row, n, [&](int32_t, uint32_t key) {
+            if ((key & pmask) == prefix) atomicAdd(&sh.hist[(key >> sft) & msk], 1u);
+        });
         __syncthreads();
         find_cut(sh, k_rem);
         const uint32_t d = sh.cut_digit;
@@ -468,14 +493,13 @@ __device__ int32_t stream_narrow(SelShared &sh, const RowView row, int32_t n, ui
         if (gather && above + eq <= static_cast<uint32_t>(cap)) {
             if (threadIdx.x == 0) sh.count = 0;
             __syncthreads();
-            for (int32_t i = threadIdx.x; i < n; i += NT) {
-                const uint32_t key = score_key(row.ld(i));
+            for_each_key(row, n, [&](int32_t i, uint32_t key) {
                 if ((key & pmask) >= prefix) {
                     const uint32_t slot = atomicAdd(&sh.count, 1u);
                     keys[slot] = key;
                     inv[slot] = ~static_cast<uint32_t>(i);
                 }
-            }
+            });
             __syncthreads();
             return static_cast<int32_t>(sh.count);
         }
@@ -588,10 +612,10 @@ __device__ __forceinline__ void select_row(const SelectParams &p, int32_t r, boo
     }
     int32_t n;
     if (V <= smem_cap) {
-        for (int32_t i = threadIdx.x; i < V; i += NT) {
-            keys[i] = score_key(row.ld(i));
+        for_each_key(row, V, [&](int32_t i, uint32_t key) {
+            keys[i] = key;
             inv[i] = ~static_cast<uint32_t>(i);
-        }
+        });
         __syncthreads();
         n = V;
     } else {
