@@ -149,3 +149,38 @@ def test_block_scorer_bad_page_is_reported():
     _run(inp, block_table=bt)
     assert qsa.get_device_status() == qsa.QSA_ERR_BAD_PAGE
     assert qsa.get_device_status() == qsa.QSA_OK
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_scorer_random_shapes(seed):
+    # seeded random batches: 1-4 requests of 1-700 rows over 3-6,000-token
+    # contexts, 1, 3, 8 or 16 heads, k from 1 to 16; integer data, bit-exact
+    # on every row of a small batch, else on 60 rows that include both sides
+    # of the 128-row half and 256-row group boundaries; every row checked for
+    # distinct visible blocks in score order
+    rng = np.random.default_rng(900 + seed)
+    nreq = int(rng.integers(1, 5))
+    ctx = [int(c) for c in rng.integers(3, 6000, size=nreq)]
+    rows = [int(rng.integers(1, min(c, 700) + 1)) for c in ctx]
+    heads = int(rng.choice([1, 3, 8, 16]))
+    k = int(rng.integers(1, 17))
+    inp = W.make_block_scorer_inputs(f"rand{seed}", seed=seed, ctx_tokens=ctx, rows_per_req=rows, k=k,
+                                     heads=heads, dist="int")
+    gi, gv = _run(inp)
+    assert qsa.get_device_status() == qsa.QSA_OK
+    R = gi.shape[0]
+    nvis = np.minimum(inp.row_token.astype(np.int64) // 128 + 1, k)[:, None]
+    for h in range(heads):
+        sel, val = gi[:, h], gv[:, h].astype(np.float64)
+        n_ok = (sel >= 0).sum(axis=1)
+        assert np.all(n_ok == nvis[:, 0])
+        assert np.all(np.diff(np.where(sel >= 0, val, -3e38), axis=1) <= 0)     # padding: a finite floor
+    if R <= 120:
+        sample = list(range(R))
+    else:
+        edges = {0, 127, 128, 255, 256, 383, 384, 511, 512, R - 1}
+        sample = sorted({e for e in edges if e < R} | set(rng.choice(R, 60 - len(edges), replace=False).tolist()))
+    oi, ov = BS.select_blocks(inp.q[sample], inp.k_cache, inp.block_table, inp.row_req[sample],
+                              inp.row_token[sample], k)
+    np.testing.assert_array_equal(gi[sample], oi)
+    np.testing.assert_array_equal(gv[sample], ov.astype(np.float32))
