@@ -509,6 +509,76 @@ __device__ int32_t stream_narrow(SelShared &sh, const RowView row, int32_t n, ui
     return -1;
 }
 
+// A long row's top kk through a sampled threshold: the keys of every
+// SAMPLE_TILES-th 128-score tile are staged, T = the m-th largest of them
+// (m = w + 4 sqrt(w) + 8 with w = 1.5 kk n_s / V, the expected share of the
+// top kk in the sample plus a margin), and one pass over the row gathers every
+// key >= T.  When at least kk keys reach T, the kk-th largest key of the row
+// is >= T, so the gathered keys hold the row's top kk: the result is exact.
+// Returns their count, or -1 (nothing usable in keys / inv) when fewer than
+// kk or more than cap reach T, or the sample does not fit.
+constexpr int32_t SAMPLE_TILES = 16;
+
+__device__ int32_t sample_gather(SelShared &sh, const RowView row, int32_t V, int32_t kk, int32_t cap,
+                                 uint32_t *keys, uint32_t *inv)
+{
+    const int32_t tiles = (V + TILE_M - 1) / TILE_M;
+    const int32_t nst = (tiles + SAMPLE_TILES - 1) / SAMPLE_TILES;
+    const int32_t last = (nst - 1) * SAMPLE_TILES;
+    const int32_t n_s = (nst - 1) * TILE_M + min(TILE_M, V - last * TILE_M);
+    if (kk <= 0 || n_s > cap) return -1;                      // uniform
+    // sampled element i: tile (i / 128) * SAMPLE_TILES, slot i % 128
+    auto src = [&](int32_t i) { return ((i >> 7) * SAMPLE_TILES << 7) + (i & 127); };
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    if ((reinterpret_cast<uintptr_t>(row.base) & 15u) == 0 && (row.tile_stride & 3) == 0) {
+        for (int32_t v = threadIdx.x; v < (n_s >> 2); v += NT) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(row.at(src(v << 2))));
+            const uint32_t k4[4] = {score_key(x.x), score_key(x.y), score_key(x.z), score_key(x.w)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                keys[(v << 2) + j] = k4[j];
+                kmin = min(kmin, k4[j]);
+                kmax = max(kmax, k4[j]);
+            }
+        }
+        for (int32_t i = ((n_s >> 2) << 2) + threadIdx.x; i < n_s; i += NT) {
+            const uint32_t kv = score_key(row.ld(src(i)));
+            keys[i] = kv;
+            kmin = min(kmin, kv);
+            kmax = max(kmax, kv);
+        }
+    } else {
+        for (int32_t i = threadIdx.x; i < n_s; i += NT) {
+            const uint32_t kv = score_key(row.ld(src(i)));
+            keys[i] = kv;
+            kmin = min(kmin, kv);
+            kmax = max(kmax, kv);
+        }
+    }
+    block_minmax(sh, kmin, kmax, kmin, kmax);                 // its barriers also publish keys[]
+    const float w = 1.5f * static_cast<float>(kk) * static_cast<float>(n_s) / static_cast<float>(V);
+    const uint32_t m = static_cast<uint32_t>(min(static_cast<float>(n_s), ceilf(w + 4.0f * sqrtf(w)) + 8.0f));
+    uint32_t k_rem, eq;
+    const uint32_t T = kth_largest(sh, n_s, m, kmin, kmax, static_cast<uint32_t>(n_s),
+                                   [&](int32_t i) { return keys[i]; }, [&](int32_t) { return true; }, k_rem, eq);
+    if (threadIdx.x == 0) sh.count = 0;
+    __syncthreads();                                          // the sample is dead: keys[] is reused
+    for_each_key(row, V, [&](int32_t i, uint32_t key) {
+        if (key >= T) {
+            const uint32_t slot = atomicAdd(&sh.count, 1u);
+            if (slot < static_cast<uint32_t>(cap)) {
+                keys[slot] = key;
+                inv[slot] = ~static_cast<uint32_t>(i);
+            }
+        }
+    });
+    __syncthreads();
+    const uint32_t cnt = sh.count;
+    __syncthreads();                                          // sh.count is reused by the caller
+    if (cnt < static_cast<uint32_t>(kk) || cnt > static_cast<uint32_t>(cap)) return -1;
+    return static_cast<int32_t>(cnt);
+}
+
 // Everything above the exact cut key T, then the k_rem lowest positions that
 // hold T, in position order.
 __device__ int32_t gather_cut_in_order(SelShared &sh, const RowView row, int32_t n,
@@ -619,9 +689,12 @@ __device__ __forceinline__ void select_row(const SelectParams &p, int32_t r, boo
         __syncthreads();
         n = V;
     } else {
-        uint32_t T, k_rem;
-        n = stream_narrow(sh, row, V, static_cast<uint32_t>(kk_target), smem_cap, keys, inv, T, k_rem, true);
-        if (n < 0) n = gather_cut_in_order(sh, row, V, T, k_rem, keys, inv);
+        n = sample_gather(sh, row, V, kk_target, smem_cap, keys, inv);
+        if (n < 0) {
+            uint32_t T, k_rem;
+            n = stream_narrow(sh, row, V, static_cast<uint32_t>(kk_target), smem_cap, keys, inv, T, k_rem, true);
+            if (n < 0) n = gather_cut_in_order(sh, row, V, T, k_rem, keys, inv);
+        }
     }
     const int32_t kk = min(p.k, n);
     const uint64_t *result = out64;
