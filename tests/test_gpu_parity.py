@@ -251,6 +251,9 @@ def test_filter_path_at_max_k(ctx):
 # ---------------------------------------------------- selector on its own ----
 
 @pytest.mark.parametrize("n,k,kind", [(5000, 700, "gauss"), (30000, 2048, "gauss"),
+                                      # long rows through the sampled threshold: small k, and
+                                      # a gathered set of three values (the order by position)
+                                      (50000, 100, "gauss"), (20000, 1000, "few"),
                                       (60000, 2048, "ties"), (60000, 4000, "few"),
                                       (9000, 8192, "ties"), (100, 64, "ties"),
                                       # k <= 16: the warp-per-row selector
