@@ -38,8 +38,8 @@ __device__ __forceinline__ float4 half4_to_float4(uint2 u)
 
 // W: the pooling window (4 or 8 tokens).  Each warp takes KPW keys, i_base
 // and i_base + PROD_WARPS * k, and requests every load of all of them before
-// it computes any: the bytes a warp keeps in flight, not the HBM rate, bound
-// this kernel.
+// it computes any: one memory round trip per warp.  (A persistent variant
+// that kept three rounds of loads in flight per warp measured slower.)
 template <int W>
 __global__ void __launch_bounds__(PROD_WARPS * 32, 4)
 produce_kernel(const ProduceParams p)
