@@ -254,6 +254,9 @@ def test_filter_path_at_max_k(ctx):
                                       # long rows through the sampled threshold: small k, and
                                       # a gathered set of three values (the order by position)
                                       (50000, 100, "gauss"), (20000, 1000, "few"),
+                                      # just past the staging area, and a gathered set too
+                                      # large for it (the digit passes take over)
+                                      (8200, 4096, "gauss"), (12000, 7000, "gauss"),
                                       (60000, 2048, "ties"), (60000, 4000, "few"),
                                       (9000, 8192, "ties"), (100, 64, "ties"),
                                       # k <= 16: the warp-per-row selector
