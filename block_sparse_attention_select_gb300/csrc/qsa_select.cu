@@ -748,10 +748,11 @@ select_kernel(const SelectParams p)
 constexpr int WK = 16;
 constexpr int WT_CAP = 128;             // elements >= T the warp buffer holds
 
-__device__ __forceinline__ uint64_t dense_key(const float *row, int32_t j)
+__device__ __forceinline__ uint64_t full_key(float f, int32_t j)
 {
-    return (static_cast<uint64_t>(score_key(__ldg(row + j))) << 32) | ~static_cast<uint32_t>(j);
+    return (static_cast<uint64_t>(score_key(f)) << 32) | ~static_cast<uint32_t>(j);
 }
+__device__ __forceinline__ uint64_t dense_key(const float *row, int32_t j) { return full_key(__ldg(row + j), j); }
 
 template <int K>
 __global__ void __launch_bounds__(256)
@@ -778,9 +779,23 @@ warp_topk_kernel(const SelectParams p)
     const int32_t kk = min(p.k, V);
     uint64_t *buf = wbuf[wid];
 
+    // a 16-byte aligned row is read four elements per load (lane l takes
+    // elements 4 (l + 32 i) .. + 3), the rest of it element by element
+    const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+    const int32_t V4 = vec ? V >> 2 : 0;
+    const float4 *row4 = reinterpret_cast<const float4 *>(row);
+
     // pass 1: the lane's largest key (0, below every real key, for none)
     uint64_t mx = 0ull;
-    for (int32_t j = lane; j < V; j += 32) {
+#pragma unroll 4
+    for (int32_t v = lane; v < V4; v += 32) {
+        const float4 x = __ldg(row4 + v);
+        const int32_t j = v << 2;
+        const uint64_t a = max(full_key(x.x, j), full_key(x.y, j + 1));
+        const uint64_t b = max(full_key(x.z, j + 2), full_key(x.w, j + 3));
+        mx = max(mx, max(a, b));
+    }
+    for (int32_t j = 4 * V4 + lane; j < V; j += 32) {
         const uint64_t key = dense_key(row, j);
         mx = key > mx ? key : mx;
     }
@@ -790,10 +805,37 @@ warp_topk_kernel(const SelectParams p)
     __syncwarp();
     const uint64_t T = buf[K - 1];
     __syncwarp();
-    // pass 2: the elements >= T, in index order, into the buffer
+    // pass 2: the elements >= T into the buffer (in any order: the keys are
+    // distinct and sorted below)
     const uint32_t lt = (1u << lane) - 1u;
     uint32_t cnt = 0;
-    for (int32_t j0 = 0; j0 < V; j0 += 32) {
+    for (int32_t v0 = 0; v0 < V4; v0 += 32) {
+        const int32_t v = v0 + lane;
+        uint64_t key[4] = {0ull, 0ull, 0ull, 0ull};
+        if (v < V4) {
+            const float4 x = __ldg(row4 + v);
+            key[0] = full_key(x.x, v << 2);
+            key[1] = full_key(x.y, (v << 2) + 1);
+            key[2] = full_key(x.z, (v << 2) + 2);
+            key[3] = full_key(x.w, (v << 2) + 3);
+        }
+        uint32_t at = cnt, tot = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, v < V4 && key[e] >= T);
+            at += static_cast<uint32_t>(__popc(bal & lt));
+            tot += static_cast<uint32_t>(__popc(bal));
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (v < V4 && key[e] >= T) {
+                if (at < static_cast<uint32_t>(WT_CAP)) buf[at] = key[e];
+                ++at;
+            }
+        }
+        cnt += tot;
+    }
+    for (int32_t j0 = 4 * V4; j0 < V; j0 += 32) {
         const int32_t j = j0 + lane;
         const uint64_t key = j < V ? dense_key(row, j) : 0ull;
         const bool take = j < V && key >= T;
