@@ -66,13 +66,17 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     if (tid == 0) { carry_req = -2; carry_run = 0; carry_gid = 0; }
     __syncthreads();
 
-    // Phase 1: sanitise rows, find group starts.
+    // Phase 1: sanitise rows, find group starts.  Each thread's row of the
+    // next round is loaded while this round is scanned.
+    int32_t nx_req = 0, nx_vis = 0;
+    if (tid < R) { nx_req = row_req[tid]; nx_vis = row_visible[tid]; }
     for (int32_t base = 0; base < R; base += PLAN_THREADS) {
         const int32_t r = base + tid;
+        int32_t b = nx_req;
+        int64_t v = nx_vis;
+        if (r + PLAN_THREADS < R) { nx_req = row_req[r + PLAN_THREADS]; nx_vis = row_visible[r + PLAN_THREADS]; }
         int32_t req = -1;
         if (r < R) {
-            int32_t b = row_req[r];
-            int64_t v = row_visible[r];
             bool bad = false;
             if (b < 0 || b >= num_reqs) { b = -1; v = 0; bad = true; }
             if (v < 0) { v = 0; bad = true; }
