@@ -66,45 +66,106 @@ plan_kernel(const int32_t *__restrict__ row_req, const int32_t *__restrict__ row
     if (tid == 0) { carry_req = -2; carry_run = 0; carry_gid = 0; }
     __syncthreads();
 
-    // Phase 1: sanitise rows, find group starts.  Each thread's row of the
-    // next round is loaded while this round is scanned.
-    int32_t nx_req = 0, nx_vis = 0;
-    if (tid < R) { nx_req = row_req[tid]; nx_vis = row_visible[tid]; }
-    for (int32_t base = 0; base < R; base += PLAN_THREADS) {
-        const int32_t r = base + tid;
-        int32_t b = nx_req;
-        int64_t v = nx_vis;
-        if (r + PLAN_THREADS < R) { nx_req = row_req[r + PLAN_THREADS]; nx_vis = row_visible[r + PLAN_THREADS]; }
-        int32_t req = -1;
-        if (r < R) {
-            bool bad = false;
-            if (b < 0 || b >= num_reqs) { b = -1; v = 0; bad = true; }
-            if (v < 0) { v = 0; bad = true; }
-            if (v > max_len) { v = max_len; bad = true; }
-            if (bad) record_error(status, ST_BAD_ROW);
-            row_vis[r] = static_cast<int32_t>(v);
-            if (r < PLAN_SMEM_ROWS) s_vis[r] = static_cast<int32_t>(v);
-            req = b;
+    // Phase 1: sanitise rows, find group starts.  A thread takes RPT
+    // consecutive rows per round (a run of rows of one request starts where
+    // the request changes, a group every G rows of a run); its rows of the
+    // next round are loaded while this round is scanned.
+    constexpr int RPT = 4;
+    constexpr int32_t ROUND = PLAN_THREADS * RPT;
+    int32_t nx_req[RPT], nx_vis[RPT];
+#pragma unroll
+    for (int q = 0; q < RPT; ++q) {
+        const int32_t r = tid * RPT + q;
+        nx_req[q] = r < R ? row_req[r] : 0;
+        nx_vis[q] = r < R ? row_visible[r] : 0;
+    }
+    for (int32_t base = 0; base < R; base += ROUND) {
+        const int32_t r0 = base + tid * RPT;       // this thread's first row
+        int32_t req[RPT];
+        int64_t vv[RPT];
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            req[q] = nx_req[q];
+            vv[q] = nx_vis[q];
+            const int32_t rn = r0 + ROUND + q;
+            if (rn < R) { nx_req[q] = row_req[rn]; nx_vis[q] = row_visible[rn]; }
         }
-        s_req[tid] = req;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const int32_t r = r0 + q;
+            if (r < R) {
+                int32_t b = req[q];
+                int64_t v = vv[q];
+                bool bad = false;
+                if (b < 0 || b >= num_reqs) { b = -1; v = 0; bad = true; }
+                if (v < 0) { v = 0; bad = true; }
+                if (v > max_len) { v = max_len; bad = true; }
+                if (bad) record_error(status, ST_BAD_ROW);
+                row_vis[r] = static_cast<int32_t>(v);
+                if (r < PLAN_SMEM_ROWS) s_vis[r] = static_cast<int32_t>(v);
+                req[q] = b;
+            } else {
+                req[q] = -1;
+            }
+        }
+        s_req[tid] = req[RPT - 1];
         __syncthreads();
-        const int32_t prev = tid > 0 ? s_req[tid - 1] : carry_req;
-        const bool begin = r < R && (r == 0 || req != prev);
-        int32_t rs = block_incl_scan(begin ? r : -1, wbuf, OpMax(), -1);
+        int32_t prev = tid > 0 ? s_req[tid - 1] : carry_req;
+        uint32_t beg = 0;                          // bit q: row r0 + q starts a run
+        int32_t run_last = -1;                     // this thread's latest run start
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const int32_t r = r0 + q;
+            if (r < R && (r == 0 || req[q] != prev)) {
+                beg |= 1u << q;
+                run_last = r;
+            }
+            prev = req[q];
+        }
+        // the run start in effect before this thread's rows: the latest one
+        // of the threads before it, else the previous round's
+        const int32_t run_incl = block_incl_scan(run_last, wbuf, OpMax(), -1);
+        s_req[tid] = run_incl;                     // every read of s_req above is done (the scan's barriers)
+        __syncthreads();
+        int32_t rs = tid > 0 ? s_req[tid - 1] : -1;
         if (rs < 0) rs = carry_run;
-        const bool gbegin = r < R && ((r - rs) % G == 0);
-        const int32_t incl = block_incl_scan(gbegin ? 1 : 0, wbuf, OpAdd(), 0);
-        const int32_t gid = carry_gid + incl - 1;
-        if (gbegin) {
-            groups[gid].row0 = r;
-            groups[gid].req = req;
-            if (gid < PLAN_SMEM_GROUPS) s_row0[gid] = r;
+        uint32_t gb = 0;                           // bit q: row r0 + q starts a group
+        int32_t gcnt = 0, rq = rs;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            const int32_t r = r0 + q;
+            if (beg & (1u << q)) rq = r;
+            if (r < R && (r - rq) % G == 0) {
+                gb |= 1u << q;
+                ++gcnt;
+            }
+        }
+        const int32_t g_incl = block_incl_scan(gcnt, wbuf, OpAdd(), 0);
+        int32_t gid = carry_gid + g_incl - gcnt;
+#pragma unroll
+        for (int q = 0; q < RPT; ++q) {
+            if (gb & (1u << q)) {
+                const int32_t r = r0 + q;
+                groups[gid].row0 = r;
+                groups[gid].req = req[q];
+                if (gid < PLAN_SMEM_GROUPS) s_row0[gid] = r;
+                ++gid;
+            }
         }
         __syncthreads();
-        if (tid == min(PLAN_THREADS - 1, R - 1 - base)) {
-            carry_req = req;
-            carry_run = rs;
-            carry_gid = gid + 1;
+        // carries from the thread holding the round's last row
+        const int32_t last = min(R, base + ROUND) - 1;
+        if (tid == (last - base) / RPT) {
+            const int ql = (last - base) % RPT;
+            int32_t rl = rs, cr = req[0];
+#pragma unroll
+            for (int q = 0; q < RPT; ++q) {
+                if (q <= ql && (beg & (1u << q))) rl = r0 + q;
+                if (q == ql) cr = req[q];
+            }
+            carry_req = cr;
+            carry_run = rl;
+            carry_gid = gid;
         }
         __syncthreads();
     }
