@@ -283,6 +283,35 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def capture_step(args, qsa, step, outputs):
+    """The timed loop replays one call captured as a CUDA graph: the same
+    launches on the same resident inputs, one graph launch of host work per
+    step, so the host never leaves the GPU idle inside a timed step.  A capture
+    that fails, or a replay whose outputs differ from an eager call's, falls
+    back to eager calls.  Returns (launch mode, step function)."""
+    import torch
+
+    if args.eager:
+        return "eager", step
+    ref = [t.clone() for t in outputs]                    # the last eager call's results
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for t in outputs:
+            t.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        ok = qsa.get_device_status() == qsa.QSA_OK and all(torch.equal(a, b) for a, b in zip(outputs, ref))
+    except Exception as e:                                # noqa: BLE001 (any capture failure: eager)
+        torch.cuda.synchronize()
+        qsa.get_device_status()
+        return f"eager (graph capture failed: {type(e).__name__})", step
+    if not ok:
+        return "eager (graph replay differed)", step
+    return "cuda_graph", graph.replay
+
+
 def run_ours(args, ws, rank, local):
     import torch
 
@@ -307,7 +336,8 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        qsa.select_paged_tokens(q, w, keys, rr, rv, wl.k, out_idx, out_val, wsb, stream)
+        # the stream current at the call: the capture stream while a graph is captured
+        qsa.select_paged_tokens(q, w, keys, rr, rv, wl.k, out_idx, out_val, wsb, torch.cuda.current_stream())
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -315,6 +345,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     assert qsa.get_device_status() == qsa.QSA_OK
     launches_per_step = qsa.last_launch_count()
+    launch, timed_step = capture_step(args, qsa, step, (out_idx, out_val))
 
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
@@ -327,7 +358,7 @@ def run_ours(args, ws, rank, local):
     for a, b in ev:
         flush.zero_()                                     # L2 flushed between steps
         a.record(stream)
-        step()
+        timed_step()
         b.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
@@ -402,7 +433,7 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": wl.name, "rows": wl.rows, "positions_max": int(wl.row_visible.max()),
                    "visible_pairs": alg["pairs"], "k": wl.k, "heads": wl.heads, "head_dim": 128,
                    "page_positions": int(wl.k_cache.shape[1]), "path": args.path,
-                   "l2": "flushed between steps (512 MiB write)",
+                   "l2": "flushed between steps (512 MiB write)", "launch": launch,
                    "accumulate": "f32", "median_ms": statistics.median(step_ms)},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": roof_traffic, "kernel": dom_name,
@@ -866,6 +897,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(W.CONFIGS), default="bench")
     ap.add_argument("--path", choices=["auto", "dense", "filter"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager calls instead of a captured graph of one call")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--op", choices=["select", "produce", "attend", "blocks"], default="select",
                     help="select: the indexer step (default); produce: the index-key producer; "
